@@ -1,0 +1,433 @@
+/*
+ * Float64 CPU oracle for the speculative-decoding verification step.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code, header, table or
+ * helper with the CUDA path; it is a plain sequential restatement of the method
+ * written for a reader to check against the pages by eye.  Status: pinned (see
+ * tests/test_oracle_pins.py and tests/test_oracle_law.py).
+ *
+ * Sources (page title, section):
+ *   [P1] "Speculative Decoding" (atonlee.tistory.com/330): ch.2 (one
+ *        propose/verify round, cut at the first rejection, k accepted + 1),
+ *        ch.3 (the acceptance rule r < min(1, p/q), residual
+ *        norm(max(0, p - q)), greedy rule at temperature 0).
+ *   [P2] "Speculative Decoding으로 LLM 추론 속도 높이기" (donmain.dev), section
+ *        "품질은 rejection sampling이 지킨다" (worked example and the rule).
+ *   [P3] "Fast Inference from Transformers via Speculative Decoding" notes
+ *        (obsidian-dorae222.pages.dev), method details, steps 2 and 3 (gamma+1
+ *        target distributions, accept probability, residual, bonus token).
+ *   [P4] "투기적 디코딩 — 초안 모델을 무엇으로 세울 것인가" (ailab.paldyn.com),
+ *        section on why the output does not change (rule, greedy argmax).
+ *
+ * Readings where the pages leave a step open (each also listed in the design doc):
+ *   - p and q are softmax(logits / T) with the sequence's own T; "/T" is a
+ *     true float64 division (the pages only say that a low T sharpens both).
+ *   - The accept test is evaluated as  r * q(x) < p(x), which equals the
+ *     printed strict test r < min(1, p(x)/q(x)) for r in [0,1) and q(x) > 0,
+ *     and accepts a zero-q draft exactly when p(x) > 0.
+ *   - T == 0 is greedy: accept iff the draft equals argmax of the raw target
+ *     logits, the lowest id winning ties; on rejection emit that argmax; when
+ *     every draft matches, emit the argmax of the bonus row.  No draft row and
+ *     no uniform is read.
+ *   - The final sample uses the fixed last uniform column uniforms[b, gmax],
+ *     also for sequences with fewer drafts.  Inverse CDF: the smallest j with
+ *     u*S < C_j, C_j the inclusive running sum of the weights in index order,
+ *     S their total; if rounding leaves no such j, the last j with weight > 0.
+ *   - A rejected row whose residual mass is not above 1e-300 (unreachable in
+ *     exact arithmetic) samples from p of that row instead.
+ *   - A sequence with num_draft outside [0, gmax], a temperature that is
+ *     negative, NaN, infinite or positive-but-below FLT_MIN, a drafted id
+ *     outside [0, V) at a position it uses, or a sampled row it uses whose
+ *     logits have no finite softmax normaliser (all -inf, any +inf or NaN) is
+ *     invalid: it emits -1 everywhere, 0 accepted, and sets a status bit.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+#define ORACLE_BAD_TOKEN 1
+#define ORACLE_BAD_TEMPERATURE 2
+#define ORACLE_BAD_NUM_DRAFT 4
+#define ORACLE_BAD_LOGITS 8
+
+/* One stored logit widened exactly to float64.  bfloat16 is the upper half
+ * of a float32, so the widening shifts the 16 stored bits up. */
+static double logit_at(const void *base, int dtype, size_t idx)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Normaliser of softmax(l / T) over one row:  m = max_j l_j / T and
+ * z = sum_j exp(l_j / T - m), so that p_j = exp(l_j / T - m) / z. */
+typedef struct {
+    double m;
+    double z;
+} softmax_norm;
+
+static softmax_norm row_softmax_norm(const void *base, int dtype, size_t row_off, int V, double T)
+{
+    softmax_norm s;
+    s.m = -INFINITY;
+    for (int j = 0; j < V; ++j) {
+        double zj = logit_at(base, dtype, row_off + (size_t)j) / T;
+        if (zj > s.m)
+            s.m = zj;
+    }
+    s.z = 0.0;
+    if (!isfinite(s.m)) {
+        s.z = NAN; /* no finite maximum: the row defines no distribution */
+        return s;
+    }
+    for (int j = 0; j < V; ++j)
+        s.z += exp(logit_at(base, dtype, row_off + (size_t)j) / T - s.m);
+    return s;
+}
+
+static int norm_is_valid(softmax_norm s)
+{
+    return isfinite(s.m) && isfinite(s.z) && s.z > 0.0;
+}
+
+/* p_j of one row, given its normaliser. */
+static double row_prob(const void *base, int dtype, size_t row_off, int j, double T, softmax_norm s)
+{
+    return exp(logit_at(base, dtype, row_off + (size_t)j) / T - s.m) / s.z;
+}
+
+/* Greedy decision value: index of the largest raw logit, lowest index on ties. */
+static int row_argmax(const void *base, int dtype, size_t row_off, int V)
+{
+    int best = 0;
+    double bv = logit_at(base, dtype, row_off);
+    for (int j = 1; j < V; ++j) {
+        double v = logit_at(base, dtype, row_off + (size_t)j);
+        if (v > bv) {
+            bv = v;
+            best = j;
+        }
+    }
+    return best;
+}
+
+typedef struct {
+    const void *target;
+    const void *draft;
+    int dtype;
+    const int32_t *tokens;
+    const int32_t *num_draft;
+    const float *uniforms;
+    const float *temperature;
+    int B, gmax, V;
+    int32_t *out_tokens;
+    int32_t *out_num_accepted;
+    /* optional diagnostics (may be NULL) */
+    double *p_hat;       /* [B, gmax]  p_i(x_i) for every i < g (sampled seqs) */
+    double *q_hat;       /* [B, gmax]  q_i(x_i) */
+    double *logz_t;      /* [B, gmax+1] m + log z of target rows i <= g */
+    double *logz_d;      /* [B, gmax]   of draft rows i < g */
+    double *resid_mass;  /* [B] S of the decided row */
+    double *acc_margin;  /* [B, gmax]   |r_i - p_i(x)/q_i(x)| at evaluated positions */
+    double *samp_margin; /* [B] distance of u to the nearest CDF boundary of the pick */
+    int32_t *seq_status; /* [B] status bits of each sequence */
+} oracle_args;
+
+static void write_invalid(const oracle_args *a, int b, int bits)
+{
+    for (int i = 0; i <= a->gmax; ++i)
+        a->out_tokens[(size_t)b * (a->gmax + 1) + i] = -1;
+    a->out_num_accepted[b] = 0;
+    if (a->seq_status)
+        a->seq_status[b] = bits;
+}
+
+static int temperature_is_valid(float T)
+{
+    if (isnan(T) || isinf(T) || T < 0.0f)
+        return 0;
+    if (T > 0.0f && T < FLT_MIN)
+        return 0;
+    return 1;
+}
+
+/* Diagnostics only: softmax values at every position of a sampled sequence,
+ * independent of where the round stops.  Not part of the decision path. */
+static void fill_diagnostics(const oracle_args *a, int b, int g, double T)
+{
+    const int gmax = a->gmax, V = a->V;
+    for (int i = 0; i <= g; ++i) {
+        size_t toff = ((size_t)b * (gmax + 1) + i) * (size_t)V;
+        softmax_norm st = row_softmax_norm(a->target, a->dtype, toff, V, T);
+        if (a->logz_t)
+            a->logz_t[(size_t)b * (gmax + 1) + i] = st.m + log(st.z);
+        if (i == g)
+            break;
+        size_t doff = ((size_t)b * gmax + i) * (size_t)V;
+        softmax_norm sd = row_softmax_norm(a->draft, a->dtype, doff, V, T);
+        if (a->logz_d)
+            a->logz_d[(size_t)b * gmax + i] = sd.m + log(sd.z);
+        int x = a->tokens[(size_t)b * gmax + i];
+        if (a->p_hat)
+            a->p_hat[(size_t)b * gmax + i] = row_prob(a->target, a->dtype, toff, x, T, st);
+        if (a->q_hat)
+            a->q_hat[(size_t)b * gmax + i] = row_prob(a->draft, a->dtype, doff, x, T, sd);
+    }
+}
+
+/* Sample from the weights w_j of one decided row by inverse CDF with the
+ * uniform u ([P1] ch.3 step 3, [P3] step 3).  'rejected' selects the residual
+ * max(0, p - q) of row n, otherwise the target distribution of row n (the
+ * bonus row when every draft was accepted). */
+static int sample_decided_row(const oracle_args *a, int b, int n, int rejected, double T, double u,
+                              softmax_norm st, softmax_norm sd, double *mass_out, double *margin_out)
+{
+    const int gmax = a->gmax, V = a->V;
+    size_t toff = ((size_t)b * (gmax + 1) + n) * (size_t)V;
+    size_t doff = ((size_t)b * gmax + n) * (size_t)V;
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!w)
+        return -1;
+    double S = 0.0;
+    for (int j = 0; j < V; ++j) {
+        double pj = row_prob(a->target, a->dtype, toff, j, T, st);
+        double wj = pj;
+        if (rejected) {
+            double qj = row_prob(a->draft, a->dtype, doff, j, T, sd);
+            wj = pj - qj > 0.0 ? pj - qj : 0.0;
+        }
+        w[j] = wj;
+        S += wj;
+    }
+    if (!(S > 1e-300)) {
+        /* degenerate residual: fall back to p of the same row */
+        S = 0.0;
+        for (int j = 0; j < V; ++j) {
+            w[j] = row_prob(a->target, a->dtype, toff, j, T, st);
+            S += w[j];
+        }
+    }
+    *mass_out = S;
+    double thr = u * S;
+    double C = 0.0, Cprev = 0.0;
+    int pick = -1;
+    for (int j = 0; j < V; ++j) {
+        Cprev = C;
+        C += w[j];
+        if (thr < C) {
+            pick = j;
+            break;
+        }
+    }
+    if (pick < 0) {
+        for (int j = V - 1; j >= 0; --j)
+            if (w[j] > 0.0) {
+                pick = j;
+                break;
+            }
+        *margin_out = 0.0;
+    } else {
+        double lo = u - Cprev / S, hi = C / S - u;
+        *margin_out = lo < hi ? lo : hi;
+    }
+    free(w);
+    return pick;
+}
+
+/* One sequence of the round, in the pages' order. */
+static void verify_one(const oracle_args *a, int b)
+{
+    const int gmax = a->gmax, V = a->V;
+    int32_t *out = a->out_tokens + (size_t)b * (gmax + 1);
+    const int32_t *x = a->tokens + (size_t)b * gmax;
+    const float *r = a->uniforms + (size_t)b * (gmax + 1);
+    int g = a->num_draft[b];
+    float Tf = a->temperature[b];
+
+    for (int i = 0; i < gmax; ++i) {
+        if (a->acc_margin)
+            a->acc_margin[(size_t)b * gmax + i] = NAN;
+        if (a->p_hat)
+            a->p_hat[(size_t)b * gmax + i] = NAN;
+        if (a->q_hat)
+            a->q_hat[(size_t)b * gmax + i] = NAN;
+        if (a->logz_d)
+            a->logz_d[(size_t)b * gmax + i] = NAN;
+    }
+    for (int i = 0; i <= gmax; ++i)
+        if (a->logz_t)
+            a->logz_t[(size_t)b * (gmax + 1) + i] = NAN;
+    if (a->resid_mass)
+        a->resid_mass[b] = NAN;
+    if (a->samp_margin)
+        a->samp_margin[b] = NAN;
+    if (a->seq_status)
+        a->seq_status[b] = 0;
+
+    if (g < 0 || g > gmax) {
+        write_invalid(a, b, ORACLE_BAD_NUM_DRAFT);
+        return;
+    }
+    int bits = 0;
+    if (!temperature_is_valid(Tf))
+        bits |= ORACLE_BAD_TEMPERATURE;
+    for (int i = 0; i < g; ++i)
+        if (x[i] < 0 || x[i] >= V)
+            bits |= ORACLE_BAD_TOKEN;
+    if (bits) {
+        write_invalid(a, b, bits);
+        return;
+    }
+
+    int n = g;
+    if (Tf == 0.0f) {
+        /* Greedy ([P1] ch.3, [P2], [P4]): accept while the draft equals the
+         * target argmax; the first mismatch is replaced by that argmax. */
+        int emit = -1;
+        for (int i = 0; i < g; ++i) {
+            int am = row_argmax(a->target, a->dtype, ((size_t)b * (gmax + 1) + i) * (size_t)V, V);
+            if (x[i] != am) {
+                n = i;
+                emit = am;
+                break;
+            }
+        }
+        if (emit < 0)
+            emit = row_argmax(a->target, a->dtype, ((size_t)b * (gmax + 1) + g) * (size_t)V, V);
+        for (int i = 0; i < n; ++i)
+            out[i] = x[i];
+        out[n] = emit;
+        for (int i = n + 1; i <= gmax; ++i)
+            out[i] = -1;
+        a->out_num_accepted[b] = n;
+        return;
+    }
+
+    const double T = (double)Tf;
+    if (a->p_hat || a->q_hat || a->logz_t || a->logz_d)
+        fill_diagnostics(a, b, g, T);
+
+    /* Sampled: test drafts in order; stop at the first rejection
+     * ([P1] ch.2-3, [P3] step 3). */
+    int rejected = 0;
+    softmax_norm st_dec, sd_dec;
+    sd_dec.m = NAN;
+    sd_dec.z = NAN;
+    for (int i = 0; i < g; ++i) {
+        size_t toff = ((size_t)b * (gmax + 1) + i) * (size_t)V;
+        size_t doff = ((size_t)b * gmax + i) * (size_t)V;
+        softmax_norm st = row_softmax_norm(a->target, a->dtype, toff, V, T);
+        softmax_norm sd = row_softmax_norm(a->draft, a->dtype, doff, V, T);
+        if (!norm_is_valid(st) || !norm_is_valid(sd)) {
+            write_invalid(a, b, ORACLE_BAD_LOGITS);
+            return;
+        }
+        double p = row_prob(a->target, a->dtype, toff, x[i], T, st);
+        double q = row_prob(a->draft, a->dtype, doff, x[i], T, sd);
+        double ri = (double)r[i];
+        if (a->acc_margin)
+            a->acc_margin[(size_t)b * gmax + i] = q > 0.0 ? fabs(ri - p / q) : INFINITY;
+        if (!(ri * q < p)) {
+            n = i;
+            rejected = 1;
+            st_dec = st;
+            sd_dec = sd;
+            break;
+        }
+    }
+    if (!rejected) {
+        size_t toff = ((size_t)b * (gmax + 1) + g) * (size_t)V;
+        st_dec = row_softmax_norm(a->target, a->dtype, toff, V, T);
+        if (!norm_is_valid(st_dec)) {
+            write_invalid(a, b, ORACLE_BAD_LOGITS);
+            return;
+        }
+    }
+    double mass = NAN, margin = NAN;
+    int y = sample_decided_row(a, b, n, rejected, T, (double)r[gmax], st_dec, sd_dec, &mass, &margin);
+    if (a->resid_mass)
+        a->resid_mass[b] = mass;
+    if (a->samp_margin)
+        a->samp_margin[b] = margin;
+    for (int i = 0; i < n; ++i)
+        out[i] = x[i];
+    out[n] = y;
+    for (int i = n + 1; i <= gmax; ++i)
+        out[i] = -1;
+    a->out_num_accepted[b] = n;
+}
+
+typedef struct {
+    const oracle_args *a;
+    int b0, b1;
+} oracle_slice;
+
+static void *run_slice(void *p)
+{
+    const oracle_slice *s = (const oracle_slice *)p;
+    for (int b = s->b0; b < s->b1; ++b)
+        verify_one(s->a, b);
+    return NULL;
+}
+
+/* Entry point.  All pointers are host memory.  Returns 0, or -1 on a bad
+ * argument.  Sequences are independent; nthreads > 1 splits them over POSIX
+ * threads in contiguous ranges (results do not depend on nthreads). */
+int oracle_verify(const void *target, const void *draft, int dtype, const int32_t *tokens,
+                  const int32_t *num_draft, const float *uniforms, const float *temperature, int B,
+                  int gmax, int V, int32_t *out_tokens, int32_t *out_num_accepted, double *p_hat,
+                  double *q_hat, double *logz_t, double *logz_d, double *resid_mass,
+                  double *acc_margin, double *samp_margin, int32_t *seq_status, int nthreads)
+{
+    if (B < 0 || gmax < 0 || V < 1 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16))
+        return -1;
+    if (B == 0)
+        return 0;
+    if (!target || !draft || !tokens || !num_draft || !uniforms || !temperature || !out_tokens ||
+        !out_num_accepted)
+        return -1;
+    oracle_args a = {target, draft, dtype, tokens, num_draft, uniforms, temperature, B, gmax, V,
+                     out_tokens, out_num_accepted, p_hat, q_hat, logz_t, logz_d, resid_mass,
+                     acc_margin, samp_margin, seq_status};
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > B)
+        nthreads = B;
+    if (nthreads == 1) {
+        for (int b = 0; b < B; ++b)
+            verify_one(&a, b);
+        return 0;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    oracle_slice *sl = (oracle_slice *)malloc(sizeof(oracle_slice) * (size_t)nthreads);
+    if (!th || !sl) {
+        free(th);
+        free(sl);
+        return -1;
+    }
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        sl[t].a = &a;
+        sl[t].b0 = (int)((long long)B * t / nthreads);
+        sl[t].b1 = (int)((long long)B * (t + 1) / nthreads);
+        if (pthread_create(&th[started], NULL, run_slice, &sl[t]) == 0)
+            ++started;
+        else
+            run_slice(&sl[t]); /* could not start a thread: do the slice here */
+    }
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(sl);
+    return 0;
+}

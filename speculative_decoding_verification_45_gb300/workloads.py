@@ -1,0 +1,370 @@
+"""Seeded synthetic inputs for the speculative-decoding verification step.
+
+This module only builds inputs: target logits, draft logits, drafted tokens,
+per-position uniforms and per-sequence temperatures.  It holds none of the
+verification arithmetic (no softmax, no accept test, no residual sampling), so
+both the CUDA path and the float64 oracle can be fed from it without sharing
+any of the method's code.
+
+Drafted tokens stand in for the proposer's output ("Fast Inference from
+Transformers via Speculative Decoding" notes, method details, step 1: each
+draft token is drawn from the draft distribution q at its position).  They are
+drawn with the Gumbel-max trick, x = argmax_j (d_j / T + G_j) with G_j i.i.d.
+standard Gumbel, which samples exactly from softmax(d / T) without forming it.
+For greedy sequences (T = 0) the draft proposes argmax_j d_j.
+
+All logits are drawn in float64 and rounded to the stored dtype (float32, or
+bfloat16 through float32 with round-to-nearest-even); both sides of every
+parity check read the rounded values.
+
+Padding that the verifier must never read is poisoned: target rows i > g_b and
+draft rows i >= g_b hold +inf, and draft token slots i >= g_b hold -1.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+F32 = "f32"
+BF16 = "bf16"
+
+BF16_POS_INF = np.uint16(0x7F80)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bfloat16 (via float32, both steps round-to-nearest-even).
+
+    Returns the raw 16-bit patterns as uint16.  NaN maps to the quiet NaN 0x7FC0.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    nan = np.isnan(f)
+    if nan.any():
+        rounded[nan] = np.uint16(0x7FC0)
+    return rounded
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen raw bfloat16 patterns to float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def logits_as_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
+    """The stored logits widened exactly to float64."""
+    if dtype == BF16:
+        return bf16_bits_to_f64(arr)
+    return np.asarray(arr, dtype=np.float32).astype(np.float64)
+
+
+@dataclasses.dataclass
+class Batch:
+    """One verification call's inputs, host-resident.
+
+    target      [B, gmax+1, V]  float32, or uint16 bfloat16 bit patterns
+    draft       [B, gmax,   V]  same dtype as target
+    tokens      [B, gmax]       int32 drafted token ids (-1 in padding)
+    num_draft   [B]             int32, 0 <= num_draft[b] <= gmax
+    uniforms    [B, gmax+1]     float32 in [0, 1); column i < num_draft[b] is the
+                                accept-test draw of position i, column gmax the
+                                draw for the final (residual or bonus) sample
+    temperature [B]             float32; 0 = greedy
+    """
+
+    target: np.ndarray
+    draft: np.ndarray
+    tokens: np.ndarray
+    num_draft: np.ndarray
+    uniforms: np.ndarray
+    temperature: np.ndarray
+    dtype: str
+    name: str = ""
+
+    @property
+    def B(self) -> int:
+        return int(self.tokens.shape[0])
+
+    @property
+    def gmax(self) -> int:
+        return int(self.tokens.shape[1])
+
+    @property
+    def V(self) -> int:
+        return int(self.target.shape[2])
+
+    @property
+    def elem_size(self) -> int:
+        return 2 if self.dtype == BF16 else 4
+
+    def algorithmic_bytes(self) -> int:
+        """Logit bytes one full verification sweep must read.
+
+        Every target row i <= g_b, plus draft rows i < g_b of sampled (T > 0)
+        sequences; greedy sequences never need q.  The 4-byte per-position
+        tokens, uniforms, temperatures and outputs are included too.
+        """
+        g = self.num_draft.astype(np.int64)
+        sampled = (self.temperature > 0).astype(np.int64)
+        rows = int(((g + 1) + sampled * g).sum())
+        small = 4 * (self.B * (self.gmax + self.gmax + 1 + 2) + self.B * (self.gmax + 1) + self.B)
+        return rows * self.V * self.elem_size + small
+
+    def nominal_bytes(self) -> int:
+        """Bytes of every stored logit row (target and draft), read or not."""
+        return (self.target.size + self.draft.size) * self.elem_size
+
+
+def _round(x64: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == BF16:
+        return f64_to_bf16_bits(x64)
+    return x64.astype(np.float32)
+
+
+def _draft_token(rng: np.random.Generator, d_rounded: np.ndarray, dtype: str, temp: float) -> int:
+    """Proposer stand-in: one token from softmax(d / T) by Gumbel-max, argmax d when T = 0."""
+    d64 = logits_as_f64(d_rounded, dtype)
+    if temp == 0.0:
+        return int(np.argmax(d64))
+    g = rng.gumbel(size=d64.shape[0])
+    return int(np.argmax(d64 / float(temp) + g))
+
+
+def _empty(B: int, gmax: int, V: int, dtype: str):
+    if dtype == BF16:
+        target = np.full((B, gmax + 1, V), BF16_POS_INF, dtype=np.uint16)
+        draft = np.full((B, gmax, V), BF16_POS_INF, dtype=np.uint16)
+    else:
+        target = np.full((B, gmax + 1, V), np.inf, dtype=np.float32)
+        draft = np.full((B, gmax, V), np.inf, dtype=np.float32)
+    tokens = np.full((B, gmax), -1, dtype=np.int32)
+    return target, draft, tokens
+
+
+def _zipf_shift(rng: np.random.Generator, V: int) -> np.ndarray:
+    """-1.1 * ln(rank), rank = 1 + position of the id in a random permutation."""
+    perm = rng.permutation(V)
+    rank = np.empty(V, dtype=np.float64)
+    rank[perm] = np.arange(1, V + 1, dtype=np.float64)
+    return -1.1 * np.log(rank)
+
+
+# ----------------------------------------------------------------------------
+# The five benchmark workloads
+# ----------------------------------------------------------------------------
+
+CONFIG_NAMES = {
+    1: "B=1, gamma=4, V=1024, f32 logits, T=1.0",
+    2: "B=1, gamma=5, V=32000, bf16 logits, 20 peaked ids, T=1.0 (greedy variant T=0)",
+    3: "B=32, gamma=4, V=128256, bf16 logits, Zipf-shifted, draft noise sigma in {0.3,0.7,1.5}, T=0.7",
+    4: "B=64, ragged gamma in [1,7], V=151936, bf16 logits, Zipf-shifted, T in {0,0.6,1.0}",
+    5: "B=256, gamma=4, V=128256, bf16 logits, Zipf-shifted, draft sigma ~ U[0.2,2.0], half greedy / half T=1.0",
+}
+
+
+def default_seed(cfg: int) -> int:
+    return 1234 + cfg
+
+
+def make_config(cfg: int, seed: int | None = None, greedy: bool = False, B: int | None = None) -> Batch:
+    """Build one of the five workloads (optionally with fewer sequences B)."""
+    if seed is None:
+        seed = default_seed(cfg)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if cfg == 1:
+        return _cfg1(rng, B or 1)
+    if cfg == 2:
+        return _cfg2(rng, B or 1, greedy)
+    if cfg == 3:
+        return _zipf_cfg(rng, B or 32, gamma=4, V=128256, ragged=False, name="cfg3")
+    if cfg == 4:
+        return _zipf_cfg(rng, B or 64, gamma=7, V=151936, ragged=True, name="cfg4")
+    if cfg == 5:
+        return _zipf_cfg(rng, B or 256, gamma=4, V=128256, ragged=False, name="cfg5")
+    raise ValueError(f"unknown config {cfg}")
+
+
+def _cfg1(rng: np.random.Generator, B: int) -> Batch:
+    gamma, V = 4, 1024
+    target, draft, tokens = _empty(B, gamma, V, F32)
+    temp = np.full(B, 1.0, dtype=np.float32)
+    for b in range(B):
+        t = rng.normal(0.0, 2.0, size=(gamma + 1, V))
+        d = t[:gamma] + rng.normal(0.0, 0.5, size=(gamma, V))
+        target[b] = _round(t, F32)
+        draft[b] = _round(d, F32)
+        for i in range(gamma):
+            tokens[b, i] = _draft_token(rng, draft[b, i], F32, float(temp[b]))
+    num_draft = np.full(B, gamma, dtype=np.int32)
+    uniforms = rng.random((B, gamma + 1), dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, F32, "cfg1")
+
+
+def _cfg2(rng: np.random.Generator, B: int, greedy: bool) -> Batch:
+    gamma, V = 5, 32000
+    target, draft, tokens = _empty(B, gamma, V, BF16)
+    temp = np.full(B, 0.0 if greedy else 1.0, dtype=np.float32)
+    for b in range(B):
+        t = rng.normal(0.0, 3.0, size=(gamma + 1, V))
+        for i in range(gamma + 1):
+            peaks = rng.choice(V, size=20, replace=False)
+            t[i, peaks] += 8.0
+        d = t[:gamma] + rng.normal(0.0, 1.0, size=(gamma, V))
+        target[b] = _round(t, BF16)
+        draft[b] = _round(d, BF16)
+        for i in range(gamma):
+            tokens[b, i] = _draft_token(rng, draft[b, i], BF16, float(temp[b]))
+    num_draft = np.full(B, gamma, dtype=np.int32)
+    uniforms = rng.random((B, gamma + 1), dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, BF16, "cfg2-greedy" if greedy else "cfg2")
+
+
+def _zipf_cfg(rng: np.random.Generator, B: int, gamma: int, V: int, ragged: bool, name: str) -> Batch:
+    target, draft, tokens = _empty(B, gamma, V, BF16)
+    if name == "cfg3":
+        temp = np.full(B, 0.7, dtype=np.float32)
+        sigma = np.array([(0.3, 0.7, 1.5)[b % 3] for b in range(B)])
+    elif name == "cfg4":
+        temp = np.array([(0.0, 0.6, 1.0)[b % 3] for b in range(B)], dtype=np.float32)
+        sigma = np.array([(0.3, 0.7, 1.5)[b % 3] for b in range(B)])
+    else:
+        temp = np.array([0.0 if b % 2 == 0 else 1.0 for b in range(B)], dtype=np.float32)
+        sigma = rng.uniform(0.2, 2.0, size=B)
+    if ragged:
+        num_draft = rng.integers(1, gamma + 1, size=B).astype(np.int32)
+    else:
+        num_draft = np.full(B, gamma, dtype=np.int32)
+    for b in range(B):
+        g = int(num_draft[b])
+        shift = _zipf_shift(rng, V)
+        t = rng.normal(0.0, 3.0, size=(g + 1, V)) + shift
+        d = t[:g] + rng.normal(0.0, float(sigma[b]), size=(g, V))
+        target[b, : g + 1] = _round(t, BF16)
+        draft[b, :g] = _round(d, BF16)
+        for i in range(g):
+            tokens[b, i] = _draft_token(rng, draft[b, i], BF16, float(temp[b]))
+    uniforms = rng.random((B, gamma + 1), dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, BF16, name)
+
+
+# ----------------------------------------------------------------------------
+# Tiny-vocabulary batches for the distribution checks
+# ----------------------------------------------------------------------------
+
+def tiny_batch(p_rows, q_rows, N: int, seed: int, temperature: float = 1.0) -> Batch:
+    """N independent copies of one round with fixed per-position distributions.
+
+    p_rows: gamma+1 probability vectors over a tiny vocabulary (target at each
+    position, the last one is the bonus position); q_rows: gamma vectors (draft).
+    Logits are the float32 natural logs of the given probabilities times the
+    temperature, so that softmax(logits / T) reproduces them up to float32
+    rounding.  Zero probabilities become -inf logits.  Drafted tokens are drawn
+    from q_rows by inverse transform on seeded uniforms.
+    """
+    p = np.asarray(p_rows, dtype=np.float64)
+    q = np.asarray(q_rows, dtype=np.float64)
+    gamma = q.shape[0]
+    V = p.shape[1]
+    assert p.shape == (gamma + 1, V) and q.shape == (gamma, V)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    with np.errstate(divide="ignore"):
+        tl = (np.log(p) * temperature).astype(np.float32)
+        dl = (np.log(q) * temperature).astype(np.float32) if gamma else np.zeros((0, V), np.float32)
+    target = np.broadcast_to(tl, (N, gamma + 1, V)).copy()
+    draft = np.broadcast_to(dl, (N, gamma, V)).copy()
+    tokens = np.empty((N, gamma), dtype=np.int32)
+    for i in range(gamma):
+        cdf = np.cumsum(q[i])
+        cdf[-1] = 1.0
+        x = rng.random(N)
+        tokens[:, i] = np.searchsorted(cdf, x, side="right").astype(np.int32)
+    tokens = np.minimum(tokens, V - 1)
+    num_draft = np.full(N, gamma, dtype=np.int32)
+    uniforms = rng.random((N, gamma + 1), dtype=np.float32)
+    temp = np.full(N, temperature, dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, F32, "tiny")
+
+
+def worked_example_rows():
+    """Draft gives the token 0.4, target 0.1 (the rest split so both sum to one)."""
+    p = [[0.1, 0.6, 0.3], [1.0 / 3, 1.0 / 3, 1.0 / 3]]
+    q = [[0.4, 0.3, 0.3]]
+    return p, q
+
+
+def alpha_rows(alpha: float, gamma: int):
+    """Two-token rows with sum_x min(p, q) = alpha exactly, repeated gamma times.
+
+    p = (1/2, 1/2), q = (1/2 + (1 - alpha), 1/2 - (1 - alpha)); needs alpha >= 1/2.
+    """
+    if not (0.5 <= alpha <= 1.0):
+        raise ValueError("alpha must lie in [0.5, 1]")
+    eps = 1.0 - alpha
+    p = [[0.5, 0.5]] * (gamma + 1)
+    q = [[0.5 + eps, 0.5 - eps]] * gamma
+    return p, q
+
+
+def edge_batch(kind: str, V: int = 1023, gamma: int = 3, B: int = 8, seed: int = 7,
+               dtype: str = BF16) -> Batch:
+    """Hand-made edge cases (see the parity tests for what each exercises).
+
+    kinds: 'zero_draft' (num_draft = 0 everywhere), 'reject_first' (draft logits
+    put all mass on a token the target gives ~0), 'accept_all' (draft equals
+    target), 'greedy_ties' (T = 0, repeated maxima), 'neg_inf' (some -inf
+    logits), 'mixed' (random ragged g, mixed T, generic V).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    target, draft, tokens = _empty(B, gamma, V, dtype)
+    num_draft = np.full(B, gamma, dtype=np.int32)
+    temp = np.full(B, 1.0, dtype=np.float32)
+    for b in range(B):
+        t = rng.normal(0.0, 2.0, size=(gamma + 1, V))
+        d = t[:gamma] + rng.normal(0.0, 0.7, size=(gamma, V))
+        g = gamma
+        if kind == "zero_draft":
+            g = 0
+            temp[b] = (0.0, 0.8)[b % 2]
+        elif kind == "reject_first":
+            d[:] = -30.0
+            d[:, 5] = 30.0
+            t[:, 5] = -30.0
+        elif kind == "accept_all":
+            d = t[:gamma].copy()
+        elif kind == "greedy_ties":
+            temp[b] = 0.0
+            t = np.round(t * 2.0) / 2.0
+            for i in range(gamma + 1):
+                top = t[i].max()
+                ids = rng.choice(V, size=3, replace=False)
+                t[i, ids] = top
+        elif kind == "neg_inf":
+            temp[b] = (0.0, 1.0)[b % 2]
+            mask = rng.random((gamma + 1, V)) < 0.3
+            t[mask] = -np.inf
+            dm = rng.random((gamma, V)) < 0.3
+            d[dm] = -np.inf
+        elif kind == "mixed":
+            g = int(rng.integers(0, gamma + 1))
+            temp[b] = (0.0, 0.5, 1.3)[b % 3]
+        else:
+            raise ValueError(kind)
+        num_draft[b] = g
+        target[b, : g + 1] = _round(t[: g + 1], dtype)
+        draft[b, :g] = _round(d[:g], dtype)
+        for i in range(g):
+            if kind == "greedy_ties":
+                # propose the lowest-index maximum half of the time, another tied id otherwise
+                row = logits_as_f64(target[b, i], dtype)
+                tied = np.flatnonzero(row == row.max())
+                tokens[b, i] = int(tied[0]) if rng.random() < 0.5 else int(tied[-1])
+            else:
+                tokens[b, i] = _draft_token(rng, draft[b, i], dtype, float(temp[b]))
+    uniforms = rng.random((B, gamma + 1), dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, dtype, f"edge-{kind}")
+
+
+def describe(batch: Batch) -> str:
+    return (f"{batch.name}: B={batch.B} gmax={batch.gmax} V={batch.V} dtype={batch.dtype} "
+            f"logit bytes={batch.algorithmic_bytes()} (nominal {batch.nominal_bytes()})")
