@@ -1,0 +1,395 @@
+"""Benchmark of the GB300 speculative-decoding verification step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one spec_verify call (one verification round) over one batch of the
+B=256, gamma=4, V=128256 bf16 workload (Zipf-shifted N(0, 3^2) target logits,
+draft noise sigma ~ U[0.2, 2.0], even sequences greedy, odd ones T=1.0).
+Inputs are generated on the host from a seeded generator, copied to HBM once,
+and are larger than L2 (459.7 MB read per step vs 129 MB of L2).  Under
+torchrun each rank verifies its own batch (seed + rank): weak scaling, no
+collective on the data path.  Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle (the method's plain restatement)
+on the host cores instead, one bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "spec_verify sequences/s and achieved HBM GB/s vs ~8 TB/s peak (1 GB300)"
+UNIT = "sequences/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_45_gb300", "csrc", "spec_verify.cu")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "spec_verify_cfg5_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, group_backend: str | None) -> float:
+    """Max over ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if group_backend == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_value(seqs_per_rank: int, world: int, steps: int, seconds_max: float) -> float:
+    """Whole-job sequences per second: every rank's sequences over the slowest rank's time."""
+    return seqs_per_rank * world * steps / seconds_max
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash() or rec.get("workload") != workload_key:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4], parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside
+        if not used and rows:
+            mid = 0.5 * (t0 + t1)
+            used = [min(rows, key=lambda r: abs(r[0] - mid))]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def oracle_baseline(batch, target_seconds: float):
+    """The float64 oracle on the host cores: whole batches until target_seconds of wall time."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    oracle.build()
+    n_seq, t_total, reps = 0, 0.0, 0
+    while t_total < target_seconds or reps == 0:
+        t0 = time.perf_counter()
+        oracle.verify_batch(batch, diagnostics=False, nthreads=cores)
+        t_total += time.perf_counter() - t0
+        n_seq += batch.B
+        reps += 1
+    return {"value": n_seq / t_total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x the full {batch.B}-sequence batch ({n_seq} sequences), {t_total:.1f} s wall, "
+                      f"{cores} threads"}
+
+
+def workload_desc(cfg: int):
+    from speculative_decoding_verification_45_gb300 import workloads
+
+    return workloads.CONFIG_NAMES[cfg]
+
+
+def run_reference(args):
+    """Reference arm: the float64 oracle timed on the host cores."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from speculative_decoding_verification_45_gb300 import workloads
+
+    batch = workloads.make_config(args.config)
+    oracle.build()
+    cores = os.cpu_count() or 1
+    # size one step's sample so the whole run stays within ~60 s of oracle time
+    t0 = time.perf_counter()
+    cal = min(batch.B, 16)
+    sub = _slice(batch, 0, cal)
+    oracle.verify_batch(sub, diagnostics=False, nthreads=cores)
+    per_seq = (time.perf_counter() - t0) / cal
+    total_steps = args.steps + args.warmup
+    per_step = max(1, min(batch.B, int(60.0 / max(total_steps, 1) / max(per_seq, 1e-6))))
+    samples = [_slice(batch, (i * per_step) % batch.B, per_step) for i in range(4)]
+    for i in range(args.warmup):
+        oracle.verify_batch(samples[i % 4], diagnostics=False, nthreads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.verify_batch(samples[i % 4], diagnostics=False, nthreads=cores)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(args.config), "sequences_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} sequences of the {batch.B}-sequence batch per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _slice(batch, start, count):
+    import numpy as np
+
+    from speculative_decoding_verification_45_gb300 import workloads
+
+    idx = (np.arange(count) + start) % batch.B
+    return workloads.Batch(batch.target[idx], batch.draft[idx], batch.tokens[idx], batch.num_draft[idx],
+                           batch.uniforms[idx], batch.temperature[idx], batch.dtype, batch.name)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    backend = None
+    if ws > 1:
+        backend = "nccl"
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import speculative_decoding_verification_45_gb300 as sv
+    from speculative_decoding_verification_45_gb300 import workloads
+
+    if rank == 0:
+        sv.build()
+    barrier()
+    sv._native.load()
+
+    batch = workloads.make_config(args.config, seed=workloads.default_seed(args.config) + rank)
+    B = batch.B
+    inputs = sv.to_device(batch, dev)
+    out_tokens = torch.empty((B, batch.gmax + 1), dtype=torch.int32, device=dev)
+    out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    algo_bytes = batch.algorithmic_bytes()
+    C, nctas, threads = sv.launch_shape(B, batch.gmax, batch.V, batch.dtype)
+
+    def step():
+        sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = None
+    if not args.quick:
+        props = torch.cuda.get_device_properties(dev)
+        uuid = str(getattr(props, "uuid", ""))
+        gpu_id = uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local))
+        sampler = ClockSampler(gpu_id)
+        sampler.start()
+        time.sleep(0.3)
+
+    start_ev = torch.cuda.Event(enable_timing=True)
+    stop_ev = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    start_ev.record(stream)
+    for _ in range(args.steps):
+        step()
+    stop_ev.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    ms_total = start_ev.elapsed_time(stop_ev)
+    ms_max = reduce_max(ms_total, backend)
+    clocks = None
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+        clocks = sampler.summary(w0, w1)
+
+    value = aggregate_value(B, ws, args.steps, ms_max / 1e3)
+    ms_step = ms_max / args.steps
+
+    # end to end through the public API with host buffers: pinned H2D of every
+    # input each step, the call, D2H of the outputs
+    e2e = None
+    if not args.quick:
+        host = {k: v.cpu().pin_memory() for k, v in inputs.items()}
+        dev_in = {k: torch.empty_like(v) for k, v in inputs.items()}
+        h_tok = torch.empty(out_tokens.shape, dtype=torch.int32).pin_memory()
+        h_num = torch.empty(out_num.shape, dtype=torch.int32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = h_tok.numel() * 4 + h_num.numel() * 4
+        k_e2e = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            sv.verify(**dev_in, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream)
+            h_tok.copy_(out_tokens, non_blocking=True)
+            h_num.copy_(out_num, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        z.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(a.elapsed_time(z), backend)
+        e2e = {"value": aggregate_value(B, ws, k_e2e, e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k_e2e}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = measured_peaks()
+    achieved = algo_bytes / (ms_step / 1e3) / 1e9
+    workload_key = f"cfg{args.config}-B{B}-g{batch.gmax}-V{batch.V}-{batch.dtype}"
+    traffic = recorded_traffic(workload_key)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(args.config), "B": B, "gamma": batch.gmax, "V": batch.V,
+                   "logits": batch.dtype, "parallelism": f"dp{ws} (independent sequences per rank)",
+                   "l2": "inputs larger than L2 (read set per step > 129 MB), no flush",
+                   "cluster_size": C, "ctas": nctas, "threads_per_cta": threads},
+        "rounds_per_s": ws * args.steps / (ms_max / 1e3),
+        "hbm_gbs_algorithmic": achieved,
+        "hbm_gbs_nominal_590MB": batch.nominal_bytes() / (ms_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": algo_bytes},
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.quick and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(batch, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--quick", action="store_true", help="skip e2e, clocks and the CPU baseline (profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and not args.quick:
+        log("warning: fewer than 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

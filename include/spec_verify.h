@@ -1,0 +1,147 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification step.
+ *
+ * The operation (one verification round, after the target model's single
+ * forward over the drafted tokens) is the modified rejection sampler that all
+ * of these pages state:
+ *   [P1] "Speculative Decoding" (atonlee.tistory.com/330), ch.2 (one round:
+ *        accept in order, cut at the first rejection, k accepted + 1 token)
+ *        and ch.3 (accept test r < min(1, p(x)/q(x)), residual
+ *        norm(max(0, p - q)), greedy rule at temperature 0);
+ *   [P2] "Speculative Decoding으로 LLM 추론 속도 높이기" (donmain.dev), section
+ *        "품질은 rejection sampling이 지킨다";
+ *   [P3] "Fast Inference from Transformers via Speculative Decoding" notes
+ *        (obsidian-dorae222.pages.dev), method details, steps 2-3 (gamma+1
+ *        target distributions from one forward, accept probability, residual
+ *        sample, bonus token from p at row gamma when every draft passes);
+ *   [P4] "투기적 디코딩 — 초안 모델을 무엇으로 세울 것인가" (ailab.paldyn.com),
+ *        section on why the output does not change (greedy: draft == argmax).
+ *
+ * For each sequence b with g = num_draft[b] drafts and temperature T = temperature[b]:
+ *   T > 0:  p_i = softmax(target_logits[b, i, :] / T) for i <= g,
+ *           q_i = softmax(draft_logits[b, i, :] / T) for i < g.
+ *           Position i < g accepts draft x_i = draft_tokens[b, i] iff
+ *           uniforms[b, i] * q_i(x_i) < p_i(x_i); n = first rejected i, or g.
+ *           One more token y is drawn by inverse CDF with u = uniforms[b, gamma_max]
+ *           from max(0, p_n - q_n) (n < g) or from p_g (n == g): y is the
+ *           smallest id j with u * S < C_j, C_j the running sum of the weights
+ *           in id order and S their total.
+ *   T == 0: greedy; a_i = argmax of the raw target logits of row i (lowest id
+ *           on ties); position i accepts iff x_i == a_i; y = a_n.  No draft row
+ *           and no uniform is read.
+ *   Output: out_tokens[b, 0..n-1] = x_0..x_{n-1}, out_tokens[b, n] = y,
+ *           out_tokens[b, n+1..gamma_max] = -1, out_num_accepted[b] = n.
+ * Rows after the cut are still read by this full-sweep variant; rows
+ * i > g (target) and i >= g (draft), and every draft row of a greedy
+ * sequence, are never read.
+ *
+ * Layout.  All arrays are dense, row-major, on the device of the calling
+ * thread's current CUDA context:
+ *   target_logits  [B, gamma_max + 1, V]   dtype (SPEC_F32 or SPEC_BF16)
+ *   draft_logits   [B, gamma_max, V]       dtype
+ *   draft_tokens   [B, gamma_max]          int32
+ *   num_draft      [B]                     int32
+ *   uniforms       [B, gamma_max + 1]      float32 in [0, 1)
+ *   temperature    [B]                     float32
+ *   out_tokens     [B, gamma_max + 1]      int32 (written)
+ *   out_num_accepted [B]                   int32 (written)
+ * Logit pointers must be aligned to their element size; the fast path is
+ * taken when both are 16-byte aligned and V * element size is a multiple of
+ * 16 bytes, a scalar-load path otherwise.  int32/float32 arrays must be
+ * 4-byte aligned.  Outputs must not overlap inputs.
+ *
+ * Ownership and execution.  The caller owns every buffer.  The call enqueues
+ * one kernel on 'stream' (a cudaStream_t; NULL = legacy default stream) and
+ * returns without synchronising; it allocates no memory.  It is reentrant:
+ * the only process-wide state is a per-device cache of kernel attributes.
+ *
+ * Errors.  Argument problems found on the host return an error code before
+ * anything is enqueued.  Problems in the data never trap: a sequence with
+ * num_draft outside [0, gamma_max], a temperature that is negative, NaN,
+ * infinite or positive but below FLT_MIN, a drafted id outside [0, V) at a
+ * position it uses, or a sampled row it uses whose logits have no finite
+ * softmax normaliser (all -inf, any +inf or NaN) gets out_tokens[b, :] = -1
+ * and out_num_accepted[b] = 0, and its SPEC_STATUS_* bit is OR-ed into
+ * *status when status is not NULL (the caller zeroes it).  NaN logits in
+ * greedy rows give unspecified (in-range) tokens.
+ *
+ * Limits: 0 <= B <= SPEC_MAX_BATCH (B == 0 is a no-op), 0 <= gamma_max <=
+ * SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_VOCAB.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_MAX_GAMMA 16
+#define SPEC_MAX_VOCAB (1 << 24)
+#define SPEC_MAX_BATCH (1 << 26)
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* null pointer, size out of range, misaligned pointer */
+    SPEC_ERR_UNSUPPORTED = 2, /* unknown dtype, or no usable launch shape on this device */
+    SPEC_ERR_CUDA = 3         /* a CUDA runtime call or the launch failed */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Per-sequence data problems (bits OR-ed into *status). */
+#define SPEC_STATUS_BAD_TOKEN 1u
+#define SPEC_STATUS_BAD_TEMPERATURE 2u
+#define SPEC_STATUS_BAD_NUM_DRAFT 4u
+#define SPEC_STATUS_BAD_LOGITS 8u
+
+/* One verification round for B independent sequences (see the top of this
+ * file for the operation, layout, ownership and errors).
+ * status: optional device word (may be NULL) receiving SPEC_STATUS_* bits. */
+spec_status spec_verify(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                        const int32_t *num_draft, const float *uniforms, const float *temperature,
+                        int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
+                        spec_dtype dtype, uint32_t *status, void *stream);
+
+/* Same round, plus optional float32 diagnostics for tests (any may be NULL):
+ *   p_hat [B, gamma_max]     p_i(x_i) for i < g of sampled sequences, NaN elsewhere
+ *   q_hat [B, gamma_max]     q_i(x_i), same positions
+ *   logz_t [B, gamma_max+1]  natural-log normaliser log sum_j exp(l_j / T) of
+ *                            target rows i <= g of sampled sequences, NaN elsewhere
+ *   logz_d [B, gamma_max]    same for draft rows i < g
+ *   resid_mass [B]           total weight S of the decided row of a sampled
+ *                            sequence (residual mass, or ~1 for a bonus row)
+ *   seq_status [B]           SPEC_STATUS_* bits of each sequence (0 = valid)
+ * The diagnostic rows are computed for every i <= g, also after the cut. */
+spec_status spec_verify_debug(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                              const int32_t *num_draft, const float *uniforms, const float *temperature,
+                              int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
+                              spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
+                              float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status);
+
+/* spec_verify with an explicit thread-block-cluster size (CTAs sharing one
+ * sequence's rows): 0 = automatic, else 1, 2, 4, 8 or 16.  Results do not
+ * depend on it.  Returns SPEC_ERR_UNSUPPORTED if the device cannot co-schedule
+ * a cluster of that size. */
+spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
+                           const int32_t *num_draft, const float *uniforms, const float *temperature,
+                           int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
+                           spec_dtype dtype, uint32_t *status, void *stream, int cluster_size);
+
+/* Launch shape spec_verify would use on the current device for these sizes:
+ * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any
+ * output pointer may be NULL.  Touches the device (attribute queries) but
+ * enqueues nothing. */
+spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
+                                     int *num_ctas, int *threads_per_cta);
+
+/* Static description of a status code. */
+const char *spec_status_string(spec_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,185 @@
+"""GB300 (sm_103a) speculative-decoding verification: Python binding.
+
+The work runs in the CUDA kernels of libspec_verify.so behind the C ABI declared
+in include/spec_verify.h; this module only checks tensors and marshals pointers
+(ctypes).  PyTorch provides device memory and the current stream.  There is no
+CPU fallback: if the library is missing, every call raises.
+
+    out_tokens, out_num = verify(target_logits, draft_logits, draft_tokens,
+                                 num_draft, uniforms, temperature)
+
+See include/spec_verify.h for the operation, layouts and error behaviour.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _native
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED = 2
+SPEC_ERR_CUDA = 3
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+
+STATUS_BAD_TOKEN = 1
+STATUS_BAD_TEMPERATURE = 2
+STATUS_BAD_NUM_DRAFT = 4
+STATUS_BAD_LOGITS = 8
+
+MAX_GAMMA = 16
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = _native.load()
+        super().__init__(f"{where}: {lib.spec_status_string(code).decode()} (code {code})")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    return _native.build(force=force)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must live on {device}, found {t.device}")
+
+
+def _prepare(target, draft, tokens, num_draft, uniforms, temperature, out_tokens, out_num):
+    import torch
+
+    if not target.is_cuda:
+        raise ValueError("target_logits must be a CUDA tensor")
+    dev = target.device
+    B, g1, V = target.shape
+    gmax = g1 - 1
+    code = _dtype_code(target)
+    _check(target, "target_logits", target.dtype, (B, gmax + 1, V), dev)
+    _check(draft, "draft_logits", target.dtype, (B, gmax, V), dev)
+    _check(tokens, "draft_tokens", torch.int32, (B, gmax), dev)
+    _check(num_draft, "num_draft", torch.int32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, gmax + 1), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gmax + 1), dtype=torch.int32, device=dev)
+    if out_num is None:
+        out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, gmax + 1), dev)
+    _check(out_num, "out_num_accepted", torch.int32, (B,), dev)
+    return B, gmax, V, code, out_tokens, out_num
+
+
+def _stream_handle(stream, device):
+    import torch
+
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
+           out_num_accepted=None, status=None, stream=None, cluster_size: int = 0):
+    """One verification round on the GPU (asynchronous on ``stream``).
+
+    Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
+    ``status``: optional int32 CUDA tensor of one element receiving the
+    per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
+    ``cluster_size``: 0 = automatic, else 1/2/4/8/16 CTAs per sequence.
+    """
+    B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
+        target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
+    lib = _native.load()
+    args = [_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft), _ptr(uniforms),
+            _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code, _ptr(status),
+            _stream_handle(stream, target_logits.device)]
+    if cluster_size:
+        rc = lib.spec_verify_ex(*args, int(cluster_size))
+    else:
+        rc = lib.spec_verify(*args)
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify")
+    return out_tokens, out_num_accepted
+
+
+def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, stream=None):
+    """verify() plus the float32 diagnostics of spec_verify_debug (a dict of tensors)."""
+    import torch
+
+    B, gmax, V, code, out_tokens, out_num = _prepare(
+        target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, None, None)
+    dev = target_logits.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    d = {
+        "p_hat": torch.empty((B, gmax), **f32),
+        "q_hat": torch.empty((B, gmax), **f32),
+        "logz_t": torch.empty((B, gmax + 1), **f32),
+        "logz_d": torch.empty((B, gmax), **f32),
+        "resid_mass": torch.empty((B,), **f32),
+        "seq_status": torch.empty((B,), dtype=torch.int32, device=dev),
+        "status": torch.zeros((1,), dtype=torch.int32, device=dev),
+    }
+    lib = _native.load()
+    rc = lib.spec_verify_debug(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft),
+                               _ptr(uniforms), _ptr(temperature), _ptr(out_tokens), _ptr(out_num), B, gmax, V,
+                               code, _ptr(d["status"]), _stream_handle(stream, dev), _ptr(d["p_hat"]),
+                               _ptr(d["q_hat"]), _ptr(d["logz_t"]), _ptr(d["logz_d"]), _ptr(d["resid_mass"]),
+                               _ptr(d["seq_status"]))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_debug")
+    d["out_tokens"] = out_tokens
+    d["out_num_accepted"] = out_num
+    return d
+
+
+def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):
+    """(cluster size, CTAs, threads per CTA) the library picks for these sizes on the current device."""
+    lib = _native.load()
+    c, n, t = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib.spec_verify_launch_shape(B, gamma_max, V, SPEC_BF16 if dtype == "bf16" else SPEC_F32,
+                                      ctypes.byref(c), ctypes.byref(n), ctypes.byref(t))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_launch_shape")
+    return c.value, n.value, t.value
+
+
+def to_device(batch, device="cuda"):
+    """Copy a workloads.Batch (host numpy arrays) to device tensors, logits in their stored dtype."""
+    import numpy as np
+    import torch
+
+    if batch.dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(batch.target).view(np.int16)).view(torch.bfloat16)
+        d = torch.from_numpy(np.ascontiguousarray(batch.draft).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(batch.target, dtype=np.float32))
+        d = torch.from_numpy(np.ascontiguousarray(batch.draft, dtype=np.float32))
+    return dict(
+        target_logits=t.to(device),
+        draft_logits=d.to(device),
+        draft_tokens=torch.from_numpy(np.ascontiguousarray(batch.tokens, dtype=np.int32)).to(device),
+        num_draft=torch.from_numpy(np.ascontiguousarray(batch.num_draft, dtype=np.int32)).to(device),
+        uniforms=torch.from_numpy(np.ascontiguousarray(batch.uniforms, dtype=np.float32)).to(device),
+        temperature=torch.from_numpy(np.ascontiguousarray(batch.temperature, dtype=np.float32)).to(device),
+    )

@@ -1,0 +1,79 @@
+"""Build and load the sm_103a shared library (libspec_verify.so) in-tree."""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+INCLUDE = os.path.join(ROOT, "include")
+SOURCES = [os.path.join(PKG, "csrc", "spec_verify.cu")]
+HEADERS = [os.path.join(INCLUDE, "spec_verify.h")]
+BUILD_DIR = os.path.join(PKG, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libspec_verify.so")
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def nvcc_path() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is needed to build libspec_verify.so")
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    return any(os.path.getmtime(f) > t for f in SOURCES + HEADERS)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a into _build/libspec_verify.so (one nvcc call)."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    if not force and not _stale():
+        return LIB_PATH
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc_path(), "-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
+           "-I", INCLUDE, "-o", tmp, *SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    if verbose:
+        print(res.stdout + res.stderr)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() (or "
+                               "speculative_decoding_verification_45_gb300._native.build()) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        common = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
+        lib.spec_verify.argtypes = common
+        lib.spec_verify.restype = i32
+        lib.spec_verify_debug.argtypes = common + [vp] * 6
+        lib.spec_verify_debug.restype = i32
+        lib.spec_verify_ex.argtypes = common + [i32]
+        lib.spec_verify_ex.restype = i32
+        lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_verify_launch_shape.restype = i32
+        lib.spec_status_string.argtypes = [i32]
+        lib.spec_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib

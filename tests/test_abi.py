@@ -1,0 +1,71 @@
+"""The C ABI library: it loads, exports every declared entry point, and rejects
+bad arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_45_gb300 import _native
+
+HEADER = os.path.join(_native.INCLUDE, "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _native.build()
+    return _native.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_verify_launch_shape",
+              "spec_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        assert lib.spec_status_string(code)
+    assert lib.spec_status_string(99) == b"unknown status"
+
+
+def _call(lib, **over):
+    fake = 0x10000  # never dereferenced: every case below fails validation first
+    args = dict(target=fake, draft=fake, tokens=fake, num_draft=fake, uniforms=fake, temperature=fake,
+                out_tokens=fake, out_num=fake, B=4, gmax=4, V=1024, dtype=1, status=None, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.spec_verify(vp(args["target"]), vp(args["draft"]), vp(args["tokens"]), vp(args["num_draft"]),
+                           vp(args["uniforms"]), vp(args["temperature"]), vp(args["out_tokens"]),
+                           vp(args["out_num"]), args["B"], args["gmax"], args["V"], args["dtype"],
+                           vp(args["status"]) if args["status"] else None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(target=0), 1), (dict(num_draft=0), 1), (dict(uniforms=0), 1), (dict(temperature=0), 1),
+    (dict(out_tokens=0), 1), (dict(out_num=0), 1), (dict(draft=0), 1), (dict(tokens=0), 1),
+    (dict(B=-1), 1), (dict(gmax=17), 1), (dict(gmax=-1), 1), (dict(V=0), 1), (dict(V=(1 << 24) + 1), 1),
+    (dict(dtype=7), 2), (dict(target=0x10001), 1), (dict(tokens=0x10002), 1), (dict(status=0x10003), 1),
+    (dict(B=0), 0),
+])
+def test_host_argument_checks(lib, over, code):
+    assert _call(lib, **over) == code
+
+
+def test_cluster_size_argument_checked(lib):
+    vp = ctypes.c_void_p
+    f = vp(0x10000)
+    rc = lib.spec_verify_ex(f, f, f, f, f, f, f, f, 4, 4, 1024, 1, None, None, 3)
+    assert rc == 1

@@ -1,0 +1,101 @@
+"""GPU parity with the float64 oracle on the five workloads (full sizes, the
+launch shape the benchmark times) and their diagnostics (softmax values within
+rel 1e-5)."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_45_gb300 import workloads
+from tests import parity
+
+gpu = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_45_gb300 as m
+
+    m.build()
+    return m
+
+
+def run_debug(sv, batch):
+    import torch
+
+    dev = sv.to_device(batch)
+    d = sv.verify_debug(**dev)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in d.items()}
+
+
+def check_batch(sv, oracle_mod, batch, diagnostics=True):
+    d = run_debug(sv, batch)
+    ref = oracle_mod.verify_batch(batch)
+    rep = parity.compare(batch, d["out_tokens"], d["out_num_accepted"], ref, gpu_status=d["seq_status"])
+    assert rep.mismatches_far == 0, (str(rep), rep.far_detail[:5])
+    if diagnostics:
+        parity.softmax_close(d["p_hat"], ref.p_hat)
+        parity.softmax_close(d["q_hat"], ref.q_hat)
+        parity.softmax_close(d["logz_t"], ref.logz_t, atol=1e-5)
+        parity.softmax_close(d["logz_d"], ref.logz_d, atol=1e-5)
+    assert int(d["status"][0]) == int(np.bitwise_or.reduce(ref.seq_status)) if batch.B else True
+    return rep, d, ref
+
+
+@gpu
+@pytest.mark.parametrize("cfg,greedy", [(1, False), (2, False), (2, True), (3, False), (4, False), (5, False)])
+def test_config_parity(sv, oracle_mod, cfg, greedy):
+    batch = workloads.make_config(cfg, greedy=greedy)
+    rep, d, ref = check_batch(sv, oracle_mod, batch)
+    print(f"cfg{cfg}{'-greedy' if greedy else ''}: {rep}")
+
+
+@gpu
+@pytest.mark.parametrize("cfg,seed", [(3, 11), (3, 12), (4, 13), (5, 14), (1, 15), (2, 16)])
+def test_config_parity_more_seeds(sv, oracle_mod, cfg, seed):
+    batch = workloads.make_config(cfg, seed=seed)
+    rep, _, _ = check_batch(sv, oracle_mod, batch, diagnostics=False)
+    print(f"cfg{cfg} seed {seed}: {rep}")
+
+
+@gpu
+def test_resid_mass_matches_oracle(sv, oracle_mod):
+    batch = workloads.make_config(3)
+    d = run_debug(sv, batch)
+    ref = oracle_mod.verify_batch(batch)
+    same_n = d["out_num_accepted"] == ref.out_num_accepted
+    np.testing.assert_allclose(d["resid_mass"][same_n], ref.resid_mass[same_n], rtol=1e-5, atol=1e-7)
+
+
+@gpu
+def test_cluster_sizes_agree(sv, oracle_mod):
+    """Every cluster size gives the oracle's result (the split of rows over CTAs is invisible)."""
+    import torch
+
+    batch = workloads.make_config(4, B=12)
+    ref = oracle_mod.verify_batch(batch)
+    dev = sv.to_device(batch)
+    for C in (1, 2, 4, 8, 16):
+        toks, num = sv.verify(**dev, cluster_size=C)
+        torch.cuda.synchronize()
+        rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref)
+        assert rep.mismatches_far == 0, (C, str(rep), rep.far_detail[:3])
+
+
+@gpu
+def test_deterministic_and_stream(sv):
+    import torch
+
+    batch = workloads.make_config(3, B=8)
+    dev = sv.to_device(batch)
+    a = [t.clone() for t in sv.verify(**dev)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        b = sv.verify(**dev, stream=s)
+    s.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
