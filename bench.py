@@ -264,9 +264,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     algo_bytes = batch.algorithmic_bytes()
     C, nctas, threads = sv.launch_shape(B, batch.gmax, batch.V, batch.dtype)
+    if args.cluster:
+        C, nctas = args.cluster, B * args.cluster
+    if args.kernel != "auto":
+        threads = 288 if args.kernel == "ring" else 256
+
+    kernel = {"auto": sv.KERNEL_AUTO, "stream": sv.KERNEL_REGISTER, "ring": sv.KERNEL_RING}[args.kernel]
 
     def step():
-        sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream)
+        sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream,
+                  cluster_size=args.cluster, kernel=kernel)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -319,7 +326,8 @@ def run_ours(args):
         def e2e_step():
             for k, v in host.items():
                 dev_in[k].copy_(v, non_blocking=True)
-            sv.verify(**dev_in, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream)
+            sv.verify(**dev_in, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream,
+                      cluster_size=args.cluster, kernel=kernel)
             h_tok.copy_(out_tokens, non_blocking=True)
             h_num.copy_(out_num, non_blocking=True)
 
@@ -345,7 +353,7 @@ def run_ours(args):
     peak, peak_src = measured_peaks()
     achieved = algo_bytes / (ms_step / 1e3) / 1e9
     workload_key = f"cfg{args.config}-B{B}-g{batch.gmax}-V{batch.V}-{batch.dtype}"
-    traffic = recorded_traffic(workload_key)
+    traffic = recorded_traffic(workload_key) if args.kernel == "auto" and not args.cluster else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -353,7 +361,7 @@ def run_ours(args):
         "config": {"workload": workload_desc(args.config), "B": B, "gamma": batch.gmax, "V": batch.V,
                    "logits": batch.dtype, "parallelism": f"dp{ws} (independent sequences per rank)",
                    "l2": "inputs larger than L2 (read set per step > 129 MB), no flush",
-                   "cluster_size": C, "ctas": nctas, "threads_per_cta": threads},
+                   "cluster_size": C, "ctas": nctas, "threads_per_cta": threads, "kernel": args.kernel},
         "rounds_per_s": ws * args.steps / (ms_max / 1e3),
         "hbm_gbs_algorithmic": achieved,
         "hbm_gbs_nominal_590MB": batch.nominal_bytes() / (ms_step / 1e3) / 1e9,
@@ -380,6 +388,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kernel", choices=["auto", "stream", "ring"], default="auto",
+                    help="kernel choice (A/B measurement; auto = the library's default)")
+    ap.add_argument("--cluster", type=int, default=0, choices=[0, 1, 2, 4, 8, 16],
+                    help="CTAs per sequence (0 = the library's default)")
     ap.add_argument("--quick", action="store_true", help="skip e2e, clocks and the CPU baseline (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -63,7 +63,9 @@
  * position it uses, or a sampled row it uses whose logits have no finite
  * softmax normaliser (all -inf, any +inf or NaN) gets out_tokens[b, :] = -1
  * and out_num_accepted[b] = 0, and its SPEC_STATUS_* bit is OR-ed into
- * *status when status is not NULL (the caller zeroes it).  NaN logits in
+ * *status when status is not NULL (the caller zeroes it).  Every wait inside
+ * the kernel is bounded; one that runs out sets SPEC_STATUS_TIMEOUT instead of
+ * hanging.  NaN logits in
  * greedy rows give unspecified (in-range) tokens.
  *
  * Limits: 0 <= B <= SPEC_MAX_BATCH (B == 0 is a no-op), 0 <= gamma_max <=
@@ -96,6 +98,9 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_TEMPERATURE 2u
 #define SPEC_STATUS_BAD_NUM_DRAFT 4u
 #define SPEC_STATUS_BAD_LOGITS 8u
+/* An internal wait of the kernel on its own asynchronous copies exceeded its
+ * iteration limit (not expected on a healthy GPU): the sequence gets -1 tokens. */
+#define SPEC_STATUS_TIMEOUT 16u
 
 /* One verification round for B independent sequences (see the top of this
  * file for the operation, layout, ownership and errors).
@@ -121,14 +126,19 @@ spec_status spec_verify_debug(const void *target_logits, const void *draft_logit
                               spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
                               float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status);
 
-/* spec_verify with an explicit thread-block-cluster size (CTAs sharing one
- * sequence's rows): 0 = automatic, else 1, 2, 4, 8 or 16.  Results do not
- * depend on it.  Returns SPEC_ERR_UNSUPPORTED if the device cannot co-schedule
- * a cluster of that size. */
+/* Launch options (tuning and A/B measurement; results do not depend on them). */
+typedef struct spec_verify_options {
+    int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1, 2, 4, 8 or 16 */
+    int kernel;       /* 0 = automatic; 1 = bulk-copy ring (16-byte aligned rows only, else
+                         SPEC_ERR_UNSUPPORTED); 2 = register loads */
+} spec_verify_options;
+
+/* spec_verify with explicit launch options (NULL = automatic).  Returns
+ * SPEC_ERR_UNSUPPORTED if the device cannot co-schedule the requested shape. */
 spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                            const int32_t *num_draft, const float *uniforms, const float *temperature,
                            int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
-                           spec_dtype dtype, uint32_t *status, void *stream, int cluster_size);
+                           spec_dtype dtype, uint32_t *status, void *stream, const spec_verify_options *options);
 
 /* Launch shape spec_verify would use on the current device for these sizes:
  * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any

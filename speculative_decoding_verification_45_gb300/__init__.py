@@ -28,6 +28,7 @@ STATUS_BAD_TOKEN = 1
 STATUS_BAD_TEMPERATURE = 2
 STATUS_BAD_NUM_DRAFT = 4
 STATUS_BAD_LOGITS = 8
+STATUS_TIMEOUT = 16
 
 MAX_GAMMA = 16
 
@@ -99,14 +100,20 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+KERNEL_AUTO = 0
+KERNEL_RING = 1      # bulk-copy ring (16-byte aligned rows)
+KERNEL_REGISTER = 2  # register loads
+
+
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
-           out_num_accepted=None, status=None, stream=None, cluster_size: int = 0):
+           out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO):
     """One verification round on the GPU (asynchronous on ``stream``).
 
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
     ``status``: optional int32 CUDA tensor of one element receiving the
     per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
     ``cluster_size``: 0 = automatic, else 1/2/4/8/16 CTAs per sequence.
+    ``kernel``: KERNEL_AUTO, KERNEL_RING or KERNEL_REGISTER (A/B measurement).
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
@@ -114,8 +121,9 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     args = [_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft), _ptr(uniforms),
             _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code, _ptr(status),
             _stream_handle(stream, target_logits.device)]
-    if cluster_size:
-        rc = lib.spec_verify_ex(*args, int(cluster_size))
+    if cluster_size or kernel:
+        opts = _native.Options(int(cluster_size), int(kernel))
+        rc = lib.spec_verify_ex(*args, ctypes.byref(opts))
     else:
         rc = lib.spec_verify(*args)
     if rc != SPEC_OK:

@@ -20,6 +20,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Options(ctypes.Structure):
+    """spec_verify_options of include/spec_verify.h."""
+
+    _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int)]
+
+
 def nvcc_path() -> str:
     for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
         if cand and os.path.exists(cand):
@@ -69,7 +75,7 @@ def load() -> ctypes.CDLL:
         lib.spec_verify.restype = i32
         lib.spec_verify_debug.argtypes = common + [vp] * 6
         lib.spec_verify_debug.restype = i32
-        lib.spec_verify_ex.argtypes = common + [i32]
+        lib.spec_verify_ex.argtypes = common + [vp]
         lib.spec_verify_ex.restype = i32
         lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
         lib.spec_verify_launch_shape.restype = i32

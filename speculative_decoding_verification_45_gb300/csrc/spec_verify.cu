@@ -14,13 +14,13 @@
 //   * One thread-block cluster of C CTAs per sequence (C in {1,2,4,8,16},
 //     chosen from B and V).  CTA c of the cluster owns the contiguous slice
 //     [c*NC/C, (c+1)*NC/C) of 16-byte chunks of every row the sequence needs.
-//   * Pass 1 streams those slices once with 128-bit loads.  Target and draft
-//     rows of sampled sequences (T > 0) keep an online (max, sum of 2^(a-m))
-//     per thread, a = logit * log2(e)/T, with m an integer so that rescaling
-//     is an exact power of two and the sum compensated; greedy rows (T = 0)
-//     keep (max, lowest argmax) of the raw logits.  Partials are reduced over
-//     the warp (shuffles), the CTA (shared memory) and the cluster (every CTA
-//     pushes its row partials into every other CTA's shared memory, DSMEM).
+//   * Pass 1 streams those slices once.  Target and draft rows of sampled
+//     sequences (T > 0) keep an online (max, sum of 2^(a-m)) per thread,
+//     a = logit * log2(e)/T, with m an integer so that rescaling is an exact
+//     power of two and the sum compensated; greedy rows (T = 0) keep
+//     (max, lowest argmax) of the raw logits.  Partials are reduced over the
+//     warp (shuffles), the CTA (shared memory) and the cluster (every CTA pushes
+//     its row partials into every other CTA's shared memory, DSMEM).
 //   * After one cluster barrier each CTA holds all partials, merges them in
 //     rank order (identical bits in every CTA) and takes the accept decision
 //     itself: one lane per draft position, a warp ballot gives the first
@@ -30,9 +30,28 @@
 //     unsigned 64-bit fixed point (2^-60 units), so every sum is exact and
 //     order-free.  Slice sums are exchanged over DSMEM; the CTA whose slice
 //     holds floor(u*S) scans its chunks and writes the sampled id.
-//   No global scratch memory, no atomics on the data path (only the optional
-//   status word), no spin waits: the only waits are hardware cluster barriers
-//   that every thread of the cluster reaches.
+//
+// Two kernels share that protocol:
+//   spec_verify_stream_kernel (default) 128-bit loads straight into registers,
+//                             eight per thread in flight, 32 reducing warps per
+//                             SM; element loads when rows are not 16-byte
+//                             aligned.  Pass 2a keeps each chunk's weight sum in
+//                             shared memory, so pass 2b is a scan there plus one
+//                             reload.
+//   spec_verify_ring_kernel   16-byte-aligned rows only.  A producer warp streams
+//                             the CTA's slices through an 8-stage shared-memory
+//                             ring with cp.async.bulk (the bulk-copy engine)
+//                             and mbarriers; eight reducing warps read shared
+//                             memory.  All rows of a CTA form one copy stream
+//                             (64 KB in flight across row boundaries).  On GB300
+//                             it is slower here: the reduction is issue-bound,
+//                             and the ring's 78 KB of shared memory leaves only
+//                             16 reducing warps per SM.  Kept for A/B runs.
+// Clusters take sequences longest-first (rows to read), so the grid's tail is
+// short work.  Neither kernel uses global scratch memory, atomics on the data
+// path (only the optional status word) or unbounded waits: mbarrier waits give
+// up after a fixed number of tries and report SPEC_STATUS_TIMEOUT, and the only
+// other waits are hardware barriers that every thread reaches.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -49,14 +68,25 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = 8;  // warps that reduce (both kernels)
+constexpr int kThreads = kWarps * 32;
+constexpr int kTmaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMaxRows = 2 * SPEC_MAX_GAMMA + 1;
 constexpr int kMaxCluster = 16;
-constexpr int kUnroll = 8;  // independent 16-byte loads in flight per thread
+constexpr int kUnroll = 8;       // scalar kernel: 16-byte loads in flight per thread
+constexpr int kSegChunks = 512;  // ring kernel: 16-byte chunks per ring stage (8 KB)
+constexpr int kChunksPerThread = kSegChunks / kThreads;
+constexpr int kStages = 8;  // ring depth: 64 KB
+constexpr int kRingBytes = kStages * kSegChunks * 16;
+constexpr int kMaxSpin = 1 << 18;  // tries of one mbarrier wait before giving up
+constexpr int kMaxScanTiles = 48;  // register kernel: at most 48 * kThreads chunk sums (48 KB) in shared memory
+constexpr int kMaxOrdered = 1024;  // longest-first scheduling for B up to this
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kFixedScale = 1152921504606846976.0f;  // 2^60: pass-2 weight units
+constexpr float kFixedUnit = 8.6736173798840355e-19f;    // 2^-60: pass-2 weight unit (to_fixed60)
+constexpr unsigned long long kTimeoutFlag = 1ull << 63;  // carried in exchanged slice sums
+
+static_assert(kSegChunks % kThreads == 0, "a segment must split evenly over the reducing threads");
 
 struct Params {
     const void *target;
@@ -76,6 +106,8 @@ struct Params {
     int32_t *seq_status;
     int B, gmax, V;
     int num_chunks;  // 16-byte chunks per row; the last is partial on the scalar path
+    int scan_tiles;  // register kernel: tiles of kThreads chunk sums kept in shared memory (0 = none)
+    int ordered;     // map clusters to sequences longest-first (small B only)
 };
 
 // ---------------------------------------------------------------------------
@@ -179,23 +211,48 @@ __device__ __forceinline__ float pow2_int(float d)
     return __int_as_float((127 + (int)d) << 23);
 }
 
-// Sum over a chunk of 2^(x*k - m), tree order.
-template <typename T> __device__ __forceinline__ float chunk_exp_sum(const uint4 &v, float k, float negm)
+// Pair q of a chunk as two floats (elements 2q and 2q+1); bfloat16 is the top
+// half of a float, so widening is a shift or a mask.
+template <typename T> __device__ __forceinline__ float2 pair(const uint4 &v, int q)
 {
-    float e[Elem<T>::W];
+    if (sizeof(T) == 2) {
+        const uint32_t w = word(v, q);
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+    return make_float2(__uint_as_float(word(v, 2 * q)), __uint_as_float(word(v, 2 * q + 1)));
+}
+
+// Largest value over N chunks (NaN elements ignored), packed where possible.
+template <typename T, int N> __device__ __forceinline__ float chunks_max(const uint4 (&v)[N])
+{
+    if (sizeof(T) == 2) {
+        __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&v[0].x);
 #pragma unroll
-    for (int i = 0; i < Elem<T>::W; ++i)
-        e[i] = ex2_approx(fmaf(elem<T>(v, i), k, negm));
-    if (Elem<T>::W == 8)
-        return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    return (e[0] + e[1]) + (e[2] + e[3]);
+        for (int u = 0; u < N; ++u) {
+            m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162 *>(&v[u].x));
+            m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162 *>(&v[u].y));
+            m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162 *>(&v[u].z));
+            m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162 *>(&v[u].w));
+        }
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+        m = fmaxf(m, chunk_max<T>(v[u]));
+    return m;
+}
+
+__device__ __forceinline__ float2 ex2_pair(float2 a)
+{
+    return make_float2(ex2_approx(a.x), ex2_approx(a.y));
 }
 
 // ---------------------------------------------------------------------------
 // per-row statistics and their merges
 // ---------------------------------------------------------------------------
 // Softmax rows: sum_j 2^(a_j - m) = hi + lo, m integer-valued (or -inf).
-// Greedy rows:  (v, i) = largest raw logit and its lowest index.
+// Greedy rows:  (m, idx) = largest raw logit and its lowest index.
 struct RowStat {
     float m;
     float hi;
@@ -247,29 +304,37 @@ __device__ __forceinline__ RowStat shfl_xor_stat(const RowStat &s, int mask)
     return r;
 }
 
+__device__ __forceinline__ RowStat warp_reduce(RowStat s, bool sampled)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        s = sampled ? soft_merge(s, shfl_xor_stat(s, o)) : arg_merge(s, shfl_xor_stat(s, o));
+    return s;
+}
+
 __device__ __forceinline__ bool soft_row_ok(const RowStat &s)
 {
     const float z = s.hi + s.lo;
     return isfinite(s.m) && isfinite(z) && z > 0.0f;
 }
 
-// Pass-1 sweep of one row slice for a sampled sequence.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ RowStat sweep_softmax(const T *row, int c0, int c1, int V, float k)
-{
-    float m = -INFINITY, hi = 0.0f, lo = 0.0f;
-    for (int ch = c0 + (int)threadIdx.x; ch < c1; ch += kUnroll * kThreads) {
-        uint4 v[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int c = ch + u * kThreads;
-            v[u] = c < c1 ? load_chunk<T, ALIGNED>(row, c, V) : neg_inf_chunk<T>();
-        }
-        float bmax = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            bmax = fmaxf(bmax, chunk_max<T>(v[u]));
-        const float amax = bmax * k;
+// Running per-thread statistics of one row.
+struct RowAcc {
+    float m, hi, lo;  // sampled rows (greedy rows: m is the best value)
+    int idx;          // greedy rows: index of the best value
+    __device__ __forceinline__ void reset(int first_idx)
+    {
+        m = -INFINITY;
+        hi = 0.0f;
+        lo = 0.0f;
+        idx = first_idx;
+    }
+    // Adds chunks v[0..N) of a softmax row: online max, exact power-of-two
+    // rescale, packed FMA/add (two elements per instruction), four independent
+    // partial sums, then one compensated add per batch.
+    template <typename T, int N> __device__ __forceinline__ void add_soft(const uint4 (&v)[N], float k)
+    {
+        const float amax = chunks_max<T, N>(v) * k;
         if (amax > m) {
             const float mn = ceilf(amax);
             const float sc = pow2_int(m - mn);
@@ -278,74 +343,142 @@ __device__ __forceinline__ RowStat sweep_softmax(const T *row, int c0, int c1, i
             m = mn;
         }
         if (m == -INFINITY)
-            continue;
-        const float negm = -m;
+            return;
+        constexpr int P = Elem<T>::W / 2;
+        const float2 k2 = make_float2(k, k), nm2 = make_float2(-m, -m);
+        float2 acc[P];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            compensated_add(hi, lo, chunk_exp_sum<T>(v[u], k, negm));
+        for (int q = 0; q < P; ++q)
+            acc[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int u = 0; u < N; ++u)
+#pragma unroll
+            for (int q = 0; q < P; ++q)
+                acc[q] = __fadd2_rn(acc[q], ex2_pair(__ffma2_rn(pair<T>(v[u], q), k2, nm2)));
+        float2 t = acc[0];
+#pragma unroll
+        for (int q = 1; q < P; ++q)
+            t = __fadd2_rn(t, acc[q]);
+        compensated_add(hi, lo, t.x + t.y);
     }
-    RowStat s;
-    s.m = m;
-    s.hi = hi;
-    s.lo = lo;
-    s.idx = 0;
-    return s;
-}
-
-// Pass-1 sweep of one row slice for a greedy sequence.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ RowStat sweep_argmax(const T *row, int c0, int c1, int V)
-{
-    float best = -INFINITY;
-    int bidx = c0 + (int)threadIdx.x < c1 ? (c0 + (int)threadIdx.x) * Elem<T>::W : INT_MAX;
-    for (int ch = c0 + (int)threadIdx.x; ch < c1; ch += kUnroll * kThreads) {
-        uint4 v[kUnroll];
+    // Adds chunks v[0..N) of a greedy row; chunk u starts at element index
+    // base + u * stride.  Chunks arrive in increasing index order, so a strict
+    // improvement keeps the lowest index of the maximum.
+    template <typename T, int N>
+    __device__ __forceinline__ void add_arg(const uint4 (&v)[N], int base, int stride)
+    {
+        const float bm = chunks_max<T, N>(v);
+        if (bm > m) {
+            int found = -1;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int c = ch + u * kThreads;
-            v[u] = c < c1 ? load_chunk<T, ALIGNED>(row, c, V) : neg_inf_chunk<T>();
-        }
+            for (int u = 0; u < N; ++u)
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const float cm = chunk_max<T>(v[u]);
-            if (cm > best) {  // chunks arrive in increasing index order: strict > keeps the lowest
-                int first = 0;
-#pragma unroll
-                for (int e = Elem<T>::W - 1; e >= 0; --e)
-                    if (elem<T>(v[u], e) == cm)
-                        first = e;
-                best = cm;
-                bidx = (ch + u * kThreads) * Elem<T>::W + first;
-            }
+                for (int e = 0; e < Elem<T>::W; ++e)
+                    if (found < 0 && elem<T>(v[u], e) == bm)
+                        found = base + u * stride + e;
+            m = bm;
+            idx = found;
         }
     }
-    RowStat s;
-    s.m = best;
-    s.hi = 0.0f;
-    s.lo = 0.0f;
-    s.idx = bidx;
-    return s;
+    __device__ __forceinline__ RowStat stat() const
+    {
+        RowStat s;
+        s.m = m;
+        s.hi = hi;
+        s.lo = lo;
+        s.idx = idx;
+        return s;
+    }
+};
+
+// floor(w * 2^60) for a finite w in [0, 16), by integer operations only (a
+// float-to-64-bit-integer conversion instruction would run on the FP64 pipe).
+__device__ __forceinline__ unsigned long long to_fixed60(float w)
+{
+    const uint32_t bits = __float_as_uint(w);
+    const int ex = (int)(bits >> 23);  // w >= 0: no sign bit
+    if (ex == 0)
+        return 0ull;  // zero or below 2^-126, far under the 2^-60 unit
+    const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
+    const int sh = ex - 90;  // w = mant * 2^(ex - 150), so w * 2^60 = mant * 2^(ex - 90)
+    if (sh >= 0)
+        return mant << sh;
+    if (sh <= -24)
+        return 0ull;
+    return mant >> (-sh);
 }
 
-// Fixed-point pass-2 weights of one chunk of the decided row.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ void chunk_weights(const T *trow, const T *drow, int c, int V, bool residual, float k,
-                                              float negmt, float invzt, float negmd, float invzd,
-                                              unsigned long long (&w)[Elem<T>::W])
+// Pass-2 weights of one chunk of the decided row: max(0, p - q) (residual) or
+// p, in float32.  tv/dv: the target and draft chunk.
+struct WeightParams {
+    float k, negmt, invzt, negmd, invzd;
+    bool residual;
+};
+
+template <typename T>
+__device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, const WeightParams &wp,
+                                              float (&w)[Elem<T>::W])
 {
-    const uint4 tv = load_chunk<T, ALIGNED>(trow, c, V);
-    uint4 dv = make_uint4(0, 0, 0, 0);
-    if (residual)
-        dv = load_chunk<T, ALIGNED>(drow, c, V);
+    constexpr int P = Elem<T>::W / 2;
+    const float2 k2 = make_float2(wp.k, wp.k);
+    const float2 nmt = make_float2(wp.negmt, wp.negmt), izt = make_float2(wp.invzt, wp.invzt);
+    const float2 nmd = make_float2(wp.negmd, wp.negmd), nizd = make_float2(-wp.invzd, -wp.invzd);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+        float2 pq = __fmul2_rn(ex2_pair(__ffma2_rn(pair<T>(tv, q), k2, nmt)), izt);
+        if (wp.residual) {
+            pq = __ffma2_rn(ex2_pair(__ffma2_rn(pair<T>(dv, q), k2, nmd)), nizd, pq);  // p - q
+            pq.x = fmaxf(pq.x, 0.0f);
+            pq.y = fmaxf(pq.y, 0.0f);
+        }
+        w[2 * q] = pq.x;
+        w[2 * q + 1] = pq.y;
+    }
+}
+
+// A chunk's weight: the float32 sum of its elements in a fixed tree order ...
+template <typename T> __device__ __forceinline__ float chunk_sum(const float (&w)[Elem<T>::W])
+{
+    if (Elem<T>::W == 8)
+        return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+    return (w[0] + w[1]) + (w[2] + w[3]);
+}
+
+// ... on the exact 2^-60 grid, converted once.  Prefix sums of these are exact,
+// so every CTA and every pass sees the same cumulative boundaries.
+template <typename T> __device__ __forceinline__ unsigned long long chunk_fixed(const float (&w)[Elem<T>::W])
+{
+    return to_fixed60(chunk_sum<T>(w));
+}
+
+template <typename T>
+__device__ __forceinline__ unsigned long long chunk_weight_fixed(const uint4 &tv, const uint4 &dv,
+                                                                 const WeightParams &wp)
+{
+    float w[Elem<T>::W];
+    chunk_weights<T>(tv, dv, wp, w);
+    return chunk_fixed<T>(w);
+}
+
+// Inside the chunk whose cumulative interval holds theta (rel = theta - chunk
+// start, 0 <= rel < chunk weight): the first element whose running float sum,
+// on the 2^-60 grid, passes rel; the last element with weight > 0 if rounding
+// leaves none.  An element of weight 0 is never picked.
+template <typename T>
+__device__ __forceinline__ int pick_in_chunk(const float (&w)[Elem<T>::W], unsigned long long rel)
+{
+    float run = 0.0f;
+    int last = 0;
 #pragma unroll
     for (int e = 0; e < Elem<T>::W; ++e) {
-        float p = ex2_approx(fmaf(elem<T>(tv, e), k, negmt)) * invzt;
-        if (residual) {
-            const float q = ex2_approx(fmaf(elem<T>(dv, e), k, negmd)) * invzd;
-            p = fmaxf(p - q, 0.0f);
+        run += w[e];
+        if (w[e] > 0.0f) {
+            if (rel < to_fixed60(run))
+                return e;
+            last = e;
         }
-        w[e] = __float2ull_rn(p * kFixedScale);
     }
+    return last;
 }
 
 // floor(u * S) exactly, u a float in [0, 1), S a 64-bit integer.
@@ -366,6 +499,9 @@ __device__ __forceinline__ unsigned long long scaled_floor(float u, unsigned lon
     return (lo >> sh) | (hi << (64 - sh));
 }
 
+// ---------------------------------------------------------------------------
+// barriers
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ void cluster_arrive_relaxed()
 {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -379,190 +515,217 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Barrier of the kThreads reducing threads only (named barrier 1).
+__device__ __forceinline__ void reducers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Waits for the phase of the given parity to complete; false after kMaxSpin tries.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    for (int i = 0; i < kMaxSpin; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+// Bulk copy (bulk-copy engine, no registers involved) of 'bytes' from global
+// memory into this CTA's shared memory; completion is signalled on 'bar'.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// shared state and the per-sequence protocol common to both kernels
+// ---------------------------------------------------------------------------
 struct SharedState {
     RowStat warp_part[kMaxRows][kWarps];
     RowStat recv[kMaxCluster][kMaxRows];  // written remotely by every CTA of the cluster
     RowStat row[kMaxRows];                // merged statistics, identical in every CTA
     unsigned long long recv_sum[2][kMaxCluster];
-    unsigned long long warp_sum[kWarps];
+    unsigned long long warp_sum[kWarps + 1];
+    unsigned long long tile_tot[kMaxScanTiles];
+    int hist[kMaxRows + 1];
+    int cnt[kWarps];
+    int seq;
+    int bin;
+    int rank_in_bin;
+    int recv_flag[kMaxCluster];
     int n;
     int bits;
+    int timeout;
 };
 
-// Block-wide sum of a 64-bit value (exact); every thread gets the total.
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, SharedState &sh)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0)
-        sh.warp_sum[threadIdx.x >> 5] = v;
-    __syncthreads();
-    unsigned long long t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-        t += sh.warp_sum[w];
-    return t;
-}
+struct Seq {
+    int b, g, gmax, V, rank, C, c0, c1;
+    bool sampled;
+    float k;  // log2(e) / T for sampled sequences
+    size_t rowlen;
+};
 
-// Block-wide inclusive scan of a 64-bit value (exact); also returns the total.
-__device__ __forceinline__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long &total,
-                                                             SharedState &sh)
+// Validates the sequence's inputs (identical in every CTA of the cluster).
+__device__ __forceinline__ uint32_t check_inputs(const Params &p, int b, int g, float temp)
 {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o)
-            v += y;
-    }
-    __syncthreads();
-    if (lane == 31)
-        sh.warp_sum[wid] = v;
-    __syncthreads();
-    unsigned long long before = 0, t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        if (w < wid)
-            before += sh.warp_sum[w];
-        t += sh.warp_sum[w];
-    }
-    total = t;
-    return v + before;
-}
-
-template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
-{
-    __shared__ SharedState sh;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-    const int b = (int)(blockIdx.x / (unsigned)C);
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int gmax = p.gmax, V = p.V;
-    const size_t rowlen = (size_t)V;
-    int32_t *out = p.out_tokens + (size_t)b * (gmax + 1);
-
-    // ---- inputs of this sequence; every CTA of the cluster decides the same way
-    const int g = p.num_draft[b];
-    const float temp = p.temperature[b];
     uint32_t bad = 0;
-    if (g < 0 || g > gmax)
-        bad = SPEC_STATUS_BAD_NUM_DRAFT;
-    else {
-        if (isnan(temp) || isinf(temp) || temp < 0.0f || (temp > 0.0f && temp < FLT_MIN))
-            bad |= SPEC_STATUS_BAD_TEMPERATURE;
-        for (int i = 0; i < g; ++i) {
-            const int x = p.tokens[(size_t)b * gmax + i];
-            if (x < 0 || x >= V)
-                bad |= SPEC_STATUS_BAD_TOKEN;
-        }
+    if (g < 0 || g > p.gmax)
+        return SPEC_STATUS_BAD_NUM_DRAFT;
+    if (isnan(temp) || isinf(temp) || temp < 0.0f || (temp > 0.0f && temp < FLT_MIN))
+        bad |= SPEC_STATUS_BAD_TEMPERATURE;
+    for (int i = 0; i < g; ++i) {
+        const int x = p.tokens[(size_t)b * p.gmax + i];
+        if (x < 0 || x >= p.V)
+            bad |= SPEC_STATUS_BAD_TOKEN;
     }
-    const bool sampled = temp > 0.0f;
+    return bad;
+}
 
-    // diagnostics default to NaN (rank 0 overwrites what it computes)
-    if (rank == 0 && tid <= gmax) {
-        const float nan = __int_as_float(0x7fc00000);
-        if (p.logz_t)
-            p.logz_t[(size_t)b * (gmax + 1) + tid] = nan;
-        if (tid < gmax) {
-            if (p.p_hat)
-                p.p_hat[(size_t)b * gmax + tid] = nan;
-            if (p.q_hat)
-                p.q_hat[(size_t)b * gmax + tid] = nan;
-            if (p.logz_d)
-                p.logz_d[(size_t)b * gmax + tid] = nan;
-        }
-        if (tid == 0 && p.resid_mass)
-            p.resid_mass[b] = nan;
-    }
-
-    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
-        if (rank == 0) {
-            if (tid <= gmax)
-                out[tid] = -1;
-            if (tid == 0) {
-                p.out_num[b] = 0;
-                if (p.seq_status)
-                    p.seq_status[b] = (int32_t)bad;
-                if (p.status)
-                    atomicOr(p.status, bad);
-            }
-        }
+// Rank 0 marks the diagnostics of a sequence as "not computed" (NaN).
+__device__ __forceinline__ void init_diagnostics(const Params &p, int b, int rank)
+{
+    const int tid = threadIdx.x, gmax = p.gmax;
+    if (rank != 0 || tid > gmax)
         return;
+    const float nan = __int_as_float(0x7fc00000);
+    if (p.logz_t)
+        p.logz_t[(size_t)b * (gmax + 1) + tid] = nan;
+    if (tid < gmax) {
+        if (p.p_hat)
+            p.p_hat[(size_t)b * gmax + tid] = nan;
+        if (p.q_hat)
+            p.q_hat[(size_t)b * gmax + tid] = nan;
+        if (p.logz_d)
+            p.logz_d[(size_t)b * gmax + tid] = nan;
     }
+    if (tid == 0 && p.resid_mass)
+        p.resid_mass[b] = nan;
+}
 
-    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
-
-    const T *trows = reinterpret_cast<const T *>(p.target) + (size_t)b * (gmax + 1) * rowlen;
-    const T *drows = reinterpret_cast<const T *>(p.draft) + (size_t)b * gmax * rowlen;
-    const int c0 = (int)((long long)p.num_chunks * rank / C);
-    const int c1 = (int)((long long)p.num_chunks * (rank + 1) / C);
-    const float k = sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
-    const int nrows = sampled ? 2 * g + 1 : g + 1;
-
-    // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
-    for (int r = 0; r < nrows; ++r) {
-        const T *row = r <= g ? trows + (size_t)r * rowlen : drows + (size_t)(r - g - 1) * rowlen;
-        RowStat s;
-        if (sampled) {
-            s = sweep_softmax<T, ALIGNED>(row, c0, c1, V, k);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                s = soft_merge(s, shfl_xor_stat(s, o));
-        } else {
-            s = sweep_argmax<T, ALIGNED>(row, c0, c1, V);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                s = arg_merge(s, shfl_xor_stat(s, o));
-        }
-        if (lane == 0)
-            sh.warp_part[r][wid] = s;
+// Rank 0 writes -1 tokens and the status of an invalid sequence.
+__device__ __forceinline__ void write_invalid(const Params &p, int b, int rank, uint32_t bits)
+{
+    if (rank != 0)
+        return;
+    const int tid = threadIdx.x;
+    if (tid <= p.gmax)
+        p.out_tokens[(size_t)b * (p.gmax + 1) + tid] = -1;
+    if (tid == 0) {
+        p.out_num[b] = 0;
+        if (p.seq_status)
+            p.seq_status[b] = (int32_t)bits;
+        if (p.status)
+            atomicOr(p.status, bits);
     }
+}
+
+// Logical row r (target i -> i, draft i -> g + 1 + i) read at sweep position
+// 'step'.  Order t_g, t_{g-1}, d_{g-1}, ..., t_0, d_0: the rows most likely to
+// be decided (small i) come last, so pass 2 finds them in L2.
+__device__ __forceinline__ int row_at_step(int step, int g, bool sampled)
+{
+    if (step == 0)
+        return g;
+    if (!sampled)
+        return g - step;
+    const int i = g - 1 - (step - 1) / 2;
+    return ((step - 1) & 1) ? g + 1 + i : i;
+}
+
+template <typename T> __device__ __forceinline__ const T *row_ptr(const Params &p, const Seq &s, int r)
+{
+    if (r <= s.g)
+        return reinterpret_cast<const T *>(p.target) + ((size_t)s.b * (s.gmax + 1) + r) * s.rowlen;
+    return reinterpret_cast<const T *>(p.draft) + ((size_t)s.b * s.gmax + (r - s.g - 1)) * s.rowlen;
+}
+
+// Merges the warp partials of each row, sends them to every CTA of the cluster
+// and merges what arrives in rank order.  All threads of the CTA call it; the
+// cluster arrive (relaxed) must have been issued at kernel start.
+__device__ __forceinline__ void exchange_rows(SharedState &sh, const Seq &s, int nrows)
+{
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
     __syncthreads();
     cluster_wait();  // every CTA of the cluster is running: DSMEM is addressable
     if (tid < nrows) {
-        RowStat s = sh.warp_part[tid][0];
+        RowStat v = sh.warp_part[tid][0];
         for (int w = 1; w < kWarps; ++w)
-            s = sampled ? soft_merge(s, sh.warp_part[tid][w]) : arg_merge(s, sh.warp_part[tid][w]);
-        for (int dst = 0; dst < C; ++dst) {
-            RowStat *remote = cluster.map_shared_rank(&sh.recv[rank][tid], dst);
-            *remote = s;
-        }
+            v = s.sampled ? soft_merge(v, sh.warp_part[tid][w]) : arg_merge(v, sh.warp_part[tid][w]);
+        for (int dst = 0; dst < s.C; ++dst)
+            *cluster.map_shared_rank(&sh.recv[s.rank][tid], dst) = v;
     }
+    if (tid < s.C)
+        *cluster.map_shared_rank(&sh.recv_flag[s.rank], tid) = sh.timeout;
     cluster_sync_all();
     if (tid < nrows) {
-        RowStat s = sh.recv[0][tid];
-        for (int src = 1; src < C; ++src)
-            s = sampled ? soft_merge(s, sh.recv[src][tid]) : arg_merge(s, sh.recv[src][tid]);
-        sh.row[tid] = s;
+        RowStat v = sh.recv[0][tid];
+        for (int src = 1; src < s.C; ++src)
+            v = s.sampled ? soft_merge(v, sh.recv[src][tid]) : arg_merge(v, sh.recv[src][tid]);
+        sh.row[tid] = v;
     }
     __syncthreads();
+}
 
-    // ---- accept decisions: lane i tests draft position i; a ballot finds the cut
+// Accept decisions (warp 0: lane i tests draft position i; a ballot finds the
+// cut) and rank 0's output writes.  Returns true if the sequence goes on to
+// pass 2 (sampled and valid).  All threads call it.
+template <typename T> __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int b = s.b, g = s.g, gmax = s.gmax;
     if (wid == 0) {
         bool ok = false, valid = true;
         float phat = 0.0f, qhat = 0.0f;
         if (lane < g) {
             const int x = p.tokens[(size_t)b * gmax + lane];
-            if (!sampled) {
+            if (!s.sampled) {
                 ok = x == sh.row[lane].idx;
             } else {
                 const RowStat st = sh.row[lane], sd = sh.row[g + 1 + lane];
                 valid = soft_row_ok(st) && soft_row_ok(sd);
+                const T *tr = row_ptr<T>(p, s, lane);
+                const T *dr = row_ptr<T>(p, s, g + 1 + lane);
                 float lt, ld;
                 if (sizeof(T) == 2) {
-                    lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(trows)[(size_t)lane * rowlen + x]);
-                    ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(drows)[(size_t)lane * rowlen + x]);
+                    lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[x]);
+                    ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[x]);
                 } else {
-                    lt = reinterpret_cast<const float *>(trows)[(size_t)lane * rowlen + x];
-                    ld = reinterpret_cast<const float *>(drows)[(size_t)lane * rowlen + x];
+                    lt = reinterpret_cast<const float *>(tr)[x];
+                    ld = reinterpret_cast<const float *>(dr)[x];
                 }
-                phat = ex2_approx(fmaf(lt, k, -st.m)) / (st.hi + st.lo);
-                qhat = ex2_approx(fmaf(ld, k, -sd.m)) / (sd.hi + sd.lo);
+                phat = ex2_approx(fmaf(lt, s.k, -st.m)) / (st.hi + st.lo);
+                qhat = ex2_approx(fmaf(ld, s.k, -sd.m)) / (sd.hi + sd.lo);
                 ok = valid && (p.uniforms[(size_t)b * (gmax + 1) + lane] * qhat < phat);
             }
         }
@@ -572,15 +735,18 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
         const unsigned fail = ~pass & lanes;
         const int n = fail ? __ffs(fail) - 1 : g;
         uint32_t bits = 0;
-        if (sampled) {
-            if (n < g ? !((fine >> n) & 1u) : !soft_row_ok(sh.row[g]))
-                bits = SPEC_STATUS_BAD_LOGITS;
-        }
+        if (s.sampled && (n < g ? !((fine >> n) & 1u) : !soft_row_ok(sh.row[g])))
+            bits = SPEC_STATUS_BAD_LOGITS;
+        int flag = 0;
+        for (int c = 0; c < s.C; ++c)
+            flag |= sh.recv_flag[c];
+        if (flag)
+            bits = SPEC_STATUS_TIMEOUT;
         if (lane == 0) {
             sh.n = n;
             sh.bits = (int)bits;
         }
-        if (rank == 0 && sampled && lane < g) {
+        if (s.rank == 0 && s.sampled && lane < g) {
             if (p.p_hat)
                 p.p_hat[(size_t)b * gmax + lane] = phat;
             if (p.q_hat)
@@ -590,9 +756,9 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
     __syncthreads();
     const int n = sh.n;
     const uint32_t bits = (uint32_t)sh.bits;
-
-    if (rank == 0) {
-        if (sampled && tid <= g && (p.logz_t || p.logz_d)) {
+    if (s.rank == 0) {
+        int32_t *out = p.out_tokens + (size_t)b * (gmax + 1);
+        if (s.sampled && tid <= g) {
             const RowStat st = sh.row[tid];
             if (p.logz_t)
                 p.logz_t[(size_t)b * (gmax + 1) + tid] = (st.m + log2f(st.hi + st.lo)) * kLn2;
@@ -607,7 +773,7 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
                 if (tid < n)
                     v = p.tokens[(size_t)b * gmax + tid];
                 else if (tid == n)
-                    v = sampled ? INT_MIN : sh.row[n].idx;  // sampled: written by pass 2
+                    v = s.sampled ? INT_MIN : sh.row[n].idx;  // sampled: written by pass 2
             }
             if (v != INT_MIN)
                 out[tid] = v;
@@ -620,91 +786,642 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
                 atomicOr(p.status, bits);
         }
     }
-    if (!sampled || bits)
+    return s.sampled && !bits;
+}
+
+__device__ __forceinline__ WeightParams weight_params(const SharedState &sh, const Seq &s, int n, bool residual)
+{
+    const RowStat st = sh.row[n];
+    const RowStat sd = residual ? sh.row[s.g + 1 + n] : st;
+    WeightParams wp;
+    wp.k = s.k;
+    wp.negmt = -st.m;
+    wp.invzt = 1.0f / (st.hi + st.lo);
+    wp.negmd = -sd.m;
+    wp.invzd = 1.0f / (sd.hi + sd.lo);
+    wp.residual = residual;
+    return wp;
+}
+
+// Sends this CTA's slice sum to every CTA of the cluster, then sums what
+// arrives: S (total) and P (sum over the lower ranks).  All threads call it.
+__device__ __forceinline__ void exchange_slice_sum(SharedState &sh, const Seq &s, int attempt,
+                                                   unsigned long long mine, unsigned long long &S,
+                                                   unsigned long long &P, bool &timed_out)
+{
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
+    if (tid < s.C)
+        *cluster.map_shared_rank(&sh.recv_sum[attempt][s.rank], tid) = mine;
+    cluster_sync_all();
+    S = 0;
+    P = 0;
+    timed_out = false;
+    for (int src = 0; src < s.C; ++src) {
+        const unsigned long long v = sh.recv_sum[attempt][src];
+        timed_out |= (v & kTimeoutFlag) != 0;
+        if (src < s.rank)
+            P += v & ~kTimeoutFlag;
+        S += v & ~kTimeoutFlag;
+    }
+}
+
+// The final uniform, clamped into [0, 1).
+__device__ __forceinline__ float final_uniform(const Params &p, const Seq &s)
+{
+    float u = p.uniforms[(size_t)s.b * (s.gmax + 1) + s.gmax];
+    if (!(u >= 0.0f))
+        u = 0.0f;
+    if (u >= 1.0f)
+        u = __uint_as_float(0x3F7FFFFFu);
+    return u;
+}
+
+// Block-wide sum of a 64-bit value over all NW warps of the CTA (exact); every
+// thread gets the total.
+template <int NW>
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, SharedState &sh)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        sh.warp_sum[threadIdx.x >> 5] = v;
+    __syncthreads();
+    unsigned long long t = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+        t += sh.warp_sum[w];
+    return t;
+}
+
+// Inclusive scan of a 64-bit value over the kThreads reducing threads (exact);
+// also returns their total.  NAMED: the reducing threads are not the whole CTA
+// (ring kernel), so they meet at named barrier 1 instead of __syncthreads.
+template <bool NAMED>
+__device__ __forceinline__ unsigned long long reducers_scan_u64(unsigned long long v, unsigned long long &total,
+                                                                SharedState &sh)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += y;
+    }
+    if (NAMED)
+        reducers_sync();
+    else
+        __syncthreads();
+    if (lane == 31)
+        sh.warp_sum[wid] = v;
+    if (NAMED)
+        reducers_sync();
+    else
+        __syncthreads();
+    unsigned long long before = 0, t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < wid)
+            before += sh.warp_sum[w];
+        t += sh.warp_sum[w];
+    }
+    total = t;
+    return v + before;
+}
+
+// Number of rows sequence i reads: g + 1 target rows, plus g draft rows when
+// sampled; 0 for an invalid draft count.
+__device__ __forceinline__ int seq_cost(const Params &p, int g, float temp)
+{
+    if (g < 0 || g > p.gmax)
+        return 0;
+    return g + 1 + (temp > 0.0f ? g : 0);
+}
+
+// Sequence verified by cluster k.  With p.ordered, clusters take sequences in
+// order of decreasing row count (ties by index), so the longest start first and
+// the grid's tail is made of short ones; the block scheduler dispatches
+// clusters in index order.  Every CTA of the cluster computes the same value.
+// All threads of the CTA call it (blockDim.x >= kThreads).
+__device__ int seq_for_cluster(const Params &p, SharedState &sh, int k)
+{
+    if (!p.ordered)
+        return k;
+    constexpr int kPer = kMaxOrdered / kThreads;
+    const int tid = threadIdx.x;
+    const bool active = tid < kThreads;
+    int cost[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        const int i = tid * kPer + e;
+        cost[e] = (active && i < p.B) ? seq_cost(p, p.num_draft[i], p.temperature[i]) : -1;
+    }
+    if (tid <= kMaxRows)
+        sh.hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        if (cost[e] >= 0)
+            atomicAdd(&sh.hist[cost[e]], 1);
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0, bin = 0;
+        for (int c = kMaxRows; c >= 0; --c) {
+            if (k < run + sh.hist[c]) {
+                bin = c;
+                break;
+            }
+            run += sh.hist[c];
+        }
+        sh.bin = bin;
+        sh.rank_in_bin = k - run;
+    }
+    __syncthreads();
+    const int bin = sh.bin, want = sh.rank_in_bin;
+    int mine = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        mine += cost[e] == bin;
+    // exclusive prefix of 'mine' over threads in index order (contiguous ranges)
+    const int lane = tid & 31, wid = tid >> 5;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (active && lane == 31)
+        sh.cnt[wid] = incl;
+    __syncthreads();
+    int before = incl - mine;
+    for (int w = 0; w < wid && w < kWarps; ++w)
+        before += sh.cnt[w];
+    if (active && before <= want && want < before + mine) {
+        int r = want - before;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            if (cost[e] == bin) {
+                if (r == 0)
+                    sh.seq = tid * kPer + e;
+                --r;
+            }
+    }
+    __syncthreads();
+    return sh.seq;
+}
+
+__device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b, int g, float temp)
+{
+    Seq s;
+    s.b = b;
+    s.g = g;
+    s.gmax = p.gmax;
+    s.V = p.V;
+    s.rank = rank;
+    s.C = C;
+    s.c0 = (int)((long long)p.num_chunks * rank / C);
+    s.c1 = (int)((long long)p.num_chunks * (rank + 1) / C);
+    s.sampled = temp > 0.0f;
+    s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
+    s.rowlen = (size_t)p.V;
+    return s;
+}
+
+// ===========================================================================
+// Kernel 1: register loads (any alignment; the default)
+// ===========================================================================
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Params p)
+{
+    __shared__ SharedState sh;
+    cg::cluster_group cluster = cg::this_cluster();
+    constexpr int W = Elem<T>::W;
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int g = p.num_draft[b];
+    const float temp = p.temperature[b];
+
+    const uint32_t bad = check_inputs(p, b, g, temp);
+    init_diagnostics(p, b, rank);
+    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
+        write_invalid(p, b, rank, bad);
+        return;
+    }
+    if (tid == 0)
+        sh.timeout = 0;
+    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
+
+    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
+
+    // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
+    for (int step = 0; step < nrows; ++step) {
+        const int r = row_at_step(step, g, s.sampled);
+        const T *row = row_ptr<T>(p, s, r);
+        RowAcc acc;
+        acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
+        for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int c = ch + u * kThreads;
+                v[u] = c < s.c1 ? load_chunk<T, ALIGNED>(row, c, s.V) : neg_inf_chunk<T>();
+            }
+            if (s.sampled) {
+                acc.add_soft<T, kUnroll>(v, s.k);
+            } else {
+                acc.add_arg<T, kUnroll>(v, ch * W, kThreads * W);
+            }
+        }
+        const RowStat st = warp_reduce(acc.stat(), s.sampled);
+        if (lane == 0)
+            sh.warp_part[r][wid] = st;
+    }
+    exchange_rows(sh, s, nrows);
+    if (!decide_and_write<T>(p, sh, s))
         return;  // uniform over the cluster; no DSMEM access follows
 
-    // ---- pass 2: inverse-CDF sample from the decided row
-    const bool residual = n < g;
-    const RowStat st = sh.row[n];
-    const RowStat sd = residual ? sh.row[g + 1 + n] : st;
-    const T *trow = trows + (size_t)n * rowlen;
-    const T *drow = drows + (size_t)n * rowlen;
-    const float invzt = 1.0f / (st.hi + st.lo);
-    const float invzd = 1.0f / (sd.hi + sd.lo);
-    const float u = p.uniforms[(size_t)b * (gmax + 1) + gmax];
-    constexpr int W = Elem<T>::W;
-
-    bool use_residual = residual;
+    // ---- pass 2a: slice sums of the decided row's weights.  Chunk c = c0 +
+    // j*kThreads + tid is tile j, lane tid; with p.scan_tiles its float sum is
+    // kept in shared memory for pass 2b.
+    extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
+    const int n = sh.n;
+    bool use_residual = n < g;
+    const T *trow = row_ptr<T>(p, s, n);
+    const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
+    WeightParams wp = weight_params(sh, s, n, use_residual);
+    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
+    const bool keep = tiles <= p.scan_tiles;
     unsigned long long S = 0, P = 0, mine = 0;
+    bool timed_out = false;
+    constexpr int U2 = kUnroll / 2;
     for (int attempt = 0; attempt < 2; ++attempt) {
         unsigned long long acc = 0;
-        for (int c = c0 + tid; c < c1; c += kThreads) {
-            unsigned long long w[W];
-            chunk_weights<T, ALIGNED>(trow, drow, c, V, use_residual, k, -st.m, invzt, -sd.m, invzd, w);
+        for (int j0 = 0; j0 < tiles; j0 += U2) {
+            uint4 tv[U2], dv[U2];
 #pragma unroll
-            for (int e = 0; e < W; ++e)
-                acc += w[e];
+            for (int u = 0; u < U2; ++u) {
+                const int c = s.c0 + (j0 + u) * kThreads + tid;
+                tv[u] = c < s.c1 ? load_chunk<T, ALIGNED>(trow, c, s.V) : neg_inf_chunk<T>();
+                dv[u] = (wp.residual && c < s.c1) ? load_chunk<T, ALIGNED>(drow, c, s.V) : neg_inf_chunk<T>();
+            }
+#pragma unroll
+            for (int u = 0; u < U2; ++u) {
+                const int c = s.c0 + (j0 + u) * kThreads + tid;
+                float sum = 0.0f;
+                if (c < s.c1) {
+                    float w[W];
+                    chunk_weights<T>(tv[u], dv[u], wp, w);
+                    sum = chunk_sum<T>(w);
+                    acc += to_fixed60(sum);
+                }
+                if (keep && j0 + u < tiles)
+                    chunk_sums[(j0 + u) * kThreads + tid] = sum;
+            }
         }
-        mine = block_sum_u64(acc, sh);
-        if (tid < C) {
-            unsigned long long *remote = cluster.map_shared_rank(&sh.recv_sum[attempt][rank], tid);
-            *remote = mine;
-        }
-        cluster_sync_all();
-        S = 0;
-        P = 0;
-        for (int src = 0; src < C; ++src) {
-            const unsigned long long v = sh.recv_sum[attempt][src];
-            if (src < rank)
-                P += v;
-            S += v;
-        }
+        mine = block_sum_u64<kWarps>(acc, sh);
+        exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
         if (S > 0 || !use_residual)
             break;
         use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
+        wp = weight_params(sh, s, n, false);
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
-        p.resid_mass[b] = (float)S * (1.0f / kFixedScale);
+        p.resid_mass[b] = (float)S * kFixedUnit;
 
-    float uu = u;
-    if (!(uu >= 0.0f))
-        uu = 0.0f;
-    if (uu >= 1.0f)
-        uu = __uint_as_float(0x3F7FFFFFu);
-    const unsigned long long theta = scaled_floor(uu, S);  // pick: C_{j-1} <= theta < C_j
+    const unsigned long long theta = scaled_floor(final_uniform(p, s), S);  // pick: C_{j-1} <= theta < C_j
     if (S == 0 || !(P <= theta && theta < P + mine))
         return;  // another CTA owns the sample (S == 0 only for an all-zero bonus row)
+    int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
 
-    unsigned long long carry = P;
-    for (int base = c0; base < c1; base += kThreads) {
-        const int c = base + tid;
-        unsigned long long w[W];
-        unsigned long long sigma = 0;
-        if (c < c1) {
-            chunk_weights<T, ALIGNED>(trow, drow, c, V, use_residual, k, -st.m, invzt, -sd.m, invzd, w);
+    if (keep) {
+        // ---- pass 2b from shared memory: tile totals, the tile holding theta,
+        // a scan inside it, and one reload of the chunk found.
+        const unsigned long long rel = theta - P;  // 0 <= rel < mine
+        for (int j = wid; j < tiles; j += kWarps) {
+            unsigned long long t = 0;
+            for (int i = lane; i < kThreads; i += 32)
+                t += to_fixed60(chunk_sums[j * kThreads + i]);
 #pragma unroll
-            for (int e = 0; e < W; ++e)
-                sigma += w[e];
+            for (int o = 16; o > 0; o >>= 1)
+                t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (lane == 0)
+                sh.tile_tot[j] = t;
+        }
+        __syncthreads();
+        unsigned long long before = 0;
+        int jt = tiles - 1;
+        for (int j = 0; j < tiles; ++j) {
+            if (rel < before + sh.tile_tot[j]) {
+                jt = j;
+                break;
+            }
+            before += sh.tile_tot[j];
+        }
+        const unsigned long long f = to_fixed60(chunk_sums[jt * kThreads + tid]);
+        unsigned long long total;
+        const unsigned long long start = before + reducers_scan_u64<false>(f, total, sh) - f;
+        if (start <= rel && rel < start + f) {
+            const int c = s.c0 + jt * kThreads + tid;
+            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
+            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+            float w[W];
+            chunk_weights<T>(tv, dv, wp, w);
+            *outn = c * W + pick_in_chunk<T>(w, rel - start);
+        }
+        return;
+    }
+
+    // ---- pass 2b, slice too large for shared memory: tiles in order, reloaded
+    unsigned long long carry = P;
+    for (int base = s.c0; base < s.c1; base += kThreads) {
+        const int c = base + tid;
+        float w[W];
+        unsigned long long sigma = 0;
+        if (c < s.c1) {
+            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
+            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+            chunk_weights<T>(tv, dv, wp, w);
+            sigma = chunk_fixed<T>(w);
         }
         unsigned long long total;
-        const unsigned long long incl = block_scan_u64(sigma, total, sh);
+        const unsigned long long incl = reducers_scan_u64<false>(sigma, total, sh);
         const unsigned long long start = carry + incl - sigma;
-        if (c < c1 && start <= theta && theta < start + sigma) {
-            unsigned long long run = start;
-            int j = c * W + W - 1;
-#pragma unroll
-            for (int e = 0; e < W; ++e) {
-                run += w[e];
-                if (theta < run) {
-                    j = c * W + e;
-                    break;
-                }
-            }
-            out[n] = j;
-        }
+        if (c < s.c1 && start <= theta && theta < start + sigma)
+            *outn = c * W + pick_in_chunk<T>(w, theta - start);
         carry += total;
         if (theta < carry)
             break;
+    }
+}
+
+// ===========================================================================
+// Kernel 2: bulk-copy ring (16-byte aligned rows; A/B alternative)
+// ===========================================================================
+// Segment k of a CTA's copy stream lands in ring stage k % kStages; both the
+// producer lane and the reducing warps walk the same sequence of segments.
+struct RingState {
+    uint4 *ring;
+    unsigned long long *full;
+    unsigned long long *empty;
+};
+
+// A CTA that saw one wait run out waits no more (its results are void anyway),
+// so a fault costs at most one wait's bound per CTA.
+__device__ __forceinline__ bool timed_out_before(const SharedState &sh)
+{
+    return *reinterpret_cast<const volatile int *>(&sh.timeout) != 0;
+}
+
+// Producer: waits until stage k % kStages is free, then starts the copy of
+// segment k into it.  Returns false (copy not started) if the wait ran out or
+// an earlier one did.
+__device__ __forceinline__ bool ring_produce(const RingState &rs, const SharedState &sh, uint32_t k,
+                                             const void *src, uint32_t bytes)
+{
+    const uint32_t st = k % kStages, use = k / kStages;
+    if (timed_out_before(sh))
+        return false;
+    if (use > 0 && !mbar_wait(&rs.empty[st], (use - 1) & 1u))
+        return false;
+    mbar_arrive_expect_tx(&rs.full[st], bytes);
+    bulk_copy_g2s(rs.ring + (size_t)st * kSegChunks, src, bytes, &rs.full[st]);
+    return true;
+}
+
+// Reducers: wait for segment k, then read this thread's chunks of it.
+// 'contiguous' picks chunks tid*N .. tid*N+N-1 (prefix order, pass 2b) instead of
+// tid, tid+kThreads, ... (conflict-free, passes 1 and 2a).
+template <typename T>
+__device__ __forceinline__ void ring_consume(const RingState &rs, SharedState &sh, uint32_t k, int count,
+                                             bool contiguous, uint4 (&v)[kChunksPerThread])
+{
+    const uint32_t st = k % kStages;
+    if (!timed_out_before(sh) && !mbar_wait(&rs.full[st], (k / kStages) & 1u))
+        sh.timeout = 1;
+    const uint4 *seg = rs.ring + (size_t)st * kSegChunks;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+        const int i = contiguous ? tid * kChunksPerThread + u : tid + u * kThreads;
+        v[u] = i < count ? seg[i] : neg_inf_chunk<T>();
+    }
+    __syncwarp();
+    if ((tid & 31) == 0)
+        mbar_arrive(&rs.empty[st]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const Params p)
+{
+    extern __shared__ __align__(128) uint4 ring_mem[];
+    __shared__ SharedState sh;
+    __shared__ __align__(8) unsigned long long full_bar[kStages];
+    __shared__ __align__(8) unsigned long long empty_bar[kStages];
+    cg::cluster_group cluster = cg::this_cluster();
+    constexpr int W = Elem<T>::W;
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const bool producer = wid == kWarps;
+    const int g = p.num_draft[b];
+    const float temp = p.temperature[b];
+
+    const uint32_t bad = check_inputs(p, b, g, temp);
+    init_diagnostics(p, b, rank);
+    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
+        write_invalid(p, b, rank, bad);
+        return;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kWarps);
+        }
+        sh.timeout = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
+
+    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
+    const int slice = s.c1 - s.c0;
+    const int nseg = (slice + kSegChunks - 1) / kSegChunks;  // segments per row slice
+    const RingState rs{ring_mem, full_bar, empty_bar};
+    uint32_t k = 0;  // segment counter, identical on both sides
+
+    // ---- pass 1: every needed row slice in one continuous copy stream
+    if (producer) {
+        if (lane == 0) {
+            for (int step = 0; step < nrows; ++step) {
+                const T *row = row_ptr<T>(p, s, row_at_step(step, g, s.sampled));
+                for (int j = 0; j < nseg; ++j) {
+                    const int start = s.c0 + j * kSegChunks;
+                    const int cnt = min(kSegChunks, s.c1 - start);
+                    if (!ring_produce(rs, sh, k + (uint32_t)(step * nseg + j), row + (size_t)start * W,
+                                      (uint32_t)cnt * 16u))
+                        sh.timeout = 1;
+                }
+            }
+        }
+        __syncwarp();
+        k = (uint32_t)(nrows * nseg);
+    } else {
+        for (int step = 0; step < nrows; ++step) {
+            const int r = row_at_step(step, g, s.sampled);
+            RowAcc acc;
+            acc.reset(tid < min(kSegChunks, slice) ? (s.c0 + tid) * W : INT_MAX);
+            for (int j = 0; j < nseg; ++j) {
+                const int start = s.c0 + j * kSegChunks;
+                const int cnt = min(kSegChunks, s.c1 - start);
+                uint4 v[kChunksPerThread];
+                ring_consume<T>(rs, sh, k++, cnt, false, v);
+                if (s.sampled) {
+                    acc.add_soft<T, kChunksPerThread>(v, s.k);
+                } else {
+                    acc.add_arg<T, kChunksPerThread>(v, (start + tid) * W, kThreads * W);
+                }
+            }
+            const RowStat st = warp_reduce(acc.stat(), s.sampled);
+            if (lane == 0)
+                sh.warp_part[r][wid] = st;
+        }
+    }
+    exchange_rows(sh, s, nrows);
+    if (!decide_and_write<T>(p, sh, s))
+        return;  // uniform over the cluster; every copy issued so far has been consumed
+
+    // ---- pass 2a: slice sums of the decided row's weights (streamed again)
+    const int n = sh.n;
+    bool use_residual = n < g;
+    const T *trow = row_ptr<T>(p, s, n);
+    const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
+    WeightParams wp = weight_params(sh, s, n, use_residual);
+    unsigned long long S = 0, P = 0, mine = 0;
+    bool timed_out = false;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const uint32_t per = use_residual ? 2u : 1u;
+        unsigned long long acc = 0;
+        if (producer) {
+            if (lane == 0) {
+                for (int j = 0; j < nseg; ++j) {
+                    const int start = s.c0 + j * kSegChunks;
+                    const uint32_t bytes = (uint32_t)min(kSegChunks, s.c1 - start) * 16u;
+                    if (!ring_produce(rs, sh, k + per * j, trow + (size_t)start * W, bytes))
+                        sh.timeout = 1;
+                    if (use_residual && !ring_produce(rs, sh, k + per * j + 1, drow + (size_t)start * W, bytes))
+                        sh.timeout = 1;
+                }
+            }
+            __syncwarp();
+        } else {
+            for (int j = 0; j < nseg; ++j) {
+                const int start = s.c0 + j * kSegChunks;
+                const int cnt = min(kSegChunks, s.c1 - start);
+                uint4 tv[kChunksPerThread], dv[kChunksPerThread];
+                ring_consume<T>(rs, sh, k + per * j, cnt, false, tv);
+                if (use_residual)
+                    ring_consume<T>(rs, sh, k + per * j + 1, cnt, false, dv);
+#pragma unroll
+                for (int u = 0; u < kChunksPerThread; ++u)
+                    if (tid + u * kThreads < cnt)
+                        acc += chunk_weight_fixed<T>(tv[u], use_residual ? dv[u] : tv[u], wp);
+            }
+        }
+        k += per * (uint32_t)nseg;
+        mine = block_sum_u64<kWarps + 1>(acc, sh);
+        if (sh.timeout)
+            mine |= kTimeoutFlag;
+        exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
+        mine &= ~kTimeoutFlag;
+        if (timed_out || S > 0 || !use_residual)
+            break;
+        use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
+        wp = weight_params(sh, s, n, false);
+    }
+    if (rank == 0 && tid == 0 && p.resid_mass)
+        p.resid_mass[b] = (float)S * kFixedUnit;
+    if (timed_out) {
+        if (rank == 0) {
+            if (tid <= s.gmax)
+                p.out_tokens[(size_t)b * (s.gmax + 1) + tid] = -1;
+            if (tid == 0) {
+                p.out_num[b] = 0;
+                if (p.seq_status)
+                    p.seq_status[b] = SPEC_STATUS_TIMEOUT;
+                if (p.status)
+                    atomicOr(p.status, SPEC_STATUS_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // ---- pass 2b: the CTA whose slice holds floor(u*S) finds the id
+    const unsigned long long theta = scaled_floor(final_uniform(p, s), S);  // pick: C_{j-1} <= theta < C_j
+    if (S == 0 || !(P <= theta && theta < P + mine))
+        return;  // another CTA owns the sample (S == 0 only for an all-zero bonus row)
+    const uint32_t per = use_residual ? 2u : 1u;
+    if (producer) {
+        if (lane == 0) {
+            for (int j = 0; j < nseg; ++j) {
+                const int start = s.c0 + j * kSegChunks;
+                const uint32_t bytes = (uint32_t)min(kSegChunks, s.c1 - start) * 16u;
+                if (!ring_produce(rs, sh, k + per * j, trow + (size_t)start * W, bytes))
+                    sh.timeout = 1;
+                if (use_residual && !ring_produce(rs, sh, k + per * j + 1, drow + (size_t)start * W, bytes))
+                    sh.timeout = 1;
+            }
+        }
+        __syncwarp();
+        return;
+    }
+    unsigned long long carry = P;
+    for (int j = 0; j < nseg; ++j) {
+        const int start = s.c0 + j * kSegChunks;
+        const int cnt = min(kSegChunks, s.c1 - start);
+        uint4 tv[kChunksPerThread], dv[kChunksPerThread];
+        ring_consume<T>(rs, sh, k + per * j, cnt, true, tv);
+        if (use_residual)
+            ring_consume<T>(rs, sh, k + per * j + 1, cnt, true, dv);
+        if (theta < carry)
+            continue;  // found in an earlier segment: drain the stream only (uniform)
+        unsigned long long sig[kChunksPerThread];
+        unsigned long long L = 0;
+#pragma unroll
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int i = tid * kChunksPerThread + u;
+            sig[u] = i < cnt ? chunk_weight_fixed<T>(tv[u], use_residual ? dv[u] : tv[u], wp) : 0ull;
+            L += sig[u];
+        }
+        unsigned long long total;
+        const unsigned long long incl = reducers_scan_u64<true>(L, total, sh);
+        unsigned long long start_u = carry + incl - L;
+        if (start_u <= theta && theta < start_u + L) {
+#pragma unroll
+            for (int u = 0; u < kChunksPerThread; ++u) {
+                if (start_u <= theta && theta < start_u + sig[u]) {
+                    float w[W];
+                    chunk_weights<T>(tv[u], use_residual ? dv[u] : tv[u], wp, w);
+                    const int c = start + tid * kChunksPerThread + u;
+                    p.out_tokens[(size_t)b * (s.gmax + 1) + n] = c * W + pick_in_chunk<T>(w, theta - start_u);
+                }
+                start_u += sig[u];
+            }
+        }
+        carry += total;
+    }
+    reducers_sync();
+    if (sh.timeout && tid == 0) {
+        p.out_tokens[(size_t)b * (s.gmax + 1) + n] = -1;
+        if (p.status)
+            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
     }
 }
 
@@ -713,117 +1430,179 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Params p)
 // ---------------------------------------------------------------------------
 using KernelFn = void (*)(Params);
 
-KernelFn kernel_for(spec_dtype dt, bool aligned)
+enum KernelKind { kKindRing = 0, kKindScalarAligned = 1, kKindScalar = 2, kKinds = 3 };
+
+KernelFn kernel_for(spec_dtype dt, int kind)
 {
-    if (dt == SPEC_BF16)
-        return aligned ? spec_verify_kernel<__nv_bfloat16, true> : spec_verify_kernel<__nv_bfloat16, false>;
-    return aligned ? spec_verify_kernel<float, true> : spec_verify_kernel<float, false>;
+    if (dt == SPEC_BF16) {
+        if (kind == kKindRing)
+            return spec_verify_ring_kernel<__nv_bfloat16>;
+        return kind == kKindScalarAligned ? spec_verify_stream_kernel<__nv_bfloat16, true>
+                                          : spec_verify_stream_kernel<__nv_bfloat16, false>;
+    }
+    if (kind == kKindRing)
+        return spec_verify_ring_kernel<float>;
+    return kind == kKindScalarAligned ? spec_verify_stream_kernel<float, true> : spec_verify_stream_kernel<float, false>;
 }
 
-int kernel_slot(spec_dtype dt, bool aligned) { return (dt == SPEC_BF16 ? 2 : 0) + (aligned ? 1 : 0); }
+int kernel_threads(int kind) { return kind == kKindRing ? kTmaThreads : kThreads; }
+// Largest dynamic shared memory a kernel kind is launched with: the ring, or
+// the register kernel's chunk sums.
+int kernel_dyn_smem(int kind) { return kind == kKindRing ? kRingBytes : kMaxScanTiles * kThreads * 4; }
+int variant_slot(spec_dtype dt, int kind) { return (dt == SPEC_BF16 ? kKinds : 0) + kind; }
+int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4; }
+int chunk_width(spec_dtype dt) { return dt == SPEC_BF16 ? 8 : 4; }
+int elem_size(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
 
 constexpr int kMaxDevices = 64;
-// Per-device cache: SM count, and per kernel variant and cluster size whether
-// the size is launchable (0 unknown, 1 yes, 2 no).  Idempotent; safe to race.
+// Per-device caches (idempotent, safe to race): SM count; whether the kernel
+// attributes were applied; per variant and cluster size whether the size can be
+// resident (0 unknown, 1 yes, 2 no).
 std::atomic<int> g_sm_count[kMaxDevices];
-std::atomic<int> g_cluster_ok[kMaxDevices][4][5];
-std::atomic<int> g_nonportable_set[kMaxDevices][4];
+std::atomic<int> g_attrs[kMaxDevices][2 * kKinds];
+std::atomic<int> g_cluster_ok[kMaxDevices][2 * kKinds][5];
 
-int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4; }
+spec_status current_device(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    if (*dev < 0 || *dev >= kMaxDevices)
+        return SPEC_ERR_UNSUPPORTED;
+    return SPEC_OK;
+}
 
 spec_status device_sm_count(int dev, int *out)
 {
-    if (dev < 0 || dev >= kMaxDevices)
-        return SPEC_ERR_UNSUPPORTED;
     int v = g_sm_count[dev].load(std::memory_order_relaxed);
     if (v <= 0) {
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
             return SPEC_ERR_CUDA;
+        }
         g_sm_count[dev].store(v, std::memory_order_relaxed);
     }
     *out = v;
     return SPEC_OK;
 }
 
-// Whether clusters of C CTAs of this kernel can be resident on the device.
-spec_status cluster_launchable(int dev, spec_dtype dt, bool aligned, int C, bool *ok)
+// Applies the kernel attributes once per device: dynamic shared memory above
+// the 48 KB default (ring kernel) and clusters of 16 CTAs.
+bool prepare_kernel(int dev, spec_dtype dt, int kind)
 {
-    const int slot = kernel_slot(dt, aligned), lc = log2_cluster(C);
-    int state = g_cluster_ok[dev][slot][lc].load(std::memory_order_relaxed);
-    if (state == 0) {
-        KernelFn fn = kernel_for(dt, aligned);
-        if (C > 8 && !g_nonportable_set[dev][slot].load(std::memory_order_relaxed)) {
-            if (cudaFuncSetAttribute((const void *)fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                g_cluster_ok[dev][slot][lc].store(2, std::memory_order_relaxed);
-                *ok = false;
-                return SPEC_OK;
-            }
-            g_nonportable_set[dev][slot].store(1, std::memory_order_relaxed);
-        }
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)C * 4u);
-        cfg.blockDim = dim3(kThreads);
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)fn, &cfg);
-        if (e != cudaSuccess)
+    const int slot = variant_slot(dt, kind);
+    int st = g_attrs[dev][slot].load(std::memory_order_relaxed);
+    if (st == 0) {
+        const void *fn = (const void *)kernel_for(dt, kind);
+        bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        if (ok && kernel_dyn_smem(kind) > 0)
+            ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kernel_dyn_smem(kind)) ==
+                 cudaSuccess;
+        if (!ok)
             cudaGetLastError();
-        state = (e == cudaSuccess && clusters > 0) ? 1 : 2;
-        g_cluster_ok[dev][slot][lc].store(state, std::memory_order_relaxed);
+        st = ok ? 1 : 2;
+        g_attrs[dev][slot].store(st, std::memory_order_relaxed);
     }
-    *ok = state == 1;
-    return SPEC_OK;
+    return st == 1;
 }
 
-int chunk_width(spec_dtype dt) { return dt == SPEC_BF16 ? 8 : 4; }
-int elem_size(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
+cudaLaunchConfig_t launch_config(int kind, unsigned grid, int C, size_t dyn_smem, cudaStream_t stream,
+                                 cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((unsigned)kernel_threads(kind));
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
 
-// Automatic cluster size: enough CTAs in flight for the streaming sweep (about
-// four per SM), but at least kThreads chunks per CTA and row.
+// Whether clusters of C CTAs of this variant can be resident on the device.
+bool cluster_launchable(int dev, spec_dtype dt, int kind, int C)
+{
+    const int slot = variant_slot(dt, kind), lc = log2_cluster(C);
+    int state = g_cluster_ok[dev][slot][lc].load(std::memory_order_relaxed);
+    if (state == 0) {
+        state = 2;
+        if (prepare_kernel(dev, dt, kind)) {
+            cudaLaunchAttribute attr[1];
+            cudaLaunchConfig_t cfg = launch_config(kind, (unsigned)C * 4u, C, (size_t)kernel_dyn_smem(kind), 0, attr);
+            int clusters = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)kernel_for(dt, kind), &cfg);
+            if (e != cudaSuccess)
+                cudaGetLastError();
+            state = (e == cudaSuccess && clusters > 0) ? 1 : 2;
+        }
+        g_cluster_ok[dev][slot][lc].store(state, std::memory_order_relaxed);
+    }
+    return state == 1;
+}
+
+// Automatic cluster size: the smallest power of two giving about six CTAs per
+// SM in the grid, at most 8 (clusters of 16 CTAs schedule worse) and at least
+// kThreads chunks per CTA and row.  Measured on GB300: B=256, V=128256 is best
+// at 4; B=32 and B=64 at 8.
 int auto_cluster(int B, int num_chunks, int sms)
 {
-    const long long target = 4LL * sms;
+    const long long target = 6LL * sms;
     int C = 1;
-    while (C < kMaxCluster && (long long)B * C < target && num_chunks / (C * 2) >= kThreads)
+    while (C < 8 && (long long)B * C < target && num_chunks / (C * 2) >= kThreads)
         C *= 2;
     return C;
 }
 
-spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int requested, int *C_out)
+struct Shape {
+    int kind;
+    int C;
+};
+
+// Picks the kernel and cluster size.  want_kind: -1 automatic, else a KernelKind.
+spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_kind, int want_C, Shape *out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return SPEC_ERR_CUDA;
-    }
-    int sms = 0;
-    spec_status st = device_sm_count(dev, &sms);
+    int dev = 0, sms = 0;
+    spec_status st = current_device(&dev);
     if (st != SPEC_OK)
         return st;
+    st = device_sm_count(dev, &sms);
+    if (st != SPEC_OK)
+        return st;
+    int kinds[2];
+    int nk = 0;
+    if (want_kind >= 0) {
+        if (!aligned && want_kind != kKindScalar)
+            return SPEC_ERR_UNSUPPORTED;
+        kinds[nk++] = want_kind;
+    } else if (aligned) {
+        // Register loads: on GB300 its 32 resident reducing warps per SM beat the
+        // ring kernel's 16 (the reduction is issue-bound, not load-bound).
+        kinds[nk++] = kKindScalarAligned;
+        kinds[nk++] = kKindRing;
+    } else {
+        kinds[nk++] = kKindScalar;
+    }
     const int W = chunk_width(dt);
     const int num_chunks = (V + W - 1) / W;
-    int C = requested > 0 ? requested : auto_cluster(B, num_chunks, sms);
-    for (;;) {
-        bool ok = false;
-        st = cluster_launchable(dev, dt, aligned, C, &ok);
-        if (st != SPEC_OK)
-            return st;
-        if (ok)
-            break;
-        if (requested > 0 || C == 1)
-            return SPEC_ERR_UNSUPPORTED;
-        C >>= 1;
+    for (int i = 0; i < nk; ++i) {
+        int C = want_C > 0 ? want_C : auto_cluster(B, num_chunks, sms);
+        for (;;) {
+            if (cluster_launchable(dev, dt, kinds[i], C)) {
+                out->kind = kinds[i];
+                out->C = C;
+                return SPEC_OK;
+            }
+            if (want_C > 0 || C == 1)
+                break;
+            C >>= 1;
+        }
     }
-    *C_out = C;
-    return SPEC_OK;
+    return SPEC_ERR_UNSUPPORTED;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -831,15 +1610,22 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 spec_status run(const void *target, const void *draft, const int32_t *tokens, const int32_t *num_draft,
                 const float *uniforms, const float *temperature, int32_t *out_tokens, int32_t *out_num, int B,
                 int gmax, int V, spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
-                float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status, int cluster_req)
+                float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status,
+                const spec_verify_options *opt)
 {
     if (dtype != SPEC_F32 && dtype != SPEC_BF16)
         return SPEC_ERR_UNSUPPORTED;
     if (B < 0 || B > SPEC_MAX_BATCH || gmax < 0 || gmax > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_VOCAB)
         return SPEC_ERR_INVALID_ARG;
-    if (cluster_req != 0 && cluster_req != 1 && cluster_req != 2 && cluster_req != 4 && cluster_req != 8 &&
-        cluster_req != 16)
-        return SPEC_ERR_INVALID_ARG;
+    int want_C = 0, want_kind = -1;
+    if (opt) {
+        want_C = opt->cluster_size;
+        if (want_C != 0 && want_C != 1 && want_C != 2 && want_C != 4 && want_C != 8 && want_C != 16)
+            return SPEC_ERR_INVALID_ARG;
+        if (opt->kernel < 0 || opt->kernel > 2)
+            return SPEC_ERR_INVALID_ARG;
+        want_kind = opt->kernel == 1 ? kKindRing : opt->kernel == 2 ? kKindScalarAligned : -1;
+    }
     if (B == 0)
         return SPEC_OK;
     if (!target || !num_draft || !uniforms || !temperature || !out_tokens || !out_num)
@@ -856,9 +1642,11 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (gmax == 0 || aligned16(draft)) &&
                          ((size_t)V * (size_t)es) % 16 == 0;
+    if (!aligned && want_kind == kKindScalarAligned)
+        want_kind = kKindScalar;  // register loads work at any alignment
 
-    int C = 1;
-    spec_status st = resolve_shape(B, V, dtype, aligned, cluster_req, &C);
+    Shape shp;
+    spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp);
     if (st != SPEC_OK)
         return st;
 
@@ -882,20 +1670,16 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     prm.gmax = gmax;
     prm.V = V;
     prm.num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
+    const int slice = (prm.num_chunks + shp.C - 1) / shp.C;
+    const int tiles = (slice + kThreads - 1) / kThreads;
+    prm.scan_tiles = (shp.kind != kKindRing && tiles <= kMaxScanTiles) ? tiles : 0;
+    prm.ordered = B <= kMaxOrdered ? 1 : 0;
+    const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)B * (unsigned)C);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, aligned), prm);
+    cudaLaunchConfig_t cfg =
+        launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, shp.kind), prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
@@ -914,7 +1698,7 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
 {
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, nullptr, nullptr, nullptr, nullptr,
-               nullptr, nullptr, 0);
+               nullptr, nullptr, nullptr);
 }
 
 spec_status spec_verify_debug(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
@@ -925,17 +1709,17 @@ spec_status spec_verify_debug(const void *target_logits, const void *draft_logit
 {
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, p_hat, q_hat, logz_t, logz_d, resid_mass,
-               seq_status, 0);
+               seq_status, nullptr);
 }
 
 spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                            const int32_t *num_draft, const float *uniforms, const float *temperature,
                            int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
-                           spec_dtype dtype, uint32_t *status, void *stream, int cluster_size)
+                           spec_dtype dtype, uint32_t *status, void *stream, const spec_verify_options *options)
 {
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, nullptr, nullptr, nullptr, nullptr,
-               nullptr, nullptr, cluster_size);
+               nullptr, nullptr, options);
 }
 
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
@@ -947,16 +1731,16 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
         V > SPEC_MAX_VOCAB)
         return SPEC_ERR_INVALID_ARG;
     const bool aligned = ((size_t)V * (size_t)elem_size(dtype)) % 16 == 0;
-    int C = 1;
-    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, 0, &C);
+    Shape shp;
+    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, -1, 0, &shp);
     if (st != SPEC_OK)
         return st;
     if (cluster_size)
-        *cluster_size = C;
+        *cluster_size = shp.C;
     if (num_ctas)
-        *num_ctas = B * C;
+        *num_ctas = B * shp.C;
     if (threads_per_cta)
-        *threads_per_cta = kThreads;
+        *threads_per_cta = kernel_threads(shp.kind);
     return SPEC_OK;
 }
 

@@ -64,8 +64,10 @@ def test_host_argument_checks(lib, over, code):
     assert _call(lib, **over) == code
 
 
-def test_cluster_size_argument_checked(lib):
+@pytest.mark.parametrize("cluster,kernel", [(3, 0), (32, 0), (-1, 0), (0, 3), (0, -1)])
+def test_launch_options_checked(lib, cluster, kernel):
     vp = ctypes.c_void_p
     f = vp(0x10000)
-    rc = lib.spec_verify_ex(f, f, f, f, f, f, f, f, 4, 4, 1024, 1, None, None, 3)
+    opts = _native.Options(cluster, kernel)
+    rc = lib.spec_verify_ex(f, f, f, f, f, f, f, f, 4, 4, 1024, 1, None, None, ctypes.byref(opts))
     assert rc == 1

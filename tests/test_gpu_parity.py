@@ -71,18 +71,34 @@ def test_resid_mass_matches_oracle(sv, oracle_mod):
 
 
 @gpu
-def test_cluster_sizes_agree(sv, oracle_mod):
-    """Every cluster size gives the oracle's result (the split of rows over CTAs is invisible)."""
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_cluster_sizes_and_kernels_agree(sv, oracle_mod, kernel):
+    """Both kernels (bulk-copy ring, register loads) at every cluster size give the
+    oracle's result: the split of rows over CTAs is invisible."""
     import torch
 
     batch = workloads.make_config(4, B=12)
     ref = oracle_mod.verify_batch(batch)
     dev = sv.to_device(batch)
     for C in (1, 2, 4, 8, 16):
-        toks, num = sv.verify(**dev, cluster_size=C)
+        toks, num = sv.verify(**dev, cluster_size=C, kernel=kernel)
         torch.cuda.synchronize()
         rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref)
         assert rep.mismatches_far == 0, (C, str(rep), rep.far_detail[:3])
+
+
+@gpu
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_register_kernel_parity(sv, oracle_mod, cfg):
+    """The register-load kernel on the aligned workloads (the ring kernel's default)."""
+    import torch
+
+    batch = workloads.make_config(cfg, B=64 if cfg == 5 else None)
+    ref = oracle_mod.verify_batch(batch)
+    toks, num = sv.verify(**sv.to_device(batch), kernel=2)
+    torch.cuda.synchronize()
+    rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref)
+    assert rep.mismatches_far == 0, (str(rep), rep.far_detail[:3])
 
 
 @gpu
