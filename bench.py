@@ -269,7 +269,8 @@ def run_ours(args):
     if args.kernel != "auto":
         threads = 288 if args.kernel == "ring" else 256
 
-    kernel = {"auto": sv.KERNEL_AUTO, "stream": sv.KERNEL_REGISTER, "ring": sv.KERNEL_RING}[args.kernel]
+    kernel = {"auto": sv.KERNEL_AUTO, "stream": sv.KERNEL_REGISTER, "ring": sv.KERNEL_RING,
+              "early": sv.KERNEL_EARLY}[args.kernel]
 
     def step():
         sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=stream,
@@ -388,8 +389,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--kernel", choices=["auto", "stream", "ring"], default="auto",
-                    help="kernel choice (A/B measurement; auto = the library's default)")
+    ap.add_argument("--kernel", choices=["auto", "stream", "ring", "early"], default="auto",
+                    help="kernel choice (A/B measurement; auto = the library's default full sweep; "
+                         "early = row-ordered early exit)")
     ap.add_argument("--cluster", type=int, default=0, choices=[0, 1, 2, 4, 8, 16],
                     help="CTAs per sequence (0 = the library's default)")
     ap.add_argument("--quick", action="store_true", help="skip e2e, clocks and the CPU baseline (profiling)")

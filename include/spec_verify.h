@@ -110,6 +110,21 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
                         int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                         spec_dtype dtype, uint32_t *status, void *stream);
 
+/* Launch options (tuning, A/B measurement and the early-exit variant; the
+ * emitted tokens do not depend on them). */
+typedef struct spec_verify_options {
+    int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1, 2, 4, 8 or 16 */
+    int kernel;       /* 0 = automatic (full sweep, register loads);
+                         1 = full sweep through a bulk-copy ring (16-byte aligned rows only,
+                             else SPEC_ERR_UNSUPPORTED);
+                         2 = full sweep, register loads;
+                         3 = row-ordered early exit: position i's rows are read, reduced
+                             and tested before position i+1's, and no row after the first
+                             rejection is read (n+1 target and min(n+1, g) draft rows per
+                             sequence; the method needs nothing after the cut, "Speculative
+                             Decoding" ch.2).  Diagnostics then cover the rows read only. */
+} spec_verify_options;
+
 /* Same round, plus optional float32 diagnostics for tests (any may be NULL):
  *   p_hat [B, gamma_max]     p_i(x_i) for i < g of sampled sequences, NaN elsewhere
  *   q_hat [B, gamma_max]     q_i(x_i), same positions
@@ -119,19 +134,14 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
  *   resid_mass [B]           total weight S of the decided row of a sampled
  *                            sequence (residual mass, or ~1 for a bonus row)
  *   seq_status [B]           SPEC_STATUS_* bits of each sequence (0 = valid)
- * The diagnostic rows are computed for every i <= g, also after the cut. */
+ * The diagnostic rows are computed for every i <= g, also after the cut (with
+ * the full-sweep kernels).  options: as for spec_verify_ex (NULL = automatic). */
 spec_status spec_verify_debug(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                               const int32_t *num_draft, const float *uniforms, const float *temperature,
                               int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                               spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
-                              float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status);
-
-/* Launch options (tuning and A/B measurement; results do not depend on them). */
-typedef struct spec_verify_options {
-    int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1, 2, 4, 8 or 16 */
-    int kernel;       /* 0 = automatic; 1 = bulk-copy ring (16-byte aligned rows only, else
-                         SPEC_ERR_UNSUPPORTED); 2 = register loads */
-} spec_verify_options;
+                              float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status,
+                              const spec_verify_options *options);
 
 /* spec_verify with explicit launch options (NULL = automatic).  Returns
  * SPEC_ERR_UNSUPPORTED if the device cannot co-schedule the requested shape. */

@@ -101,8 +101,9 @@ def _stream_handle(stream, device):
 
 
 KERNEL_AUTO = 0
-KERNEL_RING = 1      # bulk-copy ring (16-byte aligned rows)
-KERNEL_REGISTER = 2  # register loads
+KERNEL_RING = 1      # full sweep through a bulk-copy ring (16-byte aligned rows)
+KERNEL_REGISTER = 2  # full sweep, register loads
+KERNEL_EARLY = 3     # row-ordered early exit: no row after the first rejection is read
 
 
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
@@ -113,7 +114,7 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     ``status``: optional int32 CUDA tensor of one element receiving the
     per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
     ``cluster_size``: 0 = automatic, else 1/2/4/8/16 CTAs per sequence.
-    ``kernel``: KERNEL_AUTO, KERNEL_RING or KERNEL_REGISTER (A/B measurement).
+    ``kernel``: KERNEL_AUTO, KERNEL_RING, KERNEL_REGISTER or KERNEL_EARLY.
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
@@ -131,7 +132,8 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     return out_tokens, out_num_accepted
 
 
-def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, stream=None):
+def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, stream=None,
+                 cluster_size: int = 0, kernel: int = KERNEL_AUTO):
     """verify() plus the float32 diagnostics of spec_verify_debug (a dict of tensors)."""
     import torch
 
@@ -153,7 +155,8 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
                                _ptr(uniforms), _ptr(temperature), _ptr(out_tokens), _ptr(out_num), B, gmax, V,
                                code, _ptr(d["status"]), _stream_handle(stream, dev), _ptr(d["p_hat"]),
                                _ptr(d["q_hat"]), _ptr(d["logz_t"]), _ptr(d["logz_d"]), _ptr(d["resid_mass"]),
-                               _ptr(d["seq_status"]))
+                               _ptr(d["seq_status"]),
+                               ctypes.byref(_native.Options(int(cluster_size), int(kernel))))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_debug")
     d["out_tokens"] = out_tokens

@@ -73,7 +73,7 @@ def load() -> ctypes.CDLL:
         common = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
         lib.spec_verify.argtypes = common
         lib.spec_verify.restype = i32
-        lib.spec_verify_debug.argtypes = common + [vp] * 6
+        lib.spec_verify_debug.argtypes = common + [vp] * 7
         lib.spec_verify_debug.restype = i32
         lib.spec_verify_ex.argtypes = common + [vp]
         lib.spec_verify_ex.restype = i32

@@ -580,12 +580,16 @@ struct SharedState {
     int hist[kMaxRows + 1];
     int cnt[kWarps];
     int seq;
+    int seq_g;
+    float seq_temp;
     int bin;
     int rank_in_bin;
     int recv_flag[kMaxCluster];
+    RowStat recv_pos[2][kMaxCluster][2];  // early-exit kernel: [position parity][source rank][t / d]
     int n;
     int bits;
     int timeout;
+    int stop;
 };
 
 struct Seq {
@@ -595,14 +599,17 @@ struct Seq {
     size_t rowlen;
 };
 
-// Validates the sequence's inputs (identical in every CTA of the cluster).
+// Problems that decide which rows would be read: a bad draft count or
+// temperature (identical in every CTA of the cluster).  Drafted ids are checked
+// here only on this error path; otherwise the decision checks them, one lane
+// per position, off the critical path.
 __device__ __forceinline__ uint32_t check_inputs(const Params &p, int b, int g, float temp)
 {
-    uint32_t bad = 0;
     if (g < 0 || g > p.gmax)
         return SPEC_STATUS_BAD_NUM_DRAFT;
-    if (isnan(temp) || isinf(temp) || temp < 0.0f || (temp > 0.0f && temp < FLT_MIN))
-        bad |= SPEC_STATUS_BAD_TEMPERATURE;
+    if (!(isnan(temp) || isinf(temp) || temp < 0.0f || (temp > 0.0f && temp < FLT_MIN)))
+        return 0;
+    uint32_t bad = SPEC_STATUS_BAD_TEMPERATURE;
     for (int i = 0; i < g; ++i) {
         const int x = p.tokens[(size_t)b * p.gmax + i];
         if (x < 0 || x >= p.V)
@@ -700,30 +707,52 @@ __device__ __forceinline__ void exchange_rows(SharedState &sh, const Seq &s, int
 // Accept decisions (warp 0: lane i tests draft position i; a ballot finds the
 // cut) and rank 0's output writes.  Returns true if the sequence goes on to
 // pass 2 (sampled and valid).  All threads call it.
-template <typename T> __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s)
+// What warp 0's lane i needs for position i's decision, loaded before pass 1
+// so the loads overlap the sweep: the drafted id and (sampled) the target and
+// draft logits at it.
+struct Gathered {
+    int x;
+    float lt, ld;
+};
+
+template <typename T> __device__ __forceinline__ Gathered gather_position(const Params &p, const Seq &s, int i)
+{
+    Gathered gt{-1, 0.0f, 0.0f};
+    if (i >= s.g)
+        return gt;
+    gt.x = p.tokens[(size_t)s.b * s.gmax + i];
+    if (s.sampled && gt.x >= 0 && gt.x < s.V) {
+        const T *tr = row_ptr<T>(p, s, i), *dr = row_ptr<T>(p, s, s.g + 1 + i);
+        if (sizeof(T) == 2) {
+            gt.lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[gt.x]);
+            gt.ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[gt.x]);
+        } else {
+            gt.lt = reinterpret_cast<const float *>(tr)[gt.x];
+            gt.ld = reinterpret_cast<const float *>(dr)[gt.x];
+        }
+    }
+    return gt;
+}
+
+template <typename T>
+__device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s, const Gathered &gt)
 {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int b = s.b, g = s.g, gmax = s.gmax;
     if (wid == 0) {
-        bool ok = false, valid = true;
+        bool ok = false, valid = true, tok_bad = false;
         float phat = 0.0f, qhat = 0.0f;
         if (lane < g) {
-            const int x = p.tokens[(size_t)b * gmax + lane];
-            if (!s.sampled) {
+            const int x = gt.x;
+            tok_bad = x < 0 || x >= p.V;
+            if (tok_bad) {
+                // an invalid id: no gather; the sequence is reported invalid below
+            } else if (!s.sampled) {
                 ok = x == sh.row[lane].idx;
             } else {
                 const RowStat st = sh.row[lane], sd = sh.row[g + 1 + lane];
                 valid = soft_row_ok(st) && soft_row_ok(sd);
-                const T *tr = row_ptr<T>(p, s, lane);
-                const T *dr = row_ptr<T>(p, s, g + 1 + lane);
-                float lt, ld;
-                if (sizeof(T) == 2) {
-                    lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[x]);
-                    ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[x]);
-                } else {
-                    lt = reinterpret_cast<const float *>(tr)[x];
-                    ld = reinterpret_cast<const float *>(dr)[x];
-                }
+                const float lt = gt.lt, ld = gt.ld;
                 phat = ex2_approx(fmaf(lt, s.k, -st.m)) / (st.hi + st.lo);
                 qhat = ex2_approx(fmaf(ld, s.k, -sd.m)) / (sd.hi + sd.lo);
                 ok = valid && (p.uniforms[(size_t)b * (gmax + 1) + lane] * qhat < phat);
@@ -735,7 +764,9 @@ template <typename T> __device__ bool decide_and_write(const Params &p, SharedSt
         const unsigned fail = ~pass & lanes;
         const int n = fail ? __ffs(fail) - 1 : g;
         uint32_t bits = 0;
-        if (s.sampled && (n < g ? !((fine >> n) & 1u) : !soft_row_ok(sh.row[g])))
+        if (__ballot_sync(0xffffffffu, tok_bad))
+            bits = SPEC_STATUS_BAD_TOKEN;
+        else if (s.sampled && (n < g ? !((fine >> n) & 1u) : !soft_row_ok(sh.row[g])))
             bits = SPEC_STATUS_BAD_LOGITS;
         int flag = 0;
         for (int c = 0; c < s.C; ++c)
@@ -900,23 +931,33 @@ __device__ __forceinline__ int seq_cost(const Params &p, int g, float temp)
     return g + 1 + (temp > 0.0f ? g : 0);
 }
 
+struct SeqPick {
+    int b;       // sequence index
+    int g;       // its num_draft
+    float temp;  // its temperature
+};
+
 // Sequence verified by cluster k.  With p.ordered, clusters take sequences in
 // order of decreasing row count (ties by index), so the longest start first and
 // the grid's tail is made of short ones; the block scheduler dispatches
 // clusters in index order.  Every CTA of the cluster computes the same value.
 // All threads of the CTA call it (blockDim.x >= kThreads).
-__device__ int seq_for_cluster(const Params &p, SharedState &sh, int k)
+__device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
 {
     if (!p.ordered)
-        return k;
+        return SeqPick{k, p.num_draft[k], p.temperature[k]};
     constexpr int kPer = kMaxOrdered / kThreads;
     const int tid = threadIdx.x;
     const bool active = tid < kThreads;
-    int cost[kPer];
+    int cost[kPer], gv[kPer];
+    float tv[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
         const int i = tid * kPer + e;
-        cost[e] = (active && i < p.B) ? seq_cost(p, p.num_draft[i], p.temperature[i]) : -1;
+        const bool in = active && i < p.B;
+        gv[e] = in ? p.num_draft[i] : 0;
+        tv[e] = in ? p.temperature[i] : 0.0f;
+        cost[e] = in ? seq_cost(p, gv[e], tv[e]) : -1;
     }
     if (tid <= kMaxRows)
         sh.hist[tid] = 0;
@@ -964,13 +1005,16 @@ __device__ int seq_for_cluster(const Params &p, SharedState &sh, int k)
 #pragma unroll
         for (int e = 0; e < kPer; ++e)
             if (cost[e] == bin) {
-                if (r == 0)
+                if (r == 0) {
                     sh.seq = tid * kPer + e;
+                    sh.seq_g = gv[e];
+                    sh.seq_temp = tv[e];
+                }
                 --r;
             }
     }
     __syncthreads();
-    return sh.seq;
+    return SeqPick{sh.seq, sh.seq_g, sh.seq_temp};
 }
 
 __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b, int g, float temp)
@@ -990,67 +1034,44 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
     return s;
 }
 
-// ===========================================================================
-// Kernel 1: register loads (any alignment; the default)
-// ===========================================================================
+// One row of pass 1 over this CTA's slice, reduced over the warp: online
+// softmax statistics (sampled) or the lowest argmax (greedy).  Eight 16-byte
+// loads per thread are issued before the batch is reduced.
 template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Params p)
+__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
 {
-    __shared__ SharedState sh;
-    cg::cluster_group cluster = cg::this_cluster();
     constexpr int W = Elem<T>::W;
-    const int C = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-    const int b = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int g = p.num_draft[b];
-    const float temp = p.temperature[b];
-
-    const uint32_t bad = check_inputs(p, b, g, temp);
-    init_diagnostics(p, b, rank);
-    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
-        write_invalid(p, b, rank, bad);
-        return;
-    }
-    if (tid == 0)
-        sh.timeout = 0;
-    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
-
-    const Seq s = make_seq(p, C, rank, b, g, temp);
-    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
-
-    // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
-    for (int step = 0; step < nrows; ++step) {
-        const int r = row_at_step(step, g, s.sampled);
-        const T *row = row_ptr<T>(p, s, r);
-        RowAcc acc;
-        acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
-        for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
-            uint4 v[kUnroll];
+    const int tid = threadIdx.x;
+    RowAcc acc;
+    acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
+    for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
+        uint4 v[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int c = ch + u * kThreads;
-                v[u] = c < s.c1 ? load_chunk<T, ALIGNED>(row, c, s.V) : neg_inf_chunk<T>();
-            }
-            if (s.sampled) {
-                acc.add_soft<T, kUnroll>(v, s.k);
-            } else {
-                acc.add_arg<T, kUnroll>(v, ch * W, kThreads * W);
-            }
+        for (int u = 0; u < kUnroll; ++u) {
+            const int c = ch + u * kThreads;
+            v[u] = c < s.c1 ? load_chunk<T, ALIGNED>(row, c, s.V) : neg_inf_chunk<T>();
         }
-        const RowStat st = warp_reduce(acc.stat(), s.sampled);
-        if (lane == 0)
-            sh.warp_part[r][wid] = st;
+        if (s.sampled)
+            acc.add_soft<T, kUnroll>(v, s.k);
+        else
+            acc.add_arg<T, kUnroll>(v, ch * W, kThreads * W);
     }
-    exchange_rows(sh, s, nrows);
-    if (!decide_and_write<T>(p, sh, s))
-        return;  // uniform over the cluster; no DSMEM access follows
+    return warp_reduce(acc.stat(), s.sampled);
+}
 
+// Pass 2 of the register-load kernels for a sampled, valid sequence whose cut
+// is n (sh.row holds the merged statistics of rows t_n and, if n < g, d_n).
+// All threads of the CTA call it; the cluster's CTAs call it together.
+template <typename T, bool ALIGNED>
+__device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n)
+{
+    constexpr int W = Elem<T>::W;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int g = s.g, b = s.b, rank = s.rank;
     // ---- pass 2a: slice sums of the decided row's weights.  Chunk c = c0 +
     // j*kThreads + tid is tile j, lane tid; with p.scan_tiles its float sum is
     // kept in shared memory for pass 2b.
     extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
-    const int n = sh.n;
     bool use_residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
     const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
@@ -1161,6 +1182,214 @@ __global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Para
 }
 
 // ===========================================================================
+// Kernel 1: register loads (any alignment; the default)
+// ===========================================================================
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Params p)
+{
+    __shared__ SharedState sh;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const int b = pick.b, g = pick.g;
+    const float temp = pick.temp;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    const uint32_t bad = check_inputs(p, b, g, temp);
+    init_diagnostics(p, b, rank);
+    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
+        write_invalid(p, b, rank, bad);
+        return;
+    }
+    if (tid == 0)
+        sh.timeout = 0;
+    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
+
+    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
+    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
+
+    // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
+    for (int step = 0; step < nrows; ++step) {
+        const int r = row_at_step(step, g, s.sampled);
+        const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, r));
+        if (lane == 0)
+            sh.warp_part[r][wid] = st;
+    }
+    exchange_rows(sh, s, nrows);
+    if (!decide_and_write<T>(p, sh, s, gt))
+        return;  // uniform over the cluster; no DSMEM access follows
+    stream_pass2<T, ALIGNED>(p, sh, s, sh.n);
+}
+
+// ===========================================================================
+// Kernel 3: row-ordered early exit (register loads; variant)
+// ===========================================================================
+// Positions are verified in order: the rows of position i (t_i, plus d_i for a
+// sampled sequence) are streamed, reduced over the cluster and tested before
+// any row of position i+1 is read, and the first rejection ends the sweep.  The
+// method needs no row after the cut (drafts after a rejection are discarded:
+// "Speculative Decoding", ch.2), so a round reads n+1 target rows and
+// min(n+1, g) draft rows instead of g+1 and g.  The outputs are those of the
+// full sweep; diagnostics exist only for the rows read.
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Params p)
+{
+    __shared__ SharedState sh;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const int b = pick.b, g = pick.g;
+    const float temp = pick.temp;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    const uint32_t bad = check_inputs(p, b, g, temp);
+    init_diagnostics(p, b, rank);
+    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
+        write_invalid(p, b, rank, bad);
+        return;
+    }
+    if (tid == 0) {
+        sh.timeout = 0;
+        sh.stop = 0;
+    }
+    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
+    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const int gmax = s.gmax;
+    // every drafted id is checked, as in the full sweep (lane-parallel)
+    if (wid == 0) {
+        const bool tb = lane < g && !(p.tokens[(size_t)b * gmax + lane] >= 0 &&
+                                      p.tokens[(size_t)b * gmax + lane] < s.V);
+        const unsigned any = __ballot_sync(0xffffffffu, tb);
+        if (lane == 0)
+            sh.bits = any ? (int)SPEC_STATUS_BAD_TOKEN : 0;
+    }
+
+    // Positions in order; each ends with one exchange over the cluster and a
+    // decision that every CTA takes identically.  (Streaming position i+1
+    // during position i's exchange was measured slower on the B=256 workload:
+    // the extra position read per rejection costs more than the barrier.)
+    int n = g;
+    uint32_t bits = 0;
+    for (int i = 0; i <= g; ++i) {
+        const int nslot = (s.sampled && i < g) ? 2 : 1;
+        // the decision's two logits at x_i, loaded ahead of the rows
+        float lt = 0.0f, ld = 0.0f;
+        int x = -1;
+        if (tid == 0 && i < g) {
+            x = p.tokens[(size_t)b * gmax + i];
+            if (s.sampled && x >= 0 && x < s.V) {
+                const T *tr = row_ptr<T>(p, s, i), *dr = row_ptr<T>(p, s, g + 1 + i);
+                if (sizeof(T) == 2) {
+                    lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[x]);
+                    ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[x]);
+                } else {
+                    lt = reinterpret_cast<const float *>(tr)[x];
+                    ld = reinterpret_cast<const float *>(dr)[x];
+                }
+            }
+        }
+        for (int slot = 0; slot < nslot; ++slot) {
+            const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, slot ? g + 1 + i : i));
+            if (lane == 0)
+                sh.warp_part[slot][wid] = st;
+        }
+        __syncthreads();
+        if (i == 0)
+            cluster_wait();  // every CTA of the cluster is running: DSMEM is addressable
+        if (tid < nslot) {
+            RowStat v = sh.warp_part[tid][0];
+            for (int w = 1; w < kWarps; ++w)
+                v = s.sampled ? soft_merge(v, sh.warp_part[tid][w]) : arg_merge(v, sh.warp_part[tid][w]);
+            for (int dst = 0; dst < C; ++dst)
+                *cluster.map_shared_rank(&sh.recv_pos[i & 1][rank][tid], dst) = v;
+        }
+        cluster_sync_all();
+        if (tid < nslot) {
+            RowStat v = sh.recv_pos[i & 1][0][tid];
+            for (int src = 1; src < C; ++src)
+                v = s.sampled ? soft_merge(v, sh.recv_pos[i & 1][src][tid]) : arg_merge(v, sh.recv_pos[i & 1][src][tid]);
+            sh.row[tid ? g + 1 + i : i] = v;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int stop = 0;
+            uint32_t bb = (uint32_t)sh.bits;
+            if (bb) {
+                stop = 1;  // invalid drafted id
+            } else if (i == g) {
+                stop = 1;  // every draft accepted: the bonus row was read
+                if (s.sampled && !soft_row_ok(sh.row[g]))
+                    bb = SPEC_STATUS_BAD_LOGITS;
+            } else if (!s.sampled) {
+                stop = x != sh.row[i].idx;
+            } else {
+                const RowStat st = sh.row[i], sd = sh.row[g + 1 + i];
+                if (!(soft_row_ok(st) && soft_row_ok(sd))) {
+                    stop = 1;
+                    bb = SPEC_STATUS_BAD_LOGITS;
+                } else {
+                    const float phat = ex2_approx(fmaf(lt, s.k, -st.m)) / (st.hi + st.lo);
+                    const float qhat = ex2_approx(fmaf(ld, s.k, -sd.m)) / (sd.hi + sd.lo);
+                    stop = !(p.uniforms[(size_t)b * (gmax + 1) + i] * qhat < phat);
+                    if (rank == 0) {
+                        if (p.p_hat)
+                            p.p_hat[(size_t)b * gmax + i] = phat;
+                        if (p.q_hat)
+                            p.q_hat[(size_t)b * gmax + i] = qhat;
+                    }
+                }
+            }
+            sh.stop = stop;
+            sh.n = i;
+            sh.bits = (int)bb;
+        }
+        __syncthreads();
+        if (sh.stop) {
+            n = sh.n;
+            bits = (uint32_t)sh.bits;
+            break;
+        }
+    }
+
+    if (rank == 0) {
+        int32_t *out = p.out_tokens + (size_t)b * (gmax + 1);
+        if (s.sampled && !bits && tid <= n) {
+            const RowStat st = sh.row[tid];
+            if (p.logz_t)
+                p.logz_t[(size_t)b * (gmax + 1) + tid] = (st.m + log2f(st.hi + st.lo)) * kLn2;
+            if (tid < g && p.logz_d) {
+                const RowStat sd = sh.row[g + 1 + tid];
+                p.logz_d[(size_t)b * gmax + tid] = (sd.m + log2f(sd.hi + sd.lo)) * kLn2;
+            }
+        }
+        if (tid <= gmax) {
+            int v = -1;
+            if (!bits) {
+                if (tid < n)
+                    v = p.tokens[(size_t)b * gmax + tid];
+                else if (tid == n)
+                    v = s.sampled ? INT_MIN : sh.row[n].idx;  // sampled: written by pass 2
+            }
+            if (v != INT_MIN)
+                out[tid] = v;
+        }
+        if (tid == 0) {
+            p.out_num[b] = bits ? 0 : n;
+            if (p.seq_status)
+                p.seq_status[b] = (int32_t)bits;
+            if (bits && p.status)
+                atomicOr(p.status, bits);
+        }
+    }
+    if (!s.sampled || bits)
+        return;  // uniform over the cluster; no DSMEM access follows
+    stream_pass2<T, ALIGNED>(p, sh, s, n);
+}
+
+// ===========================================================================
 // Kernel 2: bulk-copy ring (16-byte aligned rows; A/B alternative)
 // ===========================================================================
 // Segment k of a CTA's copy stream lands in ring stage k % kStages; both the
@@ -1227,11 +1456,11 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     constexpr int W = Elem<T>::W;
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const int b = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const int b = pick.b, g = pick.g;
+    const float temp = pick.temp;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const bool producer = wid == kWarps;
-    const int g = p.num_draft[b];
-    const float temp = p.temperature[b];
 
     const uint32_t bad = check_inputs(p, b, g, temp);
     init_diagnostics(p, b, rank);
@@ -1256,6 +1485,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     const int nseg = (slice + kSegChunks - 1) / kSegChunks;  // segments per row slice
     const RingState rs{ring_mem, full_bar, empty_bar};
     uint32_t k = 0;  // segment counter, identical on both sides
+    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
 
     // ---- pass 1: every needed row slice in one continuous copy stream
     if (producer) {
@@ -1295,7 +1525,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
         }
     }
     exchange_rows(sh, s, nrows);
-    if (!decide_and_write<T>(p, sh, s))
+    if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; every copy issued so far has been consumed
 
     // ---- pass 2a: slice sums of the decided row's weights (streamed again)
@@ -1430,19 +1660,34 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
 // ---------------------------------------------------------------------------
 using KernelFn = void (*)(Params);
 
-enum KernelKind { kKindRing = 0, kKindScalarAligned = 1, kKindScalar = 2, kKinds = 3 };
+enum KernelKind {
+    kKindRing = 0,
+    kKindScalarAligned = 1,  // full sweep, register loads, 16-byte aligned rows
+    kKindScalar = 2,         // full sweep, register loads, any alignment
+    kKindEarlyAligned = 3,   // early exit, 16-byte aligned rows
+    kKindEarly = 4,          // early exit, any alignment
+    kKinds = 5
+};
+
+template <typename T> KernelFn kernel_for_t(int kind)
+{
+    switch (kind) {
+    case kKindRing:
+        return spec_verify_ring_kernel<T>;
+    case kKindScalarAligned:
+        return spec_verify_stream_kernel<T, true>;
+    case kKindScalar:
+        return spec_verify_stream_kernel<T, false>;
+    case kKindEarlyAligned:
+        return spec_verify_early_kernel<T, true>;
+    default:
+        return spec_verify_early_kernel<T, false>;
+    }
+}
 
 KernelFn kernel_for(spec_dtype dt, int kind)
 {
-    if (dt == SPEC_BF16) {
-        if (kind == kKindRing)
-            return spec_verify_ring_kernel<__nv_bfloat16>;
-        return kind == kKindScalarAligned ? spec_verify_stream_kernel<__nv_bfloat16, true>
-                                          : spec_verify_stream_kernel<__nv_bfloat16, false>;
-    }
-    if (kind == kKindRing)
-        return spec_verify_ring_kernel<float>;
-    return kind == kKindScalarAligned ? spec_verify_stream_kernel<float, true> : spec_verify_stream_kernel<float, false>;
+    return dt == SPEC_BF16 ? kernel_for_t<__nv_bfloat16>(kind) : kernel_for_t<float>(kind);
 }
 
 int kernel_threads(int kind) { return kind == kKindRing ? kTmaThreads : kThreads; }
@@ -1576,7 +1821,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     int kinds[2];
     int nk = 0;
     if (want_kind >= 0) {
-        if (!aligned && want_kind != kKindScalar)
+        if (!aligned && (want_kind == kKindRing || want_kind == kKindScalarAligned || want_kind == kKindEarlyAligned))
             return SPEC_ERR_UNSUPPORTED;
         kinds[nk++] = want_kind;
     } else if (aligned) {
@@ -1622,9 +1867,12 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         want_C = opt->cluster_size;
         if (want_C != 0 && want_C != 1 && want_C != 2 && want_C != 4 && want_C != 8 && want_C != 16)
             return SPEC_ERR_INVALID_ARG;
-        if (opt->kernel < 0 || opt->kernel > 2)
+        if (opt->kernel < 0 || opt->kernel > 3)
             return SPEC_ERR_INVALID_ARG;
-        want_kind = opt->kernel == 1 ? kKindRing : opt->kernel == 2 ? kKindScalarAligned : -1;
+        want_kind = opt->kernel == 1   ? kKindRing
+                    : opt->kernel == 2 ? kKindScalarAligned
+                    : opt->kernel == 3 ? kKindEarlyAligned
+                                       : -1;
     }
     if (B == 0)
         return SPEC_OK;
@@ -1644,6 +1892,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
                          ((size_t)V * (size_t)es) % 16 == 0;
     if (!aligned && want_kind == kKindScalarAligned)
         want_kind = kKindScalar;  // register loads work at any alignment
+    if (!aligned && want_kind == kKindEarlyAligned)
+        want_kind = kKindEarly;
 
     Shape shp;
     spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp);
@@ -1705,11 +1955,12 @@ spec_status spec_verify_debug(const void *target_logits, const void *draft_logit
                               const int32_t *num_draft, const float *uniforms, const float *temperature,
                               int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                               spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
-                              float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status)
+                              float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status,
+                              const spec_verify_options *options)
 {
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, p_hat, q_hat, logz_t, logz_d, resid_mass,
-               seq_status, nullptr);
+               seq_status, options);
 }
 
 spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,

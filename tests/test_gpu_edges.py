@@ -14,12 +14,13 @@ gpu = pytest.mark.gpu
 
 
 @gpu
+@pytest.mark.parametrize("kernel", [0, 3])
 @pytest.mark.parametrize("kind", ["zero_draft", "reject_first", "accept_all", "greedy_ties", "neg_inf", "mixed"])
 @pytest.mark.parametrize("V,dtype", [(1023, "bf16"), (50257, "bf16"), (4096, "bf16"), (1023, "f32"),
                                      (32000, "f32")])
-def test_edge_kinds(sv, oracle_mod, kind, V, dtype):
+def test_edge_kinds(sv, oracle_mod, kind, V, dtype, kernel):
     batch = workloads.edge_batch(kind, V=V, gamma=4, B=12, dtype=dtype)
-    rep, d, ref = check_batch(sv, oracle_mod, batch)
+    rep, d, ref = check_batch(sv, oracle_mod, batch, kernel=kernel)
     if kind == "reject_first":
         assert np.all(d["out_num_accepted"] == 0)
     if kind == "accept_all":
@@ -29,11 +30,12 @@ def test_edge_kinds(sv, oracle_mod, kind, V, dtype):
 
 
 @gpu
-def test_large_gamma_and_tiny_vocab(sv, oracle_mod):
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_large_gamma_and_tiny_vocab(sv, oracle_mod, kernel):
     for V in (1, 2, 7, 9, 300):
         for dtype in ("bf16", "f32"):
             batch = workloads.edge_batch("mixed", V=V, gamma=16, B=9, dtype=dtype, seed=V)
-            check_batch(sv, oracle_mod, batch)
+            check_batch(sv, oracle_mod, batch, kernel=kernel)
 
 
 @gpu
@@ -55,7 +57,8 @@ def test_empty_batch_is_noop(sv):
 
 
 @gpu
-def test_unread_rows_are_never_read(sv, oracle_mod):
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_unread_rows_are_never_read(sv, oracle_mod, kernel):
     """NaN in padding rows, in draft rows of greedy sequences and in draft rows
     after... would change results if read; rows are poisoned with NaN here."""
     batch = workloads.make_config(4, B=15)
@@ -67,11 +70,12 @@ def test_unread_rows_are_never_read(sv, oracle_mod):
         if batch.temperature[b] == 0:
             batch.draft[b] = nan
         batch.uniforms[b, g:batch.gmax] = np.nan
-    check_batch(sv, oracle_mod, batch, diagnostics=False)
+    check_batch(sv, oracle_mod, batch, diagnostics=False, kernel=kernel)
 
 
 @gpu
-def test_data_errors_set_status(sv, oracle_mod):
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_data_errors_set_status(sv, oracle_mod, kernel):
     batch = workloads.edge_batch("mixed", V=2048, gamma=3, B=12, seed=3)
     batch.num_draft[:] = 3
     batch.tokens[batch.tokens < 0] = 5
@@ -88,7 +92,7 @@ def test_data_errors_set_status(sv, oracle_mod):
     batch.target[9, 0] = tbits         # row without a finite normaliser
     batch.target[10, 1] = workloads.f64_to_bf16_bits(np.full(2048, np.inf))
     batch.tokens[11, 2] = 3            # valid
-    rep, d, ref = check_batch(sv, oracle_mod, batch, diagnostics=False)
+    rep, d, ref = check_batch(sv, oracle_mod, batch, diagnostics=False, kernel=kernel)
     assert list(d["seq_status"][:9]) == [0, 1, 1, 4, 4, 2, 2, 2, 2]
     assert d["seq_status"][9] == 8
     assert int(d["status"][0]) == 1 | 2 | 4 | 8 | int(d["seq_status"][10])

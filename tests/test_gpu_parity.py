@@ -22,25 +22,26 @@ def sv():
     return m
 
 
-def run_debug(sv, batch):
+def run_debug(sv, batch, kernel=0):
     import torch
 
     dev = sv.to_device(batch)
-    d = sv.verify_debug(**dev)
+    d = sv.verify_debug(**dev, kernel=kernel)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in d.items()}
 
 
-def check_batch(sv, oracle_mod, batch, diagnostics=True):
-    d = run_debug(sv, batch)
+def check_batch(sv, oracle_mod, batch, diagnostics=True, kernel=0):
+    d = run_debug(sv, batch, kernel)
     ref = oracle_mod.verify_batch(batch)
     rep = parity.compare(batch, d["out_tokens"], d["out_num_accepted"], ref, gpu_status=d["seq_status"])
     assert rep.mismatches_far == 0, (str(rep), rep.far_detail[:5])
     if diagnostics:
-        parity.softmax_close(d["p_hat"], ref.p_hat)
-        parity.softmax_close(d["q_hat"], ref.q_hat)
-        parity.softmax_close(d["logz_t"], ref.logz_t, atol=1e-5)
-        parity.softmax_close(d["logz_d"], ref.logz_d, atol=1e-5)
+        sub = kernel == 3  # early exit: diagnostics for the rows read only
+        parity.softmax_close(d["p_hat"], ref.p_hat, subset=sub)
+        parity.softmax_close(d["q_hat"], ref.q_hat, subset=sub)
+        parity.softmax_close(d["logz_t"], ref.logz_t, atol=1e-5, subset=sub)
+        parity.softmax_close(d["logz_d"], ref.logz_d, atol=1e-5, subset=sub)
     assert int(d["status"][0]) == int(np.bitwise_or.reduce(ref.seq_status)) if batch.B else True
     return rep, d, ref
 
@@ -51,6 +52,20 @@ def test_config_parity(sv, oracle_mod, cfg, greedy):
     batch = workloads.make_config(cfg, greedy=greedy)
     rep, d, ref = check_batch(sv, oracle_mod, batch)
     print(f"cfg{cfg}{'-greedy' if greedy else ''}: {rep}")
+
+
+@gpu
+@pytest.mark.parametrize("cfg,greedy", [(1, False), (2, False), (2, True), (3, False), (4, False), (5, False)])
+def test_config_parity_early_exit(sv, oracle_mod, cfg, greedy):
+    """The row-ordered early-exit kernel: same outputs as the oracle (and the full sweep)."""
+    batch = workloads.make_config(cfg, greedy=greedy)
+    rep, d, ref = check_batch(sv, oracle_mod, batch, kernel=3)
+    # no row after the cut was read: diagnostics stop at position n
+    for b in range(batch.B):
+        if batch.temperature[b] > 0:
+            n = int(d["out_num_accepted"][b])
+            assert np.all(np.isnan(d["logz_t"][b, n + 1:]))
+    print(f"early cfg{cfg}{'-greedy' if greedy else ''}: {rep}")
 
 
 @gpu
@@ -71,7 +86,7 @@ def test_resid_mass_matches_oracle(sv, oracle_mod):
 
 
 @gpu
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_cluster_sizes_and_kernels_agree(sv, oracle_mod, kernel):
     """Both kernels (bulk-copy ring, register loads) at every cluster size give the
     oracle's result: the split of rows over CTAs is invisible."""

@@ -24,10 +24,10 @@ gpu = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def run(sv, batch):
+def run(sv, batch, kernel=0):
     import torch
 
-    toks, num = sv.verify(**sv.to_device(batch))
+    toks, num = sv.verify(**sv.to_device(batch), kernel=kernel)
     torch.cuda.synchronize()
     return toks.cpu().numpy(), num.cpu().numpy()
 
@@ -51,8 +51,9 @@ def test_worked_example_monte_carlo(sv):
 
 
 @gpu
+@pytest.mark.parametrize("kernel", [0, 3])
 @pytest.mark.parametrize("V,gamma,zf,seed", [(3, 1, 0.0, 31), (4, 2, 0.0, 32), (4, 3, 0.25, 33), (6, 2, 0.0, 34)])
-def test_output_law_chi_square(sv, V, gamma, zf, seed):
+def test_output_law_chi_square(sv, V, gamma, zf, seed, kernel):
     rng = np.random.default_rng(seed)
 
     def one():
@@ -70,17 +71,18 @@ def test_output_law_chi_square(sv, V, gamma, zf, seed):
     p_st = np.exp(batch.target[0].astype(np.float64))
     q_st = np.exp(batch.draft[0].astype(np.float64))
     law = enumerate_law.outcome_law(p_st / p_st.sum(1, keepdims=True), q_st / q_st.sum(1, keepdims=True))
-    toks, num = run(sv, batch)
+    toks, num = run(sv, batch, kernel)
     stat, pval, bins = law_checks.chi_square_vs_law(law_checks.outcome_keys(toks, num), law)
     assert pval > 1e-3, (stat, pval, bins)
 
 
 @gpu
+@pytest.mark.parametrize("kernel", [0, 3])
 @pytest.mark.parametrize("alpha,gamma", [(0.8, 4), (0.5, 2), (0.5, 7), (0.9, 7), (0.7, 10)])
-def test_mean_tokens_per_round(sv, alpha, gamma):
+def test_mean_tokens_per_round(sv, alpha, gamma, kernel):
     p, q = workloads.alpha_rows(alpha, gamma)
     batch = workloads.tiny_batch(p, q, N=1_000_000, seed=int(alpha * 100) + gamma)
-    _, num = run(sv, batch)
+    _, num = run(sv, batch, kernel)
     z = law_checks.mean_tokens_z(num, analytic.expected_tokens(alpha, gamma))
     assert abs(z) < 4.0, z
 
