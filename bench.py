@@ -312,6 +312,42 @@ def run_ours(args):
     value = aggregate_value(B, ws, args.steps, ms_max / 1e3)
     ms_step = ms_max / args.steps
 
+    # the row-ordered early-exit variant on the same inputs (same outputs; it
+    # reads n+1 target and min(n+1, g) draft rows per sequence)
+    early = None
+    if args.kernel == "auto" and not args.quick:
+        import numpy as np
+
+        ot_e = torch.empty_like(out_tokens)
+        on_e = torch.empty_like(out_num)
+
+        def step_early():
+            sv.verify(**inputs, out_tokens=ot_e, out_num_accepted=on_e, stream=stream,
+                      cluster_size=args.cluster, kernel=sv.KERNEL_EARLY)
+
+        for _ in range(max(args.warmup, 3)):
+            step_early()
+        torch.cuda.synchronize()
+        same = bool(torch.equal(ot_e, out_tokens) and torch.equal(on_e, out_num))
+        n_acc = on_e.cpu().numpy().astype(np.int64)
+        g = batch.num_draft.astype(np.int64)
+        smp = (batch.temperature > 0).astype(np.int64)
+        rows = int(((n_acc + 1) + smp * np.minimum(n_acc + 1, g)).sum())
+        need = rows * batch.V * batch.elem_size
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step_early()
+        z.record(stream)
+        torch.cuda.synchronize()
+        e_ms = reduce_max(a.elapsed_time(z), backend) / args.steps
+        peak_e, _ = measured_peaks()
+        early = {"value": aggregate_value(B, ws, 1, e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+                 "rows_read_per_step": rows, "needed_bytes_per_step": need,
+                 "hbm_gbs_needed": need / (e_ms / 1e3) / 1e9, "frac_of_peak": need / (e_ms / 1e3) / 1e9 / peak_e,
+                 "same_outputs_as_full_sweep": same, "gpu_launches": args.steps}
+
     # end to end through the public API with host buffers: pinned H2D of every
     # input each step, the call, D2H of the outputs
     e2e = None
@@ -371,6 +407,7 @@ def run_ours(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": algo_bytes},
         "gpu_launches": args.steps,
+        "early_exit_variant": early,
         "e2e": e2e,
         "clocks": clocks,
     }
