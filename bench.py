@@ -348,6 +348,35 @@ def run_ours(args):
                  "hbm_gbs_needed": need / (e_ms / 1e3) / 1e9, "frac_of_peak": need / (e_ms / 1e3) / 1e9 / peak_e,
                  "same_outputs_as_full_sweep": same, "gpu_launches": args.steps}
 
+    # target-only sampling (the round with no drafts): one token per sequence
+    # from row t_0 of the same inputs, B rows of V logits
+    sampling = None
+    if args.kernel == "auto" and not args.quick:
+        rows0 = inputs["target_logits"][:, 0].contiguous()
+        u0 = inputs["uniforms"][:, -1].contiguous()
+        out0 = torch.empty((B,), dtype=torch.int32, device=dev)
+
+        def step_sample():
+            sv.sample(rows0, u0, inputs["temperature"], out_tokens=out0, stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step_sample()
+        torch.cuda.synchronize()
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step_sample()
+        z.record(stream)
+        torch.cuda.synchronize()
+        s_ms = reduce_max(a.elapsed_time(z), backend) / args.steps
+        nbytes = rows0.numel() * rows0.element_size()
+        peak_s, _ = measured_peaks()
+        sampling = {"value": aggregate_value(B, ws, 1, s_ms / 1e3), "unit": UNIT, "ms_per_step": s_ms,
+                    "bytes_per_step": nbytes, "hbm_gbs": nbytes / (s_ms / 1e3) / 1e9,
+                    "frac_of_peak": nbytes / (s_ms / 1e3) / 1e9 / peak_s, "gpu_launches": args.steps,
+                    "note": "B rows of V logits; inputs larger than L2 only together with the rest of the bench"}
+
     # end to end through the public API with host buffers: pinned H2D of every
     # input each step, the call, D2H of the outputs
     e2e = None
@@ -408,6 +437,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": algo_bytes},
         "gpu_launches": args.steps,
         "early_exit_variant": early,
+        "target_only_sampling": sampling,
         "e2e": e2e,
         "clocks": clocks,
     }

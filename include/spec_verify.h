@@ -150,6 +150,21 @@ spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, 
                            int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                            spec_dtype dtype, uint32_t *status, void *stream, const spec_verify_options *options);
 
+/* Sampling from one distribution per sequence: y_b ~ softmax(logits[b, :] / T_b)
+ * by inverse CDF with u = uniforms[b] (the smallest id j with u * S < C_j), or
+ * y_b = argmax logits[b, :] (lowest id on ties) when T_b == 0.  This is the
+ * verification round with no drafts: the draft-side sampling of a proposer
+ * ("Fast Inference from Transformers via Speculative Decoding" notes, method
+ * details step 1: x ~ q) and target-only decoding, with the same kernels.
+ *   logits [B, V] dtype; uniforms [B] float32 in [0, 1); temperature [B];
+ *   out_tokens [B] int32 (-1 for a sequence with an invalid temperature or a
+ *   sampled row without a finite normaliser; its bit goes to *status).
+ * options: as for spec_verify_ex (kernel 1, the ring, is not available here).
+ * Same ownership, stream and error rules as spec_verify. */
+spec_status spec_sample(const void *logits, const float *uniforms, const float *temperature, int32_t *out_tokens,
+                        int B, int V, spec_dtype dtype, uint32_t *status, void *stream,
+                        const spec_verify_options *options);
+
 /* Launch shape spec_verify would use on the current device for these sizes:
  * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any
  * output pointer may be NULL.  Touches the device (attribute queries) but

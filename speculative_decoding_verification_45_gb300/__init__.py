@@ -164,6 +164,33 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
     return d
 
 
+def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=None, cluster_size: int = 0,
+           kernel: int = KERNEL_AUTO):
+    """One token per row: y_b ~ softmax(logits[b] / T_b) by inverse CDF with
+    uniforms[b], or argmax when T_b == 0 (spec_sample).  Draft-side sampling of
+    a proposer, or target-only decoding.  Returns out_tokens [B] int32."""
+    import torch
+
+    if not logits.is_cuda or logits.dim() != 2:
+        raise ValueError("logits must be a [B, V] CUDA tensor")
+    dev = logits.device
+    B, V = logits.shape
+    code = _dtype_code(logits)
+    _check(logits, "logits", logits.dtype, (B, V), dev)
+    _check(uniforms, "uniforms", torch.float32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B,), dev)
+    lib = _native.load()
+    opts = _native.Options(int(cluster_size), int(kernel))
+    rc = lib.spec_sample(_ptr(logits), _ptr(uniforms), _ptr(temperature), _ptr(out_tokens), B, V, code,
+                         _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_sample")
+    return out_tokens
+
+
 def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):
     """(cluster size, CTAs, threads per CTA) the library picks for these sizes on the current device."""
     lib = _native.load()

@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.spec_verify_debug.restype = i32
         lib.spec_verify_ex.argtypes = common + [vp]
         lib.spec_verify_ex.restype = i32
+        lib.spec_sample.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        lib.spec_sample.restype = i32
         lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
         lib.spec_verify_launch_shape.restype = i32
         lib.spec_status_string.argtypes = [i32]

@@ -92,11 +92,11 @@ struct Params {
     const void *target;
     const void *draft;
     const int32_t *tokens;
-    const int32_t *num_draft;
+    const int32_t *num_draft;  // NULL for spec_sample: every sequence has g = 0
     const float *uniforms;
     const float *temperature;
     int32_t *out_tokens;
-    int32_t *out_num;
+    int32_t *out_num;  // NULL for spec_sample (no accepted count)
     uint32_t *status;
     float *p_hat;
     float *q_hat;
@@ -648,7 +648,8 @@ __device__ __forceinline__ void write_invalid(const Params &p, int b, int rank, 
     if (tid <= p.gmax)
         p.out_tokens[(size_t)b * (p.gmax + 1) + tid] = -1;
     if (tid == 0) {
-        p.out_num[b] = 0;
+        if (p.out_num)
+            p.out_num[b] = 0;
         if (p.seq_status)
             p.seq_status[b] = (int32_t)bits;
         if (p.status)
@@ -810,7 +811,8 @@ __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s,
                 out[tid] = v;
         }
         if (tid == 0) {
-            p.out_num[b] = bits ? 0 : n;
+            if (p.out_num)
+                p.out_num[b] = bits ? 0 : n;
             if (p.seq_status)
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
@@ -945,7 +947,7 @@ struct SeqPick {
 __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
 {
     if (!p.ordered)
-        return SeqPick{k, p.num_draft[k], p.temperature[k]};
+        return SeqPick{k, p.num_draft ? p.num_draft[k] : 0, p.temperature[k]};
     constexpr int kPer = kMaxOrdered / kThreads;
     const int tid = threadIdx.x;
     const bool active = tid < kThreads;
@@ -955,7 +957,7 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
     for (int e = 0; e < kPer; ++e) {
         const int i = tid * kPer + e;
         const bool in = active && i < p.B;
-        gv[e] = in ? p.num_draft[i] : 0;
+        gv[e] = (in && p.num_draft) ? p.num_draft[i] : 0;
         tv[e] = in ? p.temperature[i] : 0.0f;
         cost[e] = in ? seq_cost(p, gv[e], tv[e]) : -1;
     }
@@ -1059,29 +1061,141 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
     return warp_reduce(acc.stat(), s.sampled);
 }
 
-// Pass 2 of the register-load kernels for a sampled, valid sequence whose cut
-// is n (sh.row holds the merged statistics of rows t_n and, if n < g, d_n).
-// All threads of the CTA call it; the cluster's CTAs call it together.
+// The owner CTA's search for theta inside its slice (rel = theta - P, the
+// offset from the slice's start on the exact grid).  With 'keep', chunk_sums
+// holds the slice's chunk sums ([tile][lane]); otherwise the slice is scanned
+// tile by tile with reloads.  When rounding leaves rel at or beyond the slice's
+// own total (only on the bonus path, where the slice mass comes from the pass-1
+// partials), the last id of the slice with weight > 0 is taken.  All threads of
+// the CTA call it.
 template <typename T, bool ALIGNED>
-__device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n)
+__device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
+                             const WeightParams &wp, bool keep, const float *chunk_sums, unsigned long long rel,
+                             int32_t *outn)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
+    auto pick_at = [&](int c, unsigned long long r) {
+        const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
+        const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+        float w[W];
+        chunk_weights<T>(tv, dv, wp, w);
+        *outn = c * W + pick_in_chunk<T>(w, r);
+    };
+    if (keep) {
+        for (int j = wid; j < tiles; j += kWarps) {
+            unsigned long long t = 0;
+            for (int i = lane; i < kThreads; i += 32)
+                t += to_fixed60(chunk_sums[j * kThreads + i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (lane == 0)
+                sh.tile_tot[j] = t;
+        }
+        __syncthreads();
+        unsigned long long before = 0;
+        int jt = -1;
+        for (int j = 0; j < tiles; ++j) {
+            if (rel < before + sh.tile_tot[j]) {
+                jt = j;
+                break;
+            }
+            before += sh.tile_tot[j];
+        }
+        if (jt >= 0) {
+            const unsigned long long f = to_fixed60(chunk_sums[jt * kThreads + tid]);
+            unsigned long long total;
+            const unsigned long long start = before + reducers_scan_u64<false>(f, total, sh) - f;
+            if (start <= rel && rel < start + f)
+                pick_at(s.c0 + jt * kThreads + tid, rel - start);
+            return;
+        }
+        // rel beyond the slice's chunk total: the last chunk with weight > 0
+        int last = -1;
+        for (int i = tid; i < tiles * kThreads; i += kThreads)
+            if (chunk_sums[i] > 0.0f)
+                last = i;
+        const int c_last = __reduce_max_sync(0xffffffffu, last);
+        if (lane == 0)
+            sh.cnt[wid] = c_last;
+        __syncthreads();
+        if (tid == 0) {
+            int m = -1;
+            for (int w = 0; w < kWarps; ++w)
+                m = max(m, sh.cnt[w]);
+            if (m >= 0)
+                pick_at(s.c0 + m, ~0ull);  // pick_in_chunk returns the last positive element
+        }
+        return;
+    }
+    // slice too large for shared memory: tiles in order, reloaded
+    unsigned long long carry = 0;
+    int last = -1;
+    for (int base = s.c0; base < s.c1; base += kThreads) {
+        const int c = base + tid;
+        float w[W];
+        unsigned long long sigma = 0;
+        if (c < s.c1) {
+            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
+            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+            chunk_weights<T>(tv, dv, wp, w);
+            sigma = chunk_fixed<T>(w);
+            if (chunk_sum<T>(w) > 0.0f)
+                last = c;
+        }
+        unsigned long long total;
+        const unsigned long long incl = reducers_scan_u64<false>(sigma, total, sh);
+        const unsigned long long start = carry + incl - sigma;
+        if (c < s.c1 && start <= rel && rel < start + sigma)
+            *outn = c * W + pick_in_chunk<T>(w, rel - start);
+        carry += total;
+        if (rel < carry)
+            return;
+    }
+    const int c_last = __reduce_max_sync(0xffffffffu, last);
+    __syncthreads();
+    if (lane == 0)
+        sh.cnt[wid] = c_last;
+    __syncthreads();
+    if (tid == 0) {
+        int m = -1;
+        for (int w = 0; w < kWarps; ++w)
+            m = max(m, sh.cnt[w]);
+        if (m >= 0)
+            pick_at(m, ~0ull);
+    }
+}
+
+// Pass 2 of the register-load kernels for a sampled, valid sequence whose cut
+// is n (sh.row holds the merged statistics of rows t_n and, if n < g, d_n).
+// parts[c * stride] is CTA c's pass-1 partial of row t_n.  All threads of the
+// CTA call it; the cluster's CTAs call it together.
+//   Residual row (n < g): every CTA sums its slice's weights max(0, p - q)
+//     (pass 2a, chunk sums kept in shared memory), the slice sums cross the
+//     cluster, and the CTA whose slice holds floor(u*S) searches it.
+//   Bonus row (n == g, and spec_sample): the weights are p itself, so CTA c's
+//     slice mass is its pass-1 partial over the row's normaliser, known to
+//     every CTA already; only the owner reads its slice again, and nothing
+//     crosses the cluster.
+template <typename T, bool ALIGNED>
+__device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
+                             int stride)
+{
+    constexpr int W = Elem<T>::W;
+    const int tid = threadIdx.x;
     const int g = s.g, b = s.b, rank = s.rank;
-    // ---- pass 2a: slice sums of the decided row's weights.  Chunk c = c0 +
-    // j*kThreads + tid is tile j, lane tid; with p.scan_tiles its float sum is
-    // kept in shared memory for pass 2b.
     extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
-    bool use_residual = n < g;
+    const bool residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
-    const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    WeightParams wp = weight_params(sh, s, n, use_residual);
+    const T *drow = residual ? row_ptr<T>(p, s, g + 1 + n) : trow;
+    WeightParams wp = weight_params(sh, s, n, residual);
     const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
     const bool keep = tiles <= p.scan_tiles;
-    unsigned long long S = 0, P = 0, mine = 0;
-    bool timed_out = false;
     constexpr int U2 = kUnroll / 2;
-    for (int attempt = 0; attempt < 2; ++attempt) {
+    // chunk c = c0 + j*kThreads + tid is tile j, lane tid; returns the thread's fixed-point total
+    auto slice_sums = [&]() {
         unsigned long long acc = 0;
         for (int j0 = 0; j0 < tiles; j0 += U2) {
             uint4 tv[U2], dv[U2];
@@ -1105,7 +1219,43 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
                     chunk_sums[(j0 + u) * kThreads + tid] = sum;
             }
         }
-        mine = block_sum_u64<kWarps>(acc, sh);
+        return acc;
+    };
+    int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
+    const float u = final_uniform(p, s);
+
+    if (!residual) {
+        const RowStat tot = sh.row[n];
+        const float z = tot.hi + tot.lo;
+        unsigned long long S = 0, P = 0, mine = 0;
+        for (int c = 0; c < s.C; ++c) {
+            const RowStat part = parts[c * stride];
+            const float share = (part.hi + part.lo) * pow2_int(part.m - tot.m) / z;
+            const unsigned long long f = to_fixed60(fminf(fmaxf(share, 0.0f), 8.0f));
+            if (c < rank)
+                P += f;
+            if (c == rank)
+                mine = f;
+            S += f;
+        }
+        if (rank == 0 && tid == 0 && p.resid_mass)
+            p.resid_mass[b] = (float)S * kFixedUnit;
+        const unsigned long long theta = scaled_floor(u, S);
+        if (S == 0 || !(P <= theta && theta < P + mine))
+            return;  // another CTA owns the sample
+        if (keep) {
+            slice_sums();
+            __syncthreads();
+        }
+        owner_search<T, ALIGNED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+        return;
+    }
+
+    unsigned long long S = 0, P = 0, mine = 0;
+    bool timed_out = false;
+    bool use_residual = true;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        mine = block_sum_u64<kWarps>(slice_sums(), sh);
         exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
         if (S > 0 || !use_residual)
             break;
@@ -1114,71 +1264,10 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
         p.resid_mass[b] = (float)S * kFixedUnit;
-
-    const unsigned long long theta = scaled_floor(final_uniform(p, s), S);  // pick: C_{j-1} <= theta < C_j
+    const unsigned long long theta = scaled_floor(u, S);  // pick: C_{j-1} <= theta < C_j
     if (S == 0 || !(P <= theta && theta < P + mine))
-        return;  // another CTA owns the sample (S == 0 only for an all-zero bonus row)
-    int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
-
-    if (keep) {
-        // ---- pass 2b from shared memory: tile totals, the tile holding theta,
-        // a scan inside it, and one reload of the chunk found.
-        const unsigned long long rel = theta - P;  // 0 <= rel < mine
-        for (int j = wid; j < tiles; j += kWarps) {
-            unsigned long long t = 0;
-            for (int i = lane; i < kThreads; i += 32)
-                t += to_fixed60(chunk_sums[j * kThreads + i]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (lane == 0)
-                sh.tile_tot[j] = t;
-        }
-        __syncthreads();
-        unsigned long long before = 0;
-        int jt = tiles - 1;
-        for (int j = 0; j < tiles; ++j) {
-            if (rel < before + sh.tile_tot[j]) {
-                jt = j;
-                break;
-            }
-            before += sh.tile_tot[j];
-        }
-        const unsigned long long f = to_fixed60(chunk_sums[jt * kThreads + tid]);
-        unsigned long long total;
-        const unsigned long long start = before + reducers_scan_u64<false>(f, total, sh) - f;
-        if (start <= rel && rel < start + f) {
-            const int c = s.c0 + jt * kThreads + tid;
-            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
-            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
-            float w[W];
-            chunk_weights<T>(tv, dv, wp, w);
-            *outn = c * W + pick_in_chunk<T>(w, rel - start);
-        }
-        return;
-    }
-
-    // ---- pass 2b, slice too large for shared memory: tiles in order, reloaded
-    unsigned long long carry = P;
-    for (int base = s.c0; base < s.c1; base += kThreads) {
-        const int c = base + tid;
-        float w[W];
-        unsigned long long sigma = 0;
-        if (c < s.c1) {
-            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
-            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
-            chunk_weights<T>(tv, dv, wp, w);
-            sigma = chunk_fixed<T>(w);
-        }
-        unsigned long long total;
-        const unsigned long long incl = reducers_scan_u64<false>(sigma, total, sh);
-        const unsigned long long start = carry + incl - sigma;
-        if (c < s.c1 && start <= theta && theta < start + sigma)
-            *outn = c * W + pick_in_chunk<T>(w, theta - start);
-        carry += total;
-        if (theta < carry)
-            break;
-    }
+        return;  // another CTA owns the sample (S == 0 only for an all-zero row)
+    owner_search<T, ALIGNED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
 }
 
 // ===========================================================================
@@ -1220,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Para
     exchange_rows(sh, s, nrows);
     if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED>(p, sh, s, sh.n);
+    stream_pass2<T, ALIGNED>(p, sh, s, sh.n, &sh.recv[0][sh.n], kMaxRows);
 }
 
 // ===========================================================================
@@ -1377,7 +1466,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 out[tid] = v;
         }
         if (tid == 0) {
-            p.out_num[b] = bits ? 0 : n;
+            if (p.out_num)
+                p.out_num[b] = bits ? 0 : n;
             if (p.seq_status)
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
@@ -1386,7 +1476,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     }
     if (!s.sampled || bits)
         return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED>(p, sh, s, n);
+    stream_pass2<T, ALIGNED>(p, sh, s, n, &sh.recv_pos[n & 1][0][0], 2);
 }
 
 // ===========================================================================
@@ -1583,7 +1673,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
             if (tid <= s.gmax)
                 p.out_tokens[(size_t)b * (s.gmax + 1) + tid] = -1;
             if (tid == 0) {
-                p.out_num[b] = 0;
+                if (p.out_num)
+                    p.out_num[b] = 0;
                 if (p.seq_status)
                     p.seq_status[b] = SPEC_STATUS_TIMEOUT;
                 if (p.status)
@@ -1876,8 +1967,10 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     }
     if (B == 0)
         return SPEC_OK;
-    if (!target || !num_draft || !uniforms || !temperature || !out_tokens || !out_num)
+    if (!target || !uniforms || !temperature || !out_tokens)
         return SPEC_ERR_INVALID_ARG;
+    if ((!num_draft || !out_num) && gmax != 0)
+        return SPEC_ERR_INVALID_ARG;  // only the sampler (gamma_max 0) runs without them
     if (gmax > 0 && (!draft || !tokens))
         return SPEC_ERR_INVALID_ARG;
     const uintptr_t es = (uintptr_t)elem_size(dtype);
@@ -1946,6 +2039,8 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
                         int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                         spec_dtype dtype, uint32_t *status, void *stream)
 {
+    if (B > 0 && (!num_draft || !out_num_accepted))
+        return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, nullptr, nullptr, nullptr, nullptr,
                nullptr, nullptr, nullptr);
@@ -1958,6 +2053,8 @@ spec_status spec_verify_debug(const void *target_logits, const void *draft_logit
                               float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status,
                               const spec_verify_options *options)
 {
+    if (B > 0 && (!num_draft || !out_num_accepted))
+        return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, p_hat, q_hat, logz_t, logz_d, resid_mass,
                seq_status, options);
@@ -1968,9 +2065,21 @@ spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, 
                            int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                            spec_dtype dtype, uint32_t *status, void *stream, const spec_verify_options *options)
 {
+    if (B > 0 && (!num_draft || !out_num_accepted))
+        return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
                out_num_accepted, B, gamma_max, V, dtype, status, stream, nullptr, nullptr, nullptr, nullptr,
                nullptr, nullptr, options);
+}
+
+spec_status spec_sample(const void *logits, const float *uniforms, const float *temperature, int32_t *out_tokens,
+                        int B, int V, spec_dtype dtype, uint32_t *status, void *stream,
+                        const spec_verify_options *options)
+{
+    if (options && options->kernel == 1)
+        return SPEC_ERR_UNSUPPORTED;  // the ring kernel is a full-sweep A/B variant only
+    return run(logits, nullptr, nullptr, nullptr, uniforms, temperature, out_tokens, nullptr, B, 0, V, dtype, status,
+               stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, options);
 }
 
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,

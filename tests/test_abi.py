@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_verify_launch_shape",
+    for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_sample", "spec_verify_launch_shape",
               "spec_status_string"):
         assert n in names
 
@@ -71,3 +71,25 @@ def test_launch_options_checked(lib, cluster, kernel):
     opts = _native.Options(cluster, kernel)
     rc = lib.spec_verify_ex(f, f, f, f, f, f, f, f, 4, 4, 1024, 1, None, None, ctypes.byref(opts))
     assert rc == 1
+
+
+@pytest.mark.parametrize("which,code", [("logits", 1), ("uniforms", 1), ("temperature", 1), ("out", 1),
+                                        ("V", 1), ("dtype", 2), ("B0", 0), ("ring", 2)])
+def test_sampler_argument_checks(lib, which, code):
+    vp = ctypes.c_void_p
+    a = dict(logits=0x10000, uniforms=0x10000, temperature=0x10000, out=0x10000, B=4, V=1024, dtype=1, kernel=0)
+    if which in ("logits", "uniforms", "temperature", "out"):
+        a[which] = 0
+    elif which == "V":
+        a["V"] = 0
+    elif which == "dtype":
+        a["dtype"] = 9
+    elif which == "B0":
+        a["B"] = 0
+    elif which == "ring":
+        a["kernel"] = 1
+    opts = _native.Options(0, a["kernel"])
+    rc = lib.spec_sample(vp(a["logits"]) if a["logits"] else None, vp(a["uniforms"]) if a["uniforms"] else None,
+                         vp(a["temperature"]) if a["temperature"] else None, vp(a["out"]) if a["out"] else None,
+                         a["B"], a["V"], a["dtype"], None, None, ctypes.byref(opts))
+    assert rc == code
