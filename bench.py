@@ -377,6 +377,51 @@ def run_ours(args):
                     "frac_of_peak": nbytes / (s_ms / 1e3) / 1e9 / peak_s, "gpu_launches": args.steps,
                     "note": "B rows of V logits; inputs larger than L2 only together with the rest of the bench"}
 
+    # prompt lookup (n-gram proposer) and point-mass verification of its drafts
+    # against the same target rows: contexts of 8192 tokens with repeated spans
+    lookup = None
+    if args.kernel == "auto" and not args.quick:
+        import numpy as np
+
+        ctx_np, lens_np = workloads.ngram_contexts(B, 8192, batch.V, seed=workloads.default_seed(args.config) + 7)
+        ctx = torch.from_numpy(ctx_np).to(dev)
+        lens = torch.from_numpy(lens_np).to(dev)
+        d_tok = torch.empty((B, batch.gmax), dtype=torch.int32, device=dev)
+        d_num = torch.empty((B,), dtype=torch.int32, device=dev)
+        ot_p = torch.empty_like(out_tokens)
+        on_p = torch.empty_like(out_num)
+
+        def step_propose():
+            sv.ngram_propose(ctx, lens, 1, 4, batch.gmax, out_tokens=d_tok, out_num=d_num, stream=stream)
+
+        def step_point():
+            sv.verify(inputs["target_logits"], None, d_tok, d_num, inputs["uniforms"], inputs["temperature"],
+                      out_tokens=ot_p, out_num_accepted=on_p, stream=stream)
+
+        times = {}
+        for name, fn in (("propose", step_propose), ("verify_point", step_point)):
+            for _ in range(max(args.warmup, 3)):
+                fn()
+            torch.cuda.synchronize()
+            barrier()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            z.record(stream)
+            torch.cuda.synchronize()
+            times[name] = reduce_max(a.elapsed_time(z), backend) / args.steps
+        g_prop = d_num.cpu().numpy().astype(np.int64)
+        rows = int((g_prop + 1).sum())
+        vbytes = rows * batch.V * batch.elem_size
+        peak_l, _ = measured_peaks()
+        lookup = {"contexts": f"B={B} x up to 8192 tokens, repeated spans", "min_n": 1, "max_n": 4,
+                  "propose_ms_per_step": times["propose"], "context_bytes": int(ctx_np.nbytes),
+                  "mean_drafts": float(g_prop.mean()), "verify_point_ms_per_step": times["verify_point"],
+                  "verify_point_rows": rows, "verify_point_hbm_gbs": vbytes / (times["verify_point"] / 1e3) / 1e9,
+                  "verify_point_frac_of_peak": vbytes / (times["verify_point"] / 1e3) / 1e9 / peak_l,
+                  "gpu_launches": 2 * args.steps}
+
     # end to end through the public API with host buffers: pinned H2D of every
     # input each step, the call, D2H of the outputs
     e2e = None
@@ -438,6 +483,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "early_exit_variant": early,
         "target_only_sampling": sampling,
+        "prompt_lookup": lookup,
         "e2e": e2e,
         "clocks": clocks,
     }

@@ -32,6 +32,10 @@
  *           and no uniform is read.
  *   Output: out_tokens[b, 0..n-1] = x_0..x_{n-1}, out_tokens[b, n] = y,
  *           out_tokens[b, n+1..gamma_max] = -1, out_num_accepted[b] = n.
+ * Point-mass proposals (draft_logits == NULL; a deterministic proposer such as
+ * prompt lookup, "Speculative Decoding" ch.5): q_i is 1 at x_i, so position i
+ * accepts iff uniforms[b, i] < p_i(x_i) and a rejection samples p_n with x_n
+ * removed (max(0, p - q) for that q).  No draft row is read.
  * Rows after the cut are still read by this full-sweep variant; rows
  * i > g (target) and i >= g (draft), and every draft row of a greedy
  * sequence, are never read.
@@ -39,7 +43,7 @@
  * Layout.  All arrays are dense, row-major, on the device of the calling
  * thread's current CUDA context:
  *   target_logits  [B, gamma_max + 1, V]   dtype (SPEC_F32 or SPEC_BF16)
- *   draft_logits   [B, gamma_max, V]       dtype
+ *   draft_logits   [B, gamma_max, V]       dtype, or NULL for point-mass proposals
  *   draft_tokens   [B, gamma_max]          int32
  *   num_draft      [B]                     int32
  *   uniforms       [B, gamma_max + 1]      float32 in [0, 1)
@@ -123,6 +127,11 @@ typedef struct spec_verify_options {
                              rejection is read (n+1 target and min(n+1, g) draft rows per
                              sequence; the method needs nothing after the cut, "Speculative
                              Decoding" ch.2).  Diagnostics then cover the rows read only. */
+    uint64_t *counters; /* optional device array [3] (8-byte aligned), accumulated with atomics:
+                           += drafted ids, += accepted ids, += verified sequences (valid ones).
+                           Their ratio is the acceptance rate; accepted / sequences + 1 the mean
+                           tokens per round (the counts a serving engine exports, per
+                           "Speculative Decoding으로 LLM 추론 속도 높이기", vLLM section).  NULL: none. */
 } spec_verify_options;
 
 /* Same round, plus optional float32 diagnostics for tests (any may be NULL):
@@ -164,6 +173,27 @@ spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, 
 spec_status spec_sample(const void *logits, const float *uniforms, const float *temperature, int32_t *out_tokens,
                         int B, int V, spec_dtype dtype, uint32_t *status, void *stream,
                         const spec_verify_options *options);
+
+/* Prompt-lookup (n-gram) proposer: drafts without a model.  "Speculative
+ * Decoding" (atonlee.tistory.com/330) ch.5: find the current suffix earlier in
+ * the context and propose the tokens that followed it; the vLLM section of
+ * "Speculative Decoding으로 LLM 추론 속도 높이기" sets the n-gram lengths with
+ * prompt_lookup_min / prompt_lookup_max.  For each sequence b, with
+ * L = context_len[b] tokens in context[b * context_stride, +L): the longest
+ * n in [min_n, max_n] whose last-n-token suffix also occurs at an earlier start
+ * j < L - n wins, and among its occurrences the most recent one; the proposal
+ * is the min(gamma_max, L - (j + n)) tokens after it.  No occurrence: no
+ * drafts.
+ *   context        int32, row b starts at b * context_stride (device)
+ *   context_len    [B] int32, clamped to [0, context_stride]
+ *   draft_tokens   [B, gamma_max] int32 (written; -1 after the proposal)
+ *   num_draft      [B] int32 (written)
+ * Limits: 1 <= min_n <= max_n <= 64, 0 <= gamma_max <= SPEC_MAX_GAMMA.  One
+ * kernel on 'stream'; allocates nothing.  The proposals feed spec_verify with
+ * draft_logits == NULL (point-mass proposals). */
+spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, const int32_t *context_len, int B,
+                               int min_n, int max_n, int gamma_max, int32_t *draft_tokens, int32_t *num_draft,
+                               void *stream);
 
 /* Launch shape spec_verify would use on the current device for these sizes:
  * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any

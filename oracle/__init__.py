@@ -12,6 +12,8 @@ Contents
   - analytic.py           expected tokens per round and speedup formulas.
   - enumerate_law.py      exact outcome law of one round on tiny vocabularies
                           by brute-force enumeration of every random choice.
+  - ngram.py              the prompt-lookup (n-gram) proposer, plain loops.
+  - gamma_policy.py       the draft-length controller's rule, plain loops.
 
 Parity status: every function here is pinned by -m "not gpu" tests against
 values the pages print, the distribution-preservation theorem, and brute force.
@@ -91,27 +93,30 @@ def verify(target, draft, dtype, tokens, num_draft, uniforms, temperature, diagn
     """Run the oracle on host arrays.
 
     target [B, gmax+1, V] / draft [B, gmax, V]: float32 arrays (dtype 'f32') or
-    uint16 bfloat16 bit patterns (dtype 'bf16'); tokens int32 [B, gmax];
+    uint16 bfloat16 bit patterns (dtype 'bf16'); draft None = point-mass
+    proposals (q_i is 1 at x_i); tokens int32 [B, gmax];
     num_draft int32 [B]; uniforms float32 [B, gmax+1]; temperature float32 [B].
     """
     lib = _load()
     code = {"f32": F32, "bf16": BF16}[dtype]
     elem = np.float32 if code == F32 else np.uint16
     target = np.ascontiguousarray(target, dtype=elem)
-    draft = np.ascontiguousarray(draft, dtype=elem)
+    point = draft is None  # deterministic proposals: q_i is the point mass at x_i
+    if not point:
+        draft = np.ascontiguousarray(draft, dtype=elem)
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     num_draft = np.ascontiguousarray(num_draft, dtype=np.int32)
     uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
     temperature = np.ascontiguousarray(temperature, dtype=np.float32)
     B, gmax = tokens.shape
     V = target.shape[2]
-    assert target.shape == (B, gmax + 1, V) and draft.shape == (B, gmax, V)
+    assert target.shape == (B, gmax + 1, V) and (point or draft.shape == (B, gmax, V))
     assert uniforms.shape == (B, gmax + 1) and num_draft.shape == (B,) and temperature.shape == (B,)
     res = OracleResult(B, gmax)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     d = diagnostics
-    rc = lib.oracle_verify(_ptr(target), _ptr(draft), code, _ptr(tokens), _ptr(num_draft), _ptr(uniforms),
+    rc = lib.oracle_verify(_ptr(target), None if point else _ptr(draft), code, _ptr(tokens), _ptr(num_draft), _ptr(uniforms),
                            _ptr(temperature), B, gmax, V, _ptr(res.out_tokens), _ptr(res.out_num_accepted),
                            _ptr(res.p_hat) if d else None, _ptr(res.q_hat) if d else None,
                            _ptr(res.logz_t) if d else None, _ptr(res.logz_d) if d else None,
@@ -122,7 +127,8 @@ def verify(target, draft, dtype, tokens, num_draft, uniforms, temperature, diagn
     return res
 
 
-def verify_batch(batch, diagnostics=True, nthreads=None) -> OracleResult:
-    """Oracle on a workloads.Batch-like object (attributes as in verify())."""
-    return verify(batch.target, batch.draft, batch.dtype, batch.tokens, batch.num_draft, batch.uniforms,
-                  batch.temperature, diagnostics=diagnostics, nthreads=nthreads)
+def verify_batch(batch, diagnostics=True, nthreads=None, point=False) -> OracleResult:
+    """Oracle on a workloads.Batch-like object (attributes as in verify()).
+    point=True: deterministic proposals (q_i is the point mass at x_i; no draft rows)."""
+    return verify(batch.target, None if point else batch.draft, batch.dtype, batch.tokens, batch.num_draft,
+                  batch.uniforms, batch.temperature, diagnostics=diagnostics, nthreads=nthreads)

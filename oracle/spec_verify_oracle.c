@@ -36,6 +36,11 @@
  *     S their total; if rounding leaves no such j, the last j with weight > 0.
  *   - A rejected row whose residual mass is not above 1e-300 (unreachable in
  *     exact arithmetic) samples from p of that row instead.
+ *   - A NULL draft-logit array means deterministic proposals: q_i is the
+ *     point mass at the drafted id x_i (a prompt-lookup / n-gram proposer,
+ *     [P1] ch.5 and [P4]'s table of draft methods, copies tokens from the
+ *     context).  Then the test is r < p(x_i) and the residual is p with x_i
+ *     removed: max(0, p - q) for that q.
  *   - A sequence with num_draft outside [0, gmax], a temperature that is
  *     negative, NaN, infinite or positive-but-below FLT_MIN, a drafted id
  *     outside [0, V) at a position it uses, or a sampled row it uses whose
@@ -173,13 +178,18 @@ static void fill_diagnostics(const oracle_args *a, int b, int g, double T)
             a->logz_t[(size_t)b * (gmax + 1) + i] = st.m + log(st.z);
         if (i == g)
             break;
+        int x = a->tokens[(size_t)b * gmax + i];
+        if (a->p_hat)
+            a->p_hat[(size_t)b * gmax + i] = row_prob(a->target, a->dtype, toff, x, T, st);
+        if (!a->draft) { /* point-mass draft: q(x) = 1, no draft row */
+            if (a->q_hat)
+                a->q_hat[(size_t)b * gmax + i] = 1.0;
+            continue;
+        }
         size_t doff = ((size_t)b * gmax + i) * (size_t)V;
         softmax_norm sd = row_softmax_norm(a->draft, a->dtype, doff, V, T);
         if (a->logz_d)
             a->logz_d[(size_t)b * gmax + i] = sd.m + log(sd.z);
-        int x = a->tokens[(size_t)b * gmax + i];
-        if (a->p_hat)
-            a->p_hat[(size_t)b * gmax + i] = row_prob(a->target, a->dtype, toff, x, T, st);
         if (a->q_hat)
             a->q_hat[(size_t)b * gmax + i] = row_prob(a->draft, a->dtype, doff, x, T, sd);
     }
@@ -190,7 +200,7 @@ static void fill_diagnostics(const oracle_args *a, int b, int g, double T)
  * max(0, p - q) of row n, otherwise the target distribution of row n (the
  * bonus row when every draft was accepted). */
 static int sample_decided_row(const oracle_args *a, int b, int n, int rejected, double T, double u,
-                              softmax_norm st, softmax_norm sd, double *mass_out, double *margin_out)
+                              softmax_norm st, softmax_norm sd, int xn, double *mass_out, double *margin_out)
 {
     const int gmax = a->gmax, V = a->V;
     size_t toff = ((size_t)b * (gmax + 1) + n) * (size_t)V;
@@ -203,7 +213,7 @@ static int sample_decided_row(const oracle_args *a, int b, int n, int rejected, 
         double pj = row_prob(a->target, a->dtype, toff, j, T, st);
         double wj = pj;
         if (rejected) {
-            double qj = row_prob(a->draft, a->dtype, doff, j, T, sd);
+            double qj = a->draft ? row_prob(a->draft, a->dtype, doff, j, T, sd) : (j == xn ? 1.0 : 0.0);
             wj = pj - qj > 0.0 ? pj - qj : 0.0;
         }
         w[j] = wj;
@@ -327,13 +337,15 @@ static void verify_one(const oracle_args *a, int b)
         size_t toff = ((size_t)b * (gmax + 1) + i) * (size_t)V;
         size_t doff = ((size_t)b * gmax + i) * (size_t)V;
         softmax_norm st = row_softmax_norm(a->target, a->dtype, toff, V, T);
-        softmax_norm sd = row_softmax_norm(a->draft, a->dtype, doff, V, T);
+        softmax_norm sd = {0.0, 1.0};
+        if (a->draft)
+            sd = row_softmax_norm(a->draft, a->dtype, doff, V, T);
         if (!norm_is_valid(st) || !norm_is_valid(sd)) {
             write_invalid(a, b, ORACLE_BAD_LOGITS);
             return;
         }
         double p = row_prob(a->target, a->dtype, toff, x[i], T, st);
-        double q = row_prob(a->draft, a->dtype, doff, x[i], T, sd);
+        double q = a->draft ? row_prob(a->draft, a->dtype, doff, x[i], T, sd) : 1.0;
         double ri = (double)r[i];
         if (a->acc_margin)
             a->acc_margin[(size_t)b * gmax + i] = q > 0.0 ? fabs(ri - p / q) : INFINITY;
@@ -354,7 +366,8 @@ static void verify_one(const oracle_args *a, int b)
         }
     }
     double mass = NAN, margin = NAN;
-    int y = sample_decided_row(a, b, n, rejected, T, (double)r[gmax], st_dec, sd_dec, &mass, &margin);
+    int y = sample_decided_row(a, b, n, rejected, T, (double)r[gmax], st_dec, sd_dec, rejected ? x[n] : -1,
+                               &mass, &margin);
     if (a->resid_mass)
         a->resid_mass[b] = mass;
     if (a->samp_margin)
@@ -393,9 +406,8 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
         return -1;
     if (B == 0)
         return 0;
-    if (!target || !draft || !tokens || !num_draft || !uniforms || !temperature || !out_tokens ||
-        !out_num_accepted)
-        return -1;
+    if (!target || !tokens || !num_draft || !uniforms || !temperature || !out_tokens || !out_num_accepted)
+        return -1; /* draft may be NULL: point-mass proposals */
     oracle_args a = {target, draft, dtype, tokens, num_draft, uniforms, temperature, B, gmax, V,
                      out_tokens, out_num_accepted, p_hat, q_hat, logz_t, logz_d, resid_mass,
                      acc_margin, samp_margin, seq_status};

@@ -79,7 +79,8 @@ def _prepare(target, draft, tokens, num_draft, uniforms, temperature, out_tokens
     gmax = g1 - 1
     code = _dtype_code(target)
     _check(target, "target_logits", target.dtype, (B, gmax + 1, V), dev)
-    _check(draft, "draft_logits", target.dtype, (B, gmax, V), dev)
+    if draft is not None:  # None: point-mass proposals (q_i is 1 at the drafted id)
+        _check(draft, "draft_logits", target.dtype, (B, gmax, V), dev)
     _check(tokens, "draft_tokens", torch.int32, (B, gmax), dev)
     _check(num_draft, "num_draft", torch.int32, (B,), dev)
     _check(uniforms, "uniforms", torch.float32, (B, gmax + 1), dev)
@@ -107,7 +108,8 @@ KERNEL_EARLY = 3     # row-ordered early exit: no row after the first rejection 
 
 
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
-           out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO):
+           out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO,
+           counters=None):
     """One verification round on the GPU (asynchronous on ``stream``).
 
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
@@ -115,6 +117,10 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
     ``cluster_size``: 0 = automatic, else 1/2/4/8/16 CTAs per sequence.
     ``kernel``: KERNEL_AUTO, KERNEL_RING, KERNEL_REGISTER or KERNEL_EARLY.
+    ``draft_logits=None``: point-mass proposals (a deterministic proposer such
+    as ngram_propose): accept iff u < p(x), a rejection samples p without x.
+    ``counters``: optional uint64 (int64) CUDA tensor [3], += drafted ids,
+    accepted ids, verified sequences.
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
@@ -122,8 +128,11 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     args = [_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft), _ptr(uniforms),
             _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code, _ptr(status),
             _stream_handle(stream, target_logits.device)]
-    if cluster_size or kernel:
-        opts = _native.Options(int(cluster_size), int(kernel))
+    if cluster_size or kernel or counters is not None:
+        if counters is not None and (counters.numel() < 3 or counters.element_size() != 8 or not counters.is_cuda):
+            raise ValueError("counters must be a CUDA tensor of three 64-bit integers")
+        opts = _native.Options(int(cluster_size), int(kernel),
+                               None if counters is None else ctypes.c_void_p(counters.data_ptr()))
         rc = lib.spec_verify_ex(*args, ctypes.byref(opts))
     else:
         rc = lib.spec_verify(*args)
@@ -189,6 +198,34 @@ def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=N
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_sample")
     return out_tokens
+
+
+def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, out_tokens=None, out_num=None,
+                  stream=None):
+    """Prompt-lookup drafts (spec_ngram_propose): context int32 [B, S] CUDA tensor
+    (row b holds context_len[b] tokens), returns (draft_tokens [B, gamma_max],
+    num_draft [B]) for spec_verify with draft_logits=None."""
+    import torch
+
+    if not context.is_cuda or context.dim() != 2 or context.dtype != torch.int32:
+        raise ValueError("context must be an int32 [B, S] CUDA tensor")
+    dev = context.device
+    B, S = context.shape
+    if context.stride(1) != 1:
+        raise ValueError("context rows must be contiguous")
+    _check(context_len, "context_len", torch.int32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma_max), dtype=torch.int32, device=dev)
+    if out_num is None:
+        out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(out_tokens, "draft_tokens", torch.int32, (B, gamma_max), dev)
+    _check(out_num, "num_draft", torch.int32, (B,), dev)
+    lib = _native.load()
+    rc = lib.spec_ngram_propose(_ptr(context), int(context.stride(0)), _ptr(context_len), B, int(min_n), int(max_n),
+                                int(gamma_max), _ptr(out_tokens), _ptr(out_num), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_ngram_propose")
+    return out_tokens, out_num
 
 
 def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):

@@ -23,7 +23,7 @@ _lib = None
 class Options(ctypes.Structure):
     """spec_verify_options of include/spec_verify.h."""
 
-    _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int)]
+    _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int), ("counters", ctypes.c_void_p)]
 
 
 def nvcc_path() -> str:
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.spec_verify_debug.restype = i32
         lib.spec_verify_ex.argtypes = common + [vp]
         lib.spec_verify_ex.restype = i32
+        lib.spec_ngram_propose.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_ngram_propose.restype = i32
         lib.spec_sample.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         lib.spec_sample.restype = i32
         lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]

@@ -90,7 +90,7 @@ static_assert(kSegChunks % kThreads == 0, "a segment must split evenly over the 
 
 struct Params {
     const void *target;
-    const void *draft;
+    const void *draft;  // NULL: point-mass proposals (q_i is 1 at the drafted id)
     const int32_t *tokens;
     const int32_t *num_draft;  // NULL for spec_sample: every sequence has g = 0
     const float *uniforms;
@@ -108,6 +108,7 @@ struct Params {
     int num_chunks;  // 16-byte chunks per row; the last is partial on the scalar path
     int scan_tiles;  // register kernel: tiles of kThreads chunk sums kept in shared memory (0 = none)
     int ordered;     // map clusters to sequences longest-first (small B only)
+    unsigned long long *counters;  // optional: += drafted, accepted, verified sequences
 };
 
 // ---------------------------------------------------------------------------
@@ -412,12 +413,13 @@ __device__ __forceinline__ unsigned long long to_fixed60(float w)
 // p, in float32.  tv/dv: the target and draft chunk.
 struct WeightParams {
     float k, negmt, invzt, negmd, invzd;
-    bool residual;
+    bool residual;  // max(0, p - q) with q from the draft row
+    int zero_at;    // point-mass residual: p with this id removed (-1: none)
 };
 
 template <typename T>
 __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, const WeightParams &wp,
-                                              float (&w)[Elem<T>::W])
+                                              float (&w)[Elem<T>::W], int base = 0)
 {
     constexpr int P = Elem<T>::W / 2;
     const float2 k2 = make_float2(wp.k, wp.k);
@@ -433,6 +435,12 @@ __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, 
         }
         w[2 * q] = pq.x;
         w[2 * q + 1] = pq.y;
+    }
+    if (wp.zero_at >= base && wp.zero_at < base + Elem<T>::W) {
+#pragma unroll
+        for (int e = 0; e < Elem<T>::W; ++e)
+            if (base + e == wp.zero_at)
+                w[e] = 0.0f;
     }
 }
 
@@ -595,6 +603,8 @@ struct SharedState {
 struct Seq {
     int b, g, gmax, V, rank, C, c0, c1;
     bool sampled;
+    bool point;   // deterministic proposals: no draft rows, q_i(x_i) = 1
+    bool drafts;  // sampled with draft rows to read
     float k;  // log2(e) / T for sampled sequences
     size_t rowlen;
 };
@@ -708,6 +718,16 @@ __device__ __forceinline__ void exchange_rows(SharedState &sh, const Seq &s, int
 // Accept decisions (warp 0: lane i tests draft position i; a ballot finds the
 // cut) and rank 0's output writes.  Returns true if the sequence goes on to
 // pass 2 (sampled and valid).  All threads call it.
+// Acceptance counters of a verified sequence: drafted ids, accepted ids, and
+// one round (the page on vLLM exports the same two counts; their ratio is the
+// acceptance rate a, and accepted / rounds + 1 the tokens per round).
+__device__ __forceinline__ void count_round(unsigned long long *counters, int g, int n)
+{
+    atomicAdd(&counters[0], (unsigned long long)g);
+    atomicAdd(&counters[1], (unsigned long long)n);
+    atomicAdd(&counters[2], 1ull);
+}
+
 // What warp 0's lane i needs for position i's decision, loaded before pass 1
 // so the loads overlap the sweep: the drafted id and (sampled) the target and
 // draft logits at it.
@@ -723,13 +743,17 @@ template <typename T> __device__ __forceinline__ Gathered gather_position(const 
         return gt;
     gt.x = p.tokens[(size_t)s.b * s.gmax + i];
     if (s.sampled && gt.x >= 0 && gt.x < s.V) {
-        const T *tr = row_ptr<T>(p, s, i), *dr = row_ptr<T>(p, s, s.g + 1 + i);
-        if (sizeof(T) == 2) {
+        const T *tr = row_ptr<T>(p, s, i);
+        if (sizeof(T) == 2)
             gt.lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[gt.x]);
-            gt.ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[gt.x]);
-        } else {
+        else
             gt.lt = reinterpret_cast<const float *>(tr)[gt.x];
-            gt.ld = reinterpret_cast<const float *>(dr)[gt.x];
+        if (s.drafts) {
+            const T *dr = row_ptr<T>(p, s, s.g + 1 + i);
+            if (sizeof(T) == 2)
+                gt.ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[gt.x]);
+            else
+                gt.ld = reinterpret_cast<const float *>(dr)[gt.x];
         }
     }
     return gt;
@@ -751,11 +775,15 @@ __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s,
             } else if (!s.sampled) {
                 ok = x == sh.row[lane].idx;
             } else {
-                const RowStat st = sh.row[lane], sd = sh.row[g + 1 + lane];
-                valid = soft_row_ok(st) && soft_row_ok(sd);
-                const float lt = gt.lt, ld = gt.ld;
-                phat = ex2_approx(fmaf(lt, s.k, -st.m)) / (st.hi + st.lo);
-                qhat = ex2_approx(fmaf(ld, s.k, -sd.m)) / (sd.hi + sd.lo);
+                const RowStat st = sh.row[lane];
+                valid = soft_row_ok(st);
+                phat = ex2_approx(fmaf(gt.lt, s.k, -st.m)) / (st.hi + st.lo);
+                qhat = 1.0f;  // point-mass proposal
+                if (s.drafts) {
+                    const RowStat sd = sh.row[g + 1 + lane];
+                    valid = valid && soft_row_ok(sd);
+                    qhat = ex2_approx(fmaf(gt.ld, s.k, -sd.m)) / (sd.hi + sd.lo);
+                }
                 ok = valid && (p.uniforms[(size_t)b * (gmax + 1) + lane] * qhat < phat);
             }
         }
@@ -794,7 +822,7 @@ __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s,
             const RowStat st = sh.row[tid];
             if (p.logz_t)
                 p.logz_t[(size_t)b * (gmax + 1) + tid] = (st.m + log2f(st.hi + st.lo)) * kLn2;
-            if (tid < g && p.logz_d) {
+            if (tid < g && p.logz_d && s.drafts) {
                 const RowStat sd = sh.row[g + 1 + tid];
                 p.logz_d[(size_t)b * gmax + tid] = (sd.m + log2f(sd.hi + sd.lo)) * kLn2;
             }
@@ -817,22 +845,30 @@ __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s,
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
                 atomicOr(p.status, bits);
+            if (!bits && p.counters)
+                count_round(p.counters, g, n);
         }
     }
     return s.sampled && !bits;
 }
 
-__device__ __forceinline__ WeightParams weight_params(const SharedState &sh, const Seq &s, int n, bool residual)
+// Pass-2 weight parameters of decided row n.  residual: the row of a
+// rejection, whose weights are max(0, p - q); with point-mass proposals that
+// is p with the rejected id xn removed.  Otherwise the weights are p.
+__device__ __forceinline__ WeightParams weight_params(const SharedState &sh, const Seq &s, int n, bool residual,
+                                                     int xn)
 {
     const RowStat st = sh.row[n];
-    const RowStat sd = residual ? sh.row[s.g + 1 + n] : st;
+    const bool rows = residual && s.drafts;
+    const RowStat sd = rows ? sh.row[s.g + 1 + n] : st;
     WeightParams wp;
     wp.k = s.k;
     wp.negmt = -st.m;
     wp.invzt = 1.0f / (st.hi + st.lo);
     wp.negmd = -sd.m;
     wp.invzd = 1.0f / (sd.hi + sd.lo);
-    wp.residual = residual;
+    wp.residual = rows;
+    wp.zero_at = (residual && !s.drafts) ? xn : -1;
     return wp;
 }
 
@@ -1031,6 +1067,8 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
     s.c0 = (int)((long long)p.num_chunks * rank / C);
     s.c1 = (int)((long long)p.num_chunks * (rank + 1) / C);
     s.sampled = temp > 0.0f;
+    s.point = p.draft == nullptr;
+    s.drafts = s.sampled && !s.point;
     s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
     s.rowlen = (size_t)p.V;
     return s;
@@ -1080,7 +1118,7 @@ __device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, con
         const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
         const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
         float w[W];
-        chunk_weights<T>(tv, dv, wp, w);
+        chunk_weights<T>(tv, dv, wp, w, c * W);
         *outn = c * W + pick_in_chunk<T>(w, r);
     };
     if (keep) {
@@ -1140,7 +1178,7 @@ __device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, con
         if (c < s.c1) {
             const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
             const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
-            chunk_weights<T>(tv, dv, wp, w);
+            chunk_weights<T>(tv, dv, wp, w, c * W);
             sigma = chunk_fixed<T>(w);
             if (chunk_sum<T>(w) > 0.0f)
                 last = c;
@@ -1189,8 +1227,9 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
     extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
     const bool residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
-    const T *drow = residual ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    WeightParams wp = weight_params(sh, s, n, residual);
+    const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
+    const int xn = residual ? p.tokens[(size_t)b * s.gmax + n] : -1;
+    WeightParams wp = weight_params(sh, s, n, residual, xn);
     const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
     const bool keep = tiles <= p.scan_tiles;
     constexpr int U2 = kUnroll / 2;
@@ -1211,7 +1250,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
                 float sum = 0.0f;
                 if (c < s.c1) {
                     float w[W];
-                    chunk_weights<T>(tv[u], dv[u], wp, w);
+                    chunk_weights<T>(tv[u], dv[u], wp, w, c * W);
                     sum = chunk_sum<T>(w);
                     acc += to_fixed60(sum);
                 }
@@ -1260,7 +1299,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
         if (S > 0 || !use_residual)
             break;
         use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false);
+        wp = weight_params(sh, s, n, false, -1);
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
         p.resid_mass[b] = (float)S * kFixedUnit;
@@ -1274,7 +1313,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
 // Kernel 1: register loads (any alignment; the default)
 // ===========================================================================
 template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Params p)
+__global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const Params p)
 {
     __shared__ SharedState sh;
     cg::cluster_group cluster = cg::this_cluster();
@@ -1296,12 +1335,12 @@ __global__ void __launch_bounds__(kThreads) spec_verify_stream_kernel(const Para
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
 
     const Seq s = make_seq(p, C, rank, b, g, temp);
-    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
+    const int nrows = s.drafts ? 2 * g + 1 : g + 1;
     const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
 
     // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
     for (int step = 0; step < nrows; ++step) {
-        const int r = row_at_step(step, g, s.sampled);
+        const int r = row_at_step(step, g, s.drafts);
         const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, r));
         if (lane == 0)
             sh.warp_part[r][wid] = st;
@@ -1363,23 +1402,9 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     int n = g;
     uint32_t bits = 0;
     for (int i = 0; i <= g; ++i) {
-        const int nslot = (s.sampled && i < g) ? 2 : 1;
-        // the decision's two logits at x_i, loaded ahead of the rows
-        float lt = 0.0f, ld = 0.0f;
-        int x = -1;
-        if (tid == 0 && i < g) {
-            x = p.tokens[(size_t)b * gmax + i];
-            if (s.sampled && x >= 0 && x < s.V) {
-                const T *tr = row_ptr<T>(p, s, i), *dr = row_ptr<T>(p, s, g + 1 + i);
-                if (sizeof(T) == 2) {
-                    lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[x]);
-                    ld = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dr)[x]);
-                } else {
-                    lt = reinterpret_cast<const float *>(tr)[x];
-                    ld = reinterpret_cast<const float *>(dr)[x];
-                }
-            }
-        }
+        const int nslot = (s.drafts && i < g) ? 2 : 1;
+        // the decision's logits at x_i, loaded ahead of the rows
+        const Gathered gt = tid == 0 ? gather_position<T>(p, s, i) : Gathered{-1, 0.0f, 0.0f};
         for (int slot = 0; slot < nslot; ++slot) {
             const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, slot ? g + 1 + i : i));
             if (lane == 0)
@@ -1413,15 +1438,16 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 if (s.sampled && !soft_row_ok(sh.row[g]))
                     bb = SPEC_STATUS_BAD_LOGITS;
             } else if (!s.sampled) {
-                stop = x != sh.row[i].idx;
+                stop = gt.x != sh.row[i].idx;
             } else {
-                const RowStat st = sh.row[i], sd = sh.row[g + 1 + i];
+                const RowStat st = sh.row[i];
+                const RowStat sd = s.drafts ? sh.row[g + 1 + i] : st;
                 if (!(soft_row_ok(st) && soft_row_ok(sd))) {
                     stop = 1;
                     bb = SPEC_STATUS_BAD_LOGITS;
                 } else {
-                    const float phat = ex2_approx(fmaf(lt, s.k, -st.m)) / (st.hi + st.lo);
-                    const float qhat = ex2_approx(fmaf(ld, s.k, -sd.m)) / (sd.hi + sd.lo);
+                    const float phat = ex2_approx(fmaf(gt.lt, s.k, -st.m)) / (st.hi + st.lo);
+                    const float qhat = s.drafts ? ex2_approx(fmaf(gt.ld, s.k, -sd.m)) / (sd.hi + sd.lo) : 1.0f;
                     stop = !(p.uniforms[(size_t)b * (gmax + 1) + i] * qhat < phat);
                     if (rank == 0) {
                         if (p.p_hat)
@@ -1449,7 +1475,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
             const RowStat st = sh.row[tid];
             if (p.logz_t)
                 p.logz_t[(size_t)b * (gmax + 1) + tid] = (st.m + log2f(st.hi + st.lo)) * kLn2;
-            if (tid < g && p.logz_d) {
+            if (tid < g && p.logz_d && s.drafts) {
                 const RowStat sd = sh.row[g + 1 + tid];
                 p.logz_d[(size_t)b * gmax + tid] = (sd.m + log2f(sd.hi + sd.lo)) * kLn2;
             }
@@ -1472,6 +1498,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
                 atomicOr(p.status, bits);
+            if (!bits && p.counters)
+                count_round(p.counters, g, n);
         }
     }
     if (!s.sampled || bits)
@@ -1623,7 +1651,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     bool use_residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
     const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    WeightParams wp = weight_params(sh, s, n, use_residual);
+    WeightParams wp = weight_params(sh, s, n, use_residual, -1);
     unsigned long long S = 0, P = 0, mine = 0;
     bool timed_out = false;
     for (int attempt = 0; attempt < 2; ++attempt) {
@@ -1664,7 +1692,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
         if (timed_out || S > 0 || !use_residual)
             break;
         use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false);
+        wp = weight_params(sh, s, n, false, -1);
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
         p.resid_mass[b] = (float)S * kFixedUnit;
@@ -1743,6 +1771,69 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
         p.out_tokens[(size_t)b * (s.gmax + 1) + n] = -1;
         if (p.status)
             atomicOr(p.status, SPEC_STATUS_TIMEOUT);
+    }
+}
+
+// ===========================================================================
+// Prompt-lookup (n-gram) proposer
+// ===========================================================================
+// Drafts without a model ("Speculative Decoding", ch.5: find the current suffix
+// earlier in the context and propose what followed it; prompt_lookup_min/max
+// in the vLLM section of "Speculative Decoding으로 LLM 추론 속도 높이기").  For
+// every candidate end e in [1, L-1] the kernel measures l(e), the length of the
+// longest common suffix of context[0, e) and context[0, L), capped at max_n;
+// the proposal follows the end with the largest l(e) >= min_n, the latest such
+// end on ties.  That is the same as trying n from max_n down to min_n and
+// taking the most recent occurrence of the n-gram (an occurrence of length n
+// ends at e exactly when l(e) >= n).  One CTA per sequence.
+constexpr int kMaxNgram = 64;
+constexpr int kNgramThreads = 256;
+
+__global__ void __launch_bounds__(kNgramThreads)
+    spec_ngram_kernel(const int32_t *context, long long stride, const int32_t *context_len, int min_n, int max_n,
+                      int gmax, int32_t *out_tokens, int32_t *out_num)
+{
+    __shared__ int suffix[kMaxNgram];  // suffix[t] = context[L - 1 - t]
+    __shared__ unsigned long long best_warp[kNgramThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int32_t *ctx = context + (size_t)b * (size_t)stride;
+    int L = context_len[b];
+    L = L < 0 ? 0 : (L > stride ? (int)stride : L);
+    if (tid < max_n && tid < L)
+        suffix[tid] = ctx[L - 1 - tid];
+    __syncthreads();
+    // (l << 32) | e, larger is better; 0 = no candidate
+    unsigned long long best = 0;
+    for (int e = L - 1 - tid; e >= 1; e -= kNgramThreads) {
+        int l = 0;
+        while (l < max_n && l < e && ctx[e - 1 - l] == suffix[l])
+            ++l;
+        if (l >= min_n) {
+            const unsigned long long key = ((unsigned long long)l << 32) | (unsigned)e;
+            best = key > best ? key : best;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+        best = y > best ? y : best;
+    }
+    if (lane == 0)
+        best_warp[wid] = best;
+    __syncthreads();
+    if (wid == 0) {
+        unsigned long long v = lane < kNgramThreads / 32 ? best_warp[lane] : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, v, o);
+            v = y > v ? y : v;
+        }
+        const int e = (int)(v & 0xffffffffu);
+        const int k = v ? min(gmax, L - e) : 0;
+        if (lane < gmax)
+            out_tokens[(size_t)b * gmax + lane] = lane < k ? ctx[e + lane] : -1;
+        if (lane == 0)
+            out_num[b] = k;
     }
 }
 
@@ -1900,7 +1991,9 @@ struct Shape {
 };
 
 // Picks the kernel and cluster size.  want_kind: -1 automatic, else a KernelKind.
-spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_kind, int want_C, Shape *out)
+// point: point-mass proposals, which the ring kernel does not handle.
+spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_kind, int want_C, Shape *out,
+                          bool point = false)
 {
     int dev = 0, sms = 0;
     spec_status st = current_device(&dev);
@@ -1914,12 +2007,15 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     if (want_kind >= 0) {
         if (!aligned && (want_kind == kKindRing || want_kind == kKindScalarAligned || want_kind == kKindEarlyAligned))
             return SPEC_ERR_UNSUPPORTED;
+        if (point && want_kind == kKindRing)
+            return SPEC_ERR_UNSUPPORTED;
         kinds[nk++] = want_kind;
     } else if (aligned) {
         // Register loads: on GB300 its 32 resident reducing warps per SM beat the
         // ring kernel's 16 (the reduction is issue-bound, not load-bound).
         kinds[nk++] = kKindScalarAligned;
-        kinds[nk++] = kKindRing;
+        if (!point)
+            kinds[nk++] = kKindRing;
     } else {
         kinds[nk++] = kKindScalar;
     }
@@ -1971,31 +2067,33 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         return SPEC_ERR_INVALID_ARG;
     if ((!num_draft || !out_num) && gmax != 0)
         return SPEC_ERR_INVALID_ARG;  // only the sampler (gamma_max 0) runs without them
-    if (gmax > 0 && (!draft || !tokens))
-        return SPEC_ERR_INVALID_ARG;
+    if (gmax > 0 && !tokens)
+        return SPEC_ERR_INVALID_ARG;  // draft may be NULL: point-mass proposals
     const uintptr_t es = (uintptr_t)elem_size(dtype);
     if (((uintptr_t)target % es) || (draft && ((uintptr_t)draft % es)))
         return SPEC_ERR_INVALID_ARG;
     const void *four[] = {tokens, num_draft, uniforms, temperature, out_tokens, out_num, status,
                           p_hat,  q_hat,     logz_t,   logz_d,      resid_mass, seq_status};
+    if (opt && ((uintptr_t)opt->counters & 7u))
+        return SPEC_ERR_INVALID_ARG;
     for (const void *q : four)
         if ((uintptr_t)q & 3u)
             return SPEC_ERR_INVALID_ARG;
-    const bool aligned = aligned16(target) && (gmax == 0 || aligned16(draft)) &&
-                         ((size_t)V * (size_t)es) % 16 == 0;
+    const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
+    const bool point = gmax > 0 && !draft;
     if (!aligned && want_kind == kKindScalarAligned)
         want_kind = kKindScalar;  // register loads work at any alignment
     if (!aligned && want_kind == kKindEarlyAligned)
         want_kind = kKindEarly;
 
     Shape shp;
-    spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp);
+    spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp, point);
     if (st != SPEC_OK)
         return st;
 
     Params prm;
     prm.target = target;
-    prm.draft = draft ? draft : target;
+    prm.draft = draft;
     prm.tokens = tokens;
     prm.num_draft = num_draft;
     prm.uniforms = uniforms;
@@ -2017,6 +2115,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     const int tiles = (slice + kThreads - 1) / kThreads;
     prm.scan_tiles = (shp.kind != kKindRing && tiles <= kMaxScanTiles) ? tiles : 0;
     prm.ordered = B <= kMaxOrdered ? 1 : 0;
+    prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
 
     cudaLaunchAttribute attr[1];
@@ -2080,6 +2179,28 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
         return SPEC_ERR_UNSUPPORTED;  // the ring kernel is a full-sweep A/B variant only
     return run(logits, nullptr, nullptr, nullptr, uniforms, temperature, out_tokens, nullptr, B, 0, V, dtype, status,
                stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, options);
+}
+
+spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, const int32_t *context_len, int B,
+                               int min_n, int max_n, int gamma_max, int32_t *draft_tokens, int32_t *num_draft,
+                               void *stream)
+{
+    if (B < 0 || B > SPEC_MAX_BATCH || gamma_max < 0 || gamma_max > SPEC_MAX_GAMMA || min_n < 1 ||
+        max_n < min_n || max_n > kMaxNgram || context_stride < 1 || context_stride > (int64_t)INT_MAX)
+        return SPEC_ERR_INVALID_ARG;
+    if (B == 0)
+        return SPEC_OK;
+    if (!context || !context_len || !num_draft || (gamma_max > 0 && !draft_tokens))
+        return SPEC_ERR_INVALID_ARG;
+    const void *four[] = {context, context_len, draft_tokens, num_draft};
+    for (const void *q : four)
+        if ((uintptr_t)q & 3u)
+            return SPEC_ERR_INVALID_ARG;
+    spec_ngram_kernel<<<B, kNgramThreads, 0, (cudaStream_t)stream>>>(context, (long long)context_stride,
+                                                                     context_len, min_n, max_n, gamma_max,
+                                                                     draft_tokens, num_draft);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,

@@ -368,3 +368,34 @@ def edge_batch(kind: str, V: int = 1023, gamma: int = 3, B: int = 8, seed: int =
 def describe(batch: Batch) -> str:
     return (f"{batch.name}: B={batch.B} gmax={batch.gmax} V={batch.V} dtype={batch.dtype} "
             f"logit bytes={batch.algorithmic_bytes()} (nominal {batch.nominal_bytes()})")
+
+
+# ----------------------------------------------------------------------------
+# Token contexts for the prompt-lookup proposer
+# ----------------------------------------------------------------------------
+
+def ngram_contexts(B: int, L: int, vocab: int, seed: int, copy_prob: float = 0.5, ragged: bool = True):
+    """Token histories where earlier spans reappear, as in summarising or editing
+    text whose output repeats the input ("Speculative Decoding", ch.5).
+
+    Each context is built from segments of 4..32 tokens: with probability
+    copy_prob a copy of an earlier span of the same context, otherwise fresh
+    uniform ids in [0, vocab).  Returns (contexts int32 [B, L] padded with -1,
+    lengths int32 [B]); lengths are uniform in [L/2, L] when ragged.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = np.full((B, L), -1, np.int32)
+    lens = (rng.integers(L // 2, L + 1, size=B) if ragged else np.full(B, L)).astype(np.int32)
+    for b in range(B):
+        n = int(lens[b])
+        row = []
+        while len(row) < n:
+            seg = int(rng.integers(4, 33))
+            if row and rng.random() < copy_prob:
+                start = int(rng.integers(0, len(row)))
+                piece = row[start:start + seg]
+            else:
+                piece = list(rng.integers(0, vocab, size=seg))
+            row.extend(int(t) for t in piece)
+        ctx[b, :n] = row[:n]
+    return ctx, lens

@@ -25,8 +25,8 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_sample", "spec_verify_launch_shape",
-              "spec_status_string"):
+    for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_sample", "spec_ngram_propose",
+              "spec_verify_launch_shape", "spec_status_string"):
         assert n in names
 
 
@@ -42,7 +42,9 @@ def test_status_strings(lib):
 
 
 def _call(lib, **over):
-    fake = 0x10000  # never dereferenced: every case below fails validation first
+    # Never dereferenced: every case below fails validation (or is B = 0) before
+    # anything is launched; a case that passes validation must not be added here.
+    fake = 0x10000
     args = dict(target=fake, draft=fake, tokens=fake, num_draft=fake, uniforms=fake, temperature=fake,
                 out_tokens=fake, out_num=fake, B=4, gmax=4, V=1024, dtype=1, status=None, stream=None)
     args.update(over)
@@ -55,7 +57,7 @@ def _call(lib, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(target=0), 1), (dict(num_draft=0), 1), (dict(uniforms=0), 1), (dict(temperature=0), 1),
-    (dict(out_tokens=0), 1), (dict(out_num=0), 1), (dict(draft=0), 1), (dict(tokens=0), 1),
+    (dict(out_tokens=0), 1), (dict(out_num=0), 1), (dict(tokens=0), 1),
     (dict(B=-1), 1), (dict(gmax=17), 1), (dict(gmax=-1), 1), (dict(V=0), 1), (dict(V=(1 << 24) + 1), 1),
     (dict(dtype=7), 2), (dict(target=0x10001), 1), (dict(tokens=0x10002), 1), (dict(status=0x10003), 1),
     (dict(B=0), 0),
@@ -92,4 +94,19 @@ def test_sampler_argument_checks(lib, which, code):
     rc = lib.spec_sample(vp(a["logits"]) if a["logits"] else None, vp(a["uniforms"]) if a["uniforms"] else None,
                          vp(a["temperature"]) if a["temperature"] else None, vp(a["out"]) if a["out"] else None,
                          a["B"], a["V"], a["dtype"], None, None, ctypes.byref(opts))
+    assert rc == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(context=0), 1), (dict(lens=0), 1), (dict(num=0), 1), (dict(toks=0), 1), (dict(min_n=0), 1),
+    (dict(max_n=65), 1), (dict(min_n=3, max_n=2), 1), (dict(gmax=17), 1), (dict(stride=0), 1), (dict(B=-1), 1),
+    (dict(context=0x10002), 1), (dict(B=0), 0),
+])
+def test_ngram_argument_checks(lib, over, code):
+    a = dict(context=0x10000, stride=64, lens=0x10000, B=4, min_n=1, max_n=4, gmax=4, toks=0x10000, num=0x10000)
+    a.update(over)
+    vp = ctypes.c_void_p
+    rc = lib.spec_ngram_propose(vp(a["context"]) if a["context"] else None, a["stride"],
+                                vp(a["lens"]) if a["lens"] else None, a["B"], a["min_n"], a["max_n"], a["gmax"],
+                                vp(a["toks"]) if a["toks"] else None, vp(a["num"]) if a["num"] else None, None)
     assert rc == code

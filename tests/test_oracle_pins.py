@@ -431,3 +431,39 @@ def test_bonus_row_normaliser(oracle_mod):
     assert res.out_num_accepted[0] == 1
     assert res.resid_mass[0] == pytest.approx(1.0, rel=1e-12)
     assert res.out_tokens[0, 1] == 2                          # C = (.1, .3, .6, 1): u = 0.5 -> id 2
+
+
+# ----------------------------------------------------------------------------
+# point-mass proposals (prompt lookup): q_i is 1 at the drafted id
+# ----------------------------------------------------------------------------
+
+def test_point_mass_accept_and_residual(oracle_mod):
+    """p = (0.1, 0.6, 0.3), draft id 1: accepted iff r < 0.6; the residual is p
+    without id 1, i.e. (0.25, 0, 0.75)."""
+    N = 2000
+    r, u = np.meshgrid(_grid(N // 40), _grid(40), indexing="ij")
+    p = [[0.1, 0.6, 0.3], [1 / 3, 1 / 3, 1 / 3]]
+    b = _batch(p, [[0.2, 0.2, 0.6]], np.full(r.size, 1), r.ravel(), u.ravel())
+    res = oracle_mod.verify(b["target"], None, "f32", b["tokens"], b["num_draft"], b["uniforms"],
+                            b["temperature"])
+    acc = res.out_num_accepted == 1
+    np.testing.assert_array_equal(acc, r.ravel() < 0.6 - 1e-6)
+    rej = ~acc
+    y = res.out_tokens[rej, 0]
+    assert set(np.unique(y)) <= {0, 2}
+    np.testing.assert_array_equal(y == 0, u.ravel()[rej] < 0.25)
+    np.testing.assert_allclose(res.q_hat[:, 0], 1.0)
+    assert np.all(np.isnan(res.logz_d))
+
+
+def test_point_mass_output_law_is_p(oracle_mod):
+    """Theorem with a deterministic proposal: the emitted token still follows p."""
+    p0 = np.array([0.15, 0.45, 0.1, 0.3])
+    N = 400
+    rr, uu = np.meshgrid(_grid(N), _grid(N), indexing="ij")
+    for x in range(4):
+        b = _batch([p0, [0.25] * 4], [[0.25] * 4], np.full(N * N, x), rr.ravel(), uu.ravel())
+        res = oracle_mod.verify(b["target"], None, "f32", b["tokens"], b["num_draft"], b["uniforms"],
+                                b["temperature"], diagnostics=False)
+        law = np.bincount(res.out_tokens[:, 0], minlength=4) / (N * N)
+        np.testing.assert_allclose(law, p0, atol=3.0 / N)
