@@ -415,11 +415,12 @@ struct WeightParams {
     float k, negmt, invzt, negmd, invzd;
     bool residual;  // max(0, p - q) with q from the draft row
     int zero_at;    // point-mass residual: p with this id removed (-1: none)
+    int zero_chunk; // the chunk holding zero_at (-1: none)
 };
 
 template <typename T>
 __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, const WeightParams &wp,
-                                              float (&w)[Elem<T>::W], int base = 0)
+                                              float (&w)[Elem<T>::W], int chunk = -2)
 {
     constexpr int P = Elem<T>::W / 2;
     const float2 k2 = make_float2(wp.k, wp.k);
@@ -436,10 +437,10 @@ __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, 
         w[2 * q] = pq.x;
         w[2 * q + 1] = pq.y;
     }
-    if (wp.zero_at >= base && wp.zero_at < base + Elem<T>::W) {
+    if (chunk == wp.zero_chunk) {  // point-mass residual: the rejected id has no weight
 #pragma unroll
         for (int e = 0; e < Elem<T>::W; ++e)
-            if (base + e == wp.zero_at)
+            if (chunk * Elem<T>::W + e == wp.zero_at)
                 w[e] = 0.0f;
     }
 }
@@ -760,7 +761,7 @@ template <typename T> __device__ __forceinline__ Gathered gather_position(const 
 }
 
 template <typename T>
-__device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s, const Gathered &gt)
+__device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s, const Gathered &gt)
 {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int b = s.b, g = s.g, gmax = s.gmax;
@@ -856,7 +857,7 @@ __device__ bool decide_and_write(const Params &p, SharedState &sh, const Seq &s,
 // rejection, whose weights are max(0, p - q); with point-mass proposals that
 // is p with the rejected id xn removed.  Otherwise the weights are p.
 __device__ __forceinline__ WeightParams weight_params(const SharedState &sh, const Seq &s, int n, bool residual,
-                                                     int xn)
+                                                     int xn, int chunk_width)
 {
     const RowStat st = sh.row[n];
     const bool rows = residual && s.drafts;
@@ -869,6 +870,7 @@ __device__ __forceinline__ WeightParams weight_params(const SharedState &sh, con
     wp.invzd = 1.0f / (sd.hi + sd.lo);
     wp.residual = rows;
     wp.zero_at = (residual && !s.drafts) ? xn : -1;
+    wp.zero_chunk = wp.zero_at >= 0 ? wp.zero_at / chunk_width : -1;
     return wp;
 }
 
@@ -1055,6 +1057,9 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
     return SeqPick{sh.seq, sh.seq_g, sh.seq_temp};
 }
 
+// POINT: point-mass proposals, a template parameter of the kernels so that the
+// usual path carries none of its branches.
+template <bool POINT>
 __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b, int g, float temp)
 {
     Seq s;
@@ -1067,7 +1072,7 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
     s.c0 = (int)((long long)p.num_chunks * rank / C);
     s.c1 = (int)((long long)p.num_chunks * (rank + 1) / C);
     s.sampled = temp > 0.0f;
-    s.point = p.draft == nullptr;
+    s.point = POINT;
     s.drafts = s.sampled && !s.point;
     s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
     s.rowlen = (size_t)p.V;
@@ -1107,7 +1112,7 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
 // partials), the last id of the slice with weight > 0 is taken.  All threads of
 // the CTA call it.
 template <typename T, bool ALIGNED>
-__device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
+__device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
                              const WeightParams &wp, bool keep, const float *chunk_sums, unsigned long long rel,
                              int32_t *outn)
 {
@@ -1118,7 +1123,7 @@ __device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, con
         const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
         const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
         float w[W];
-        chunk_weights<T>(tv, dv, wp, w, c * W);
+        chunk_weights<T>(tv, dv, wp, w, c);
         *outn = c * W + pick_in_chunk<T>(w, r);
     };
     if (keep) {
@@ -1178,7 +1183,7 @@ __device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, con
         if (c < s.c1) {
             const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
             const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
-            chunk_weights<T>(tv, dv, wp, w, c * W);
+            chunk_weights<T>(tv, dv, wp, w, c);
             sigma = chunk_fixed<T>(w);
             if (chunk_sum<T>(w) > 0.0f)
                 last = c;
@@ -1218,7 +1223,7 @@ __device__ void owner_search(const Params &p, SharedState &sh, const Seq &s, con
 //     every CTA already; only the owner reads its slice again, and nothing
 //     crosses the cluster.
 template <typename T, bool ALIGNED>
-__device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
+__device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
                              int stride)
 {
     constexpr int W = Elem<T>::W;
@@ -1228,8 +1233,8 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
     const bool residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
     const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    const int xn = residual ? p.tokens[(size_t)b * s.gmax + n] : -1;
-    WeightParams wp = weight_params(sh, s, n, residual, xn);
+    const int xn = (residual && !s.drafts) ? p.tokens[(size_t)b * s.gmax + n] : -1;  // point mode only
+    WeightParams wp = weight_params(sh, s, n, residual, xn, W);
     const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
     const bool keep = tiles <= p.scan_tiles;
     constexpr int U2 = kUnroll / 2;
@@ -1250,7 +1255,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
                 float sum = 0.0f;
                 if (c < s.c1) {
                     float w[W];
-                    chunk_weights<T>(tv[u], dv[u], wp, w, c * W);
+                    chunk_weights<T>(tv[u], dv[u], wp, w, c);
                     sum = chunk_sum<T>(w);
                     acc += to_fixed60(sum);
                 }
@@ -1299,7 +1304,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
         if (S > 0 || !use_residual)
             break;
         use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false, -1);
+        wp = weight_params(sh, s, n, false, -1, W);
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
         p.resid_mass[b] = (float)S * kFixedUnit;
@@ -1312,7 +1317,7 @@ __device__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int
 // ===========================================================================
 // Kernel 1: register loads (any alignment; the default)
 // ===========================================================================
-template <typename T, bool ALIGNED>
+template <typename T, bool ALIGNED, bool POINT>
 __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const Params p)
 {
     __shared__ SharedState sh;
@@ -1334,7 +1339,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const P
         sh.timeout = 0;
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
 
-    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
     const int nrows = s.drafts ? 2 * g + 1 : g + 1;
     const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
 
@@ -1361,7 +1366,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const P
 // "Speculative Decoding", ch.2), so a round reads n+1 target rows and
 // min(n+1, g) draft rows instead of g+1 and g.  The outputs are those of the
 // full sweep; diagnostics exist only for the rows read.
-template <typename T, bool ALIGNED>
+template <typename T, bool ALIGNED, bool POINT>
 __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Params p)
 {
     __shared__ SharedState sh;
@@ -1384,7 +1389,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
         sh.stop = 0;
     }
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
-    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
     const int gmax = s.gmax;
     // every drafted id is checked, as in the full sweep (lane-parallel)
     if (wid == 0) {
@@ -1597,7 +1602,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     __syncthreads();
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
 
-    const Seq s = make_seq(p, C, rank, b, g, temp);
+    const Seq s = make_seq<false>(p, C, rank, b, g, temp);
     const int nrows = s.sampled ? 2 * g + 1 : g + 1;
     const int slice = s.c1 - s.c0;
     const int nseg = (slice + kSegChunks - 1) / kSegChunks;  // segments per row slice
@@ -1651,7 +1656,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     bool use_residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
     const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    WeightParams wp = weight_params(sh, s, n, use_residual, -1);
+    WeightParams wp = weight_params(sh, s, n, use_residual, -1, W);
     unsigned long long S = 0, P = 0, mine = 0;
     bool timed_out = false;
     for (int attempt = 0; attempt < 2; ++attempt) {
@@ -1692,7 +1697,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
         if (timed_out || S > 0 || !use_residual)
             break;
         use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false, -1);
+        wp = weight_params(sh, s, n, false, -1, W);
     }
     if (rank == 0 && tid == 0 && p.resid_mass)
         p.resid_mass[b] = (float)S * kFixedUnit;
@@ -1851,32 +1856,38 @@ enum KernelKind {
     kKinds = 5
 };
 
-template <typename T> KernelFn kernel_for_t(int kind)
+template <typename T, bool POINT> KernelFn kernel_for_t(int kind)
 {
     switch (kind) {
     case kKindRing:
         return spec_verify_ring_kernel<T>;
     case kKindScalarAligned:
-        return spec_verify_stream_kernel<T, true>;
+        return spec_verify_stream_kernel<T, true, POINT>;
     case kKindScalar:
-        return spec_verify_stream_kernel<T, false>;
+        return spec_verify_stream_kernel<T, false, POINT>;
     case kKindEarlyAligned:
-        return spec_verify_early_kernel<T, true>;
+        return spec_verify_early_kernel<T, true, POINT>;
     default:
-        return spec_verify_early_kernel<T, false>;
+        return spec_verify_early_kernel<T, false, POINT>;
     }
 }
 
-KernelFn kernel_for(spec_dtype dt, int kind)
+// point: point-mass proposals (the ring kernel has no such variant).
+KernelFn kernel_for(spec_dtype dt, int kind, bool point)
 {
-    return dt == SPEC_BF16 ? kernel_for_t<__nv_bfloat16>(kind) : kernel_for_t<float>(kind);
+    if (dt == SPEC_BF16)
+        return point ? kernel_for_t<__nv_bfloat16, true>(kind) : kernel_for_t<__nv_bfloat16, false>(kind);
+    return point ? kernel_for_t<float, true>(kind) : kernel_for_t<float, false>(kind);
 }
 
 int kernel_threads(int kind) { return kind == kKindRing ? kTmaThreads : kThreads; }
 // Largest dynamic shared memory a kernel kind is launched with: the ring, or
 // the register kernel's chunk sums.
 int kernel_dyn_smem(int kind) { return kind == kKindRing ? kRingBytes : kMaxScanTiles * kThreads * 4; }
-int variant_slot(spec_dtype dt, int kind) { return (dt == SPEC_BF16 ? kKinds : 0) + kind; }
+int variant_slot(spec_dtype dt, int kind, bool point)
+{
+    return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
+}
 int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4; }
 int chunk_width(spec_dtype dt) { return dt == SPEC_BF16 ? 8 : 4; }
 int elem_size(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
@@ -1886,8 +1897,8 @@ constexpr int kMaxDevices = 64;
 // attributes were applied; per variant and cluster size whether the size can be
 // resident (0 unknown, 1 yes, 2 no).
 std::atomic<int> g_sm_count[kMaxDevices];
-std::atomic<int> g_attrs[kMaxDevices][2 * kKinds];
-std::atomic<int> g_cluster_ok[kMaxDevices][2 * kKinds][5];
+std::atomic<int> g_attrs[kMaxDevices][4 * kKinds];
+std::atomic<int> g_cluster_ok[kMaxDevices][4 * kKinds][5];
 
 spec_status current_device(int *dev)
 {
@@ -1916,12 +1927,12 @@ spec_status device_sm_count(int dev, int *out)
 
 // Applies the kernel attributes once per device: dynamic shared memory above
 // the 48 KB default (ring kernel) and clusters of 16 CTAs.
-bool prepare_kernel(int dev, spec_dtype dt, int kind)
+bool prepare_kernel(int dev, spec_dtype dt, int kind, bool point)
 {
-    const int slot = variant_slot(dt, kind);
+    const int slot = variant_slot(dt, kind, point);
     int st = g_attrs[dev][slot].load(std::memory_order_relaxed);
     if (st == 0) {
-        const void *fn = (const void *)kernel_for(dt, kind);
+        const void *fn = (const void *)kernel_for(dt, kind, point);
         bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         if (ok && kernel_dyn_smem(kind) > 0)
             ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kernel_dyn_smem(kind)) ==
@@ -1952,17 +1963,18 @@ cudaLaunchConfig_t launch_config(int kind, unsigned grid, int C, size_t dyn_smem
 }
 
 // Whether clusters of C CTAs of this variant can be resident on the device.
-bool cluster_launchable(int dev, spec_dtype dt, int kind, int C)
+bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
 {
-    const int slot = variant_slot(dt, kind), lc = log2_cluster(C);
+    const int slot = variant_slot(dt, kind, point), lc = log2_cluster(C);
     int state = g_cluster_ok[dev][slot][lc].load(std::memory_order_relaxed);
     if (state == 0) {
         state = 2;
-        if (prepare_kernel(dev, dt, kind)) {
+        if (prepare_kernel(dev, dt, kind, point)) {
             cudaLaunchAttribute attr[1];
             cudaLaunchConfig_t cfg = launch_config(kind, (unsigned)C * 4u, C, (size_t)kernel_dyn_smem(kind), 0, attr);
             int clusters = 0;
-            const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)kernel_for(dt, kind), &cfg);
+            const cudaError_t e =
+                cudaOccupancyMaxActiveClusters(&clusters, (const void *)kernel_for(dt, kind, point), &cfg);
             if (e != cudaSuccess)
                 cudaGetLastError();
             state = (e == cudaSuccess && clusters > 0) ? 1 : 2;
@@ -2024,7 +2036,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     for (int i = 0; i < nk; ++i) {
         int C = want_C > 0 ? want_C : auto_cluster(B, num_chunks, sms);
         for (;;) {
-            if (cluster_launchable(dev, dt, kinds[i], C)) {
+            if (cluster_launchable(dev, dt, kinds[i], C, point)) {
                 out->kind = kinds[i];
                 out->C = C;
                 return SPEC_OK;
@@ -2121,7 +2133,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg =
         launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, shp.kind), prm);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, shp.kind, point), prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
