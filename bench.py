@@ -160,11 +160,11 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def oracle_baseline(batch, target_seconds: float):
+def oracle_baseline(batch, target_seconds: float, threads: int = 0):
     """The float64 oracle on the host cores: whole batches until target_seconds of wall time."""
     import oracle
 
-    cores = os.cpu_count() or 1
+    cores = threads if threads > 0 else (os.cpu_count() or 1)
     oracle.build()
     n_seq, t_total, reps = 0, 0.0, 0
     while t_total < target_seconds or reps == 0:
@@ -488,7 +488,7 @@ def run_ours(args):
         "clocks": clocks,
     }
     if ws == 1 and not args.quick and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_baseline(batch, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_baseline(batch, args.cpu_seconds, args.cpu_threads)
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -510,6 +510,7 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip e2e, clocks and the CPU baseline (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-threads", type=int, default=0, help="oracle baseline threads (0 = all host cores)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.quick:
         log("warning: fewer than 3 warm-up steps")
