@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 METRIC = "spec_verify sequences/s and achieved HBM GB/s vs ~8 TB/s peak (1 GB300)"
 UNIT = "sequences/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_45_gb300", "csrc", "spec_verify.cu")
+KERNEL_DIR = os.path.join(ROOT, "speculative_decoding_verification_45_gb300", "csrc")
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "spec_verify_cfg5_traffic.json")
 
 
@@ -83,8 +83,14 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """sha256 over the kernel sources (csrc/*.cu, *.cuh in name order): the
+    recorded DRAM traffic holds only for the sources it was measured on."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_DIR)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(KERNEL_DIR, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
 
 
 def recorded_traffic(workload_key: str):

@@ -6,12 +6,16 @@ import os
 import shutil
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = [os.path.join(PKG, "csrc", "spec_verify.cu")]
-HEADERS = [os.path.join(INCLUDE, "spec_verify.h")]
+CSRC = os.path.join(PKG, "csrc")
+# The host unit plus one unit per (dtype, proposal form) of kernels: compiled in parallel.
+SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "kernels_bf16.cu", "kernels_bf16_point.cu",
+                                            "kernels_f32.cu", "kernels_f32_point.cu")]
+HEADERS = [os.path.join(INCLUDE, "spec_verify.h"), os.path.join(CSRC, "spec_verify_kernels.cuh")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libspec_verify.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,21 +44,34 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in SOURCES + HEADERS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a into _build/libspec_verify.so (one nvcc call)."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    if not force and not _stale():
-        return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), "-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-           "-I", INCLUDE, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
+def _run(cmd):
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    return res.stdout + res.stderr
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a (one nvcc per unit, in parallel) and link
+    _build/libspec_verify.so."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    if not force and not _stale():
+        return LIB_PATH
+    nvcc, tag = nvcc_path(), f"tmp{os.getpid()}"
+    objs = [os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + f".{tag}.o") for src in SOURCES]
+    cmds = [[nvcc, "-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+             *(["-Xptxas=-v"] if verbose else []), "-c", "-o", obj, src] for src, obj in zip(SOURCES, objs)]
+    tmp = LIB_PATH + f".{tag}"
+    try:
+        with ThreadPoolExecutor(max_workers=len(cmds)) as pool:
+            logs = list(pool.map(_run, cmds))
+        logs.append(_run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]))
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(logs))
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -130,3 +130,33 @@ def test_deterministic_and_stream(sv):
     s.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@gpu
+@pytest.mark.parametrize("dtype,V,Cs", [("bf16", 32000, (4, 8, 16)), ("f32", 4096, (1, 2, 4)), ("f32", 1024, (1, 2))])
+def test_narrow_slice_variants(sv, oracle_mod, dtype, V, Cs):
+    """Slices of at most 4, 2 or 1 chunks per thread and row select the variants
+    that read several rows per round trip.  At every such cluster size the
+    results and diagnostics stay the oracle's, for draft rows and for point-mass
+    proposals, with sampled and greedy sequences and ragged draft counts."""
+    import torch
+
+    batch = workloads.edge_batch("mixed", V=V, gamma=5, B=24, seed=77, dtype=dtype)
+    ref = oracle_mod.verify_batch(batch)
+    ref_point = oracle_mod.verify_batch(batch, point=True)
+    dev = sv.to_device(batch)
+    for C in Cs:
+        d = sv.verify_debug(**dev, cluster_size=C, kernel=2)
+        torch.cuda.synchronize()
+        d = {k: v.cpu().numpy() for k, v in d.items()}
+        rep = parity.compare(batch, d["out_tokens"], d["out_num_accepted"], ref, gpu_status=d["seq_status"])
+        assert rep.mismatches_far == 0, (C, str(rep), rep.far_detail[:3])
+        parity.softmax_close(d["p_hat"], ref.p_hat)
+        parity.softmax_close(d["q_hat"], ref.q_hat)
+        parity.softmax_close(d["logz_t"], ref.logz_t, atol=1e-5)
+        parity.softmax_close(d["logz_d"], ref.logz_d, atol=1e-5)
+        toks, num = sv.verify(dev["target_logits"], None, dev["draft_tokens"], dev["num_draft"], dev["uniforms"],
+                              dev["temperature"], cluster_size=C, kernel=2)
+        torch.cuda.synchronize()
+        rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref_point)
+        assert rep.mismatches_far == 0, (C, "point", str(rep), rep.far_detail[:3])
