@@ -117,7 +117,7 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
 /* Launch options (tuning, A/B measurement and the early-exit variant; the
  * emitted tokens do not depend on them). */
 typedef struct spec_verify_options {
-    int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1, 2, 4, 8 or 16 */
+    int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1 to 16 */
     int kernel;       /* 0 = automatic (full sweep, register loads);
                          1 = full sweep through a bulk-copy ring (16-byte aligned rows only,
                              else SPEC_ERR_UNSUPPORTED);

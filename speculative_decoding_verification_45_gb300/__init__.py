@@ -115,7 +115,7 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
     ``status``: optional int32 CUDA tensor of one element receiving the
     per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
-    ``cluster_size``: 0 = automatic, else 1/2/4/8/16 CTAs per sequence.
+    ``cluster_size``: 0 = automatic, else 1 to 16 CTAs per sequence.
     ``kernel``: KERNEL_AUTO, KERNEL_RING, KERNEL_REGISTER or KERNEL_EARLY.
     ``draft_logits=None``: point-mass proposals (a deterministic proposer such
     as ngram_propose): accept iff u < p(x), a rejection samples p without x.

@@ -139,7 +139,6 @@ int variant_slot(spec_dtype dt, int kind, bool point)
 {
     return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
 }
-int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4; }
 int chunk_width(spec_dtype dt) { return dt == SPEC_BF16 ? 8 : 4; }
 int elem_size(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
 
@@ -149,7 +148,7 @@ constexpr int kMaxDevices = 64;
 // resident (0 unknown, 1 yes, 2 no).
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_attrs[kMaxDevices][4 * kKinds];
-std::atomic<int> g_cluster_ok[kMaxDevices][4 * kKinds][5];
+std::atomic<int> g_cluster_ok[kMaxDevices][4 * kKinds][kMaxCluster];
 
 spec_status current_device(int *dev)
 {
@@ -216,7 +215,7 @@ cudaLaunchConfig_t launch_config(int kind, unsigned grid, int C, size_t dyn_smem
 // Whether clusters of C CTAs of this variant can be resident on the device.
 bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
 {
-    const int slot = variant_slot(dt, kind, point), lc = log2_cluster(C);
+    const int slot = variant_slot(dt, kind, point), lc = C - 1;
     int state = g_cluster_ok[dev][slot][lc].load(std::memory_order_relaxed);
     if (state == 0) {
         state = 2;
@@ -235,10 +234,18 @@ bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
     return state == 1;
 }
 
-// Automatic cluster size: the smallest power of two giving about six CTAs per
-// SM in the grid, at most 8 (clusters of 16 CTAs schedule worse) and at least
-// kThreads chunks per CTA and row.  Measured on GB300: B=256, V=128256 is best
-// at 4; B=32 and B=64 at 8.
+// Automatic cluster size.  First the smallest power of two giving about six
+// CTAs per SM in the grid, at most 8 (16 for one or two sequences) and at least
+// kThreads/2 chunks per CTA and row.  A thread reads its chunks of a row in
+// batches of kUnroll loads, and on GB300 the sweep time follows the number of
+// batches, not the bytes in the last one: when the slice leaves a second batch
+// less than half full (9 to 12 chunks per thread), the smallest cluster that
+// fits every row in one batch is taken instead, up to 16 CTAs, if the grid stays
+// within about one wave of resident CTAs (four per SM).  Measured on GB300:
+// B=256, V=128256 is best at 4; B=32 at 8; B=64, V=151936 at 10 (42 us
+// against 57 us at 8).
+int per_thread_chunks(int num_chunks, int C) { return ((num_chunks + C - 1) / C + kThreads - 1) / kThreads; }
+
 int auto_cluster(int B, int num_chunks, int sms)
 {
     const long long target = 6LL * sms;
@@ -246,13 +253,24 @@ int auto_cluster(int B, int num_chunks, int sms)
     int C = 1;
     while (C < cap && (long long)B * C < target && num_chunks / (C * 2) >= kThreads / 2)
         C *= 2;
+    const int pt = per_thread_chunks(num_chunks, C);
+    if (pt > kUnroll && pt <= kUnroll + kUnroll / 2) {
+        for (int c = C + 1; c <= kMaxCluster; ++c) {
+            if ((long long)B * c * 10 > 44LL * sms)  // more than 1.1 waves of 4 CTAs per SM
+                break;
+            if (per_thread_chunks(num_chunks, c) <= kUnroll)
+                return c;
+        }
+    }
     return C;
 }
 
 struct Shape {
     int kind;
     int C;
+    int sms;  // the device's SM count
 };
+
 
 // Picks the kernel and cluster size.  want_kind: -1 automatic, else a KernelKind.
 // point: point-mass proposals, which the ring kernel does not handle.
@@ -291,6 +309,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
             if (cluster_launchable(dev, dt, kinds[i], C, point)) {
                 out->kind = kinds[i];
                 out->C = C;
+                out->sms = sms;
                 if (kinds[i] == kKindScalarAligned) {  // narrow slices: the multi-row variant
                     const int per_thread = ((num_chunks + C - 1) / C + kThreads - 1) / kThreads;
                     const int small = per_thread <= 1 ? kKindSmall1
@@ -325,7 +344,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     int want_C = 0, want_kind = -1;
     if (opt) {
         want_C = opt->cluster_size;
-        if (want_C != 0 && want_C != 1 && want_C != 2 && want_C != 4 && want_C != 8 && want_C != 16)
+        if (want_C < 0 || want_C > kMaxCluster)
             return SPEC_ERR_INVALID_ARG;
         if (opt->kernel < 0 || opt->kernel > 3)
             return SPEC_ERR_INVALID_ARG;
@@ -387,7 +406,11 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     const int slice = (prm.num_chunks + shp.C - 1) / shp.C;
     const int tiles = (slice + kThreads - 1) / kThreads;
     prm.scan_tiles = (shp.kind != kKindRing && tiles <= kMaxScanTiles) ? tiles : 0;
-    prm.ordered = B <= kMaxOrdered ? 1 : 0;
+    // Longest-first order matters only when clusters wait for a free slot: a
+    // grid that is resident at once (at most 4 CTAs per SM; 2 for the ring
+    // kernel) skips it and its prologue.
+    const long long slots = (long long)shp.sms * (shp.kind == kKindRing ? 2 : 4);
+    prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
 

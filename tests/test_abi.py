@@ -66,7 +66,7 @@ def test_host_argument_checks(lib, over, code):
     assert _call(lib, **over) == code
 
 
-@pytest.mark.parametrize("cluster,kernel", [(3, 0), (32, 0), (-1, 0), (0, 4), (0, -1)])
+@pytest.mark.parametrize("cluster,kernel", [(17, 0), (32, 0), (-1, 0), (0, 4), (0, -1)])
 def test_launch_options_checked(lib, cluster, kernel):
     vp = ctypes.c_void_p
     f = vp(0x10000)
