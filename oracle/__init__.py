@@ -8,10 +8,12 @@ Contents
   - spec_verify_oracle.c  the sequential float64 restatement of the step
                           (softmax at T, in-order accept test cut at the first
                           rejection, residual or bonus sample, greedy rule);
-                          loaded here through ctypes as ``verify``.
+                          loaded here through ctypes as ``verify``; and the
+                          walk of a candidate tree (``tree_verify``).
   - analytic.py           expected tokens per round and speedup formulas.
   - enumerate_law.py      exact outcome law of one round on tiny vocabularies
-                          by brute-force enumeration of every random choice.
+                          by brute-force enumeration of every random choice
+                          (chains and candidate trees).
   - ngram.py              the prompt-lookup (n-gram) proposer, plain loops.
   - gamma_policy.py       the draft-length controller's rule, plain loops.
 
@@ -41,6 +43,7 @@ STATUS_BAD_TOKEN = 1
 STATUS_BAD_TEMPERATURE = 2
 STATUS_BAD_NUM_DRAFT = 4
 STATUS_BAD_LOGITS = 8
+STATUS_BAD_TREE = 32
 
 
 def build(force: bool = False) -> str:
@@ -64,6 +67,9 @@ def _load():
             lib.oracle_verify.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
             lib.oracle_verify.restype = ctypes.c_int
+            lib.oracle_tree_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int]
+            lib.oracle_tree_verify.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -132,3 +138,50 @@ def verify_batch(batch, diagnostics=True, nthreads=None, point=False) -> OracleR
     point=True: deterministic proposals (q_i is the point mass at x_i; no draft rows)."""
     return verify(batch.target, None if point else batch.draft, batch.dtype, batch.tokens, batch.num_draft,
                   batch.uniforms, batch.temperature, diagnostics=diagnostics, nthreads=nthreads)
+
+
+class TreeResult:
+    """Outputs of one tree-oracle call (numpy arrays on the host)."""
+
+    def __init__(self, B, N):
+        self.out_tokens = np.empty((B, N), np.int32)
+        self.out_num_accepted = np.empty(B, np.int32)
+        self.out_path = np.empty((B, N), np.int32)
+        self.acc_margin = np.empty((B, N), np.float64)
+        self.samp_margin = np.empty(B, np.float64)
+        self.seq_status = np.empty(B, np.int32)
+
+
+def tree_verify(target, dtype, parent, tokens, num_nodes, uniforms, temperature, nthreads=None) -> TreeResult:
+    """Tree oracle on host arrays: target [B, N, V] (float32, or uint16 bfloat16
+    bits for 'bf16'); parent, tokens int32 [B, N]; num_nodes int32 [B];
+    uniforms float32 [B, N] (column c tests node c, column 0 the final
+    sample); temperature float32 [B]."""
+    lib = _load()
+    code = {"f32": F32, "bf16": BF16}[dtype]
+    elem = np.float32 if code == F32 else np.uint16
+    target = np.ascontiguousarray(target, dtype=elem)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    num_nodes = np.ascontiguousarray(num_nodes, dtype=np.int32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    B, N, V = target.shape
+    assert parent.shape == (B, N) and tokens.shape == (B, N) and uniforms.shape == (B, N)
+    assert num_nodes.shape == (B,) and temperature.shape == (B,)
+    res = TreeResult(B, N)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = lib.oracle_tree_verify(_ptr(target), code, _ptr(parent), _ptr(tokens), _ptr(num_nodes), _ptr(uniforms),
+                                _ptr(temperature), B, N, V, _ptr(res.out_tokens), _ptr(res.out_num_accepted),
+                                _ptr(res.out_path), _ptr(res.acc_margin), _ptr(res.samp_margin),
+                                _ptr(res.seq_status), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_tree_verify rejected its arguments")
+    return res
+
+
+def tree_verify_batch(tb, nthreads=None) -> TreeResult:
+    """Tree oracle on a workloads.TreeBatch-like object."""
+    return tree_verify(tb.target, tb.dtype, tb.parent, tb.tokens, tb.num_nodes, tb.uniforms, tb.temperature,
+                       nthreads=nthreads)

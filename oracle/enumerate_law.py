@@ -85,3 +85,61 @@ def accepted_count_law(law: dict, gamma: int) -> np.ndarray:
     for key, pr in law.items():
         out[key[0]] += pr
     return out
+
+
+def tree_outcome_law(p_rows, parent, tokens) -> dict:
+    """Exact law of one tree round with deterministic (point-mass) candidates.
+
+    p_rows[k] is the target distribution at node k (node 0 = root); node k >= 1
+    carries tokens[k] under parent[k] < k.  At the current node the children
+    are tried in index order; with R the ids already rejected there, child c
+    passes with probability p(tok_c) / (1 - p(R)) (zero when tok_c is in R) --
+    the single-candidate rule of "Speculative Decoding" (atonlee.tistory.com/
+    330) ch.3 with q the point mass, applied to p without R.  When none passes
+    (or the node is a leaf) one token is drawn from p without R, renormalised.
+    Returns {(path nodes..., emitted token ids...): probability}, the key being
+    (n, node_1..node_n, y_0..y_n) with n accepted nodes.
+    """
+    p = np.asarray(p_rows, dtype=np.float64)
+    N, V = p.shape
+    children = {k: [c for c in range(1, N) if parent[c] == k] for k in range(N)}
+    law: dict = {}
+
+    def add(key, prob):
+        if prob > 0.0:
+            law[key] = law.get(key, 0.0) + prob
+
+    def walk(node, nodes, toks, prob):
+        rejected = []
+        alive = prob
+        for c in children[node]:
+            mass_left = 1.0 - sum(p[node, t] for t in set(rejected))
+            pc = 0.0 if tokens[c] in rejected else p[node, tokens[c]]
+            acc = pc / mass_left if mass_left > 0.0 else 0.0
+            if acc > 0.0:
+                walk(c, nodes + (c,), toks + (int(tokens[c]),), alive * acc)
+            alive *= 1.0 - acc
+            if tokens[c] not in rejected:
+                rejected.append(int(tokens[c]))
+            if alive <= 0.0:
+                return
+        w = p[node].copy()
+        w[list(set(rejected))] = 0.0
+        if w.sum() <= 0.0:
+            w = p[node].copy()
+        w /= w.sum()
+        for y in range(V):
+            add((len(nodes),) + nodes + toks + (y,), alive * w[y])
+
+    walk(0, (), (), 1.0)
+    return law
+
+
+def tree_emitted_law(law: dict) -> dict:
+    """{emitted token tuple: probability} of a tree round's law."""
+    out: dict = {}
+    for key, pr in law.items():
+        n = key[0]
+        toks = key[1 + n:]
+        out[toks] = out.get(toks, 0.0) + pr
+    return out

@@ -443,3 +443,267 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
     free(sl);
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Tree verification (several candidate paths checked in one round).
+ *
+ * Sources: [P1] ch.5 (Medusa heads each propose their top few candidates; the
+ * combinations form a tree that one target forward checks through a tree
+ * attention mask) and its glossary entry on tree attention; [P2]'s EAGLE
+ * paragraph (EAGLE-2 draws the candidates as a tree and checks it in one
+ * forward).  The pages state the acceptance rule for one candidate per
+ * position only ([P1] ch.3).  Readings used here (also listed in the design doc):
+ *   - Node 0 is the root (the last emitted token); node k >= 1 carries the
+ *     candidate token tokens[b][k] and hangs under parent[b][k] < k.  Row k of
+ *     the target logits is the target's next-token distribution after the
+ *     path root..k.
+ *   - Candidates are deterministic (a proposer's top tokens), so each one is
+ *     a point mass, as for prompt lookup.  The children of the current node
+ *     are tried in index order with the page's rule applied to what is left:
+ *     with R the ids of the children already rejected, child c is accepted
+ *     iff  u_c * (1 - p(R)) < p(tok_c)  (u_c = uniforms[b][c]); a child whose
+ *     id is already in R has no mass left and is rejected.  This is the
+ *     single-candidate rule r < p'(x) for the residual p' = p without R,
+ *     renormalised, so each step keeps the target's law, and with one child
+ *     per node it is the chain rule for point-mass drafts exactly.
+ *   - When no child is accepted (or the node is a leaf) the walk stops and
+ *     one token is sampled from p without R (renormalised) by inverse CDF
+ *     with uniforms[b][0] (node 0 is never tested, so its column is free);
+ *     a residual with mass not above 1e-300 samples p instead.
+ *   - T == 0: the accepted child is the first whose id equals the argmax of
+ *     the node's raw logits (lowest id on ties); the walk stops at a node
+ *     with no such child and emits that argmax.
+ *   - Invalid sequences (num_nodes outside [1, N], a parent outside [0, k),
+ *     a candidate id outside [0, V), a bad temperature, or a sampled row on
+ *     the walk with no finite normaliser) emit -1 everywhere and 0 accepted.
+ * Outputs: out_tokens[b] = accepted tokens then the sampled one, -1 after;
+ * out_path[b] = the accepted node indices, -1 after; out_num[b] = accepted.
+ * ---------------------------------------------------------------------- */
+#define ORACLE_BAD_TREE 32
+
+typedef struct {
+    const void *target;
+    int dtype;
+    const int32_t *parent, *tokens, *num_nodes;
+    const float *uniforms, *temperature;
+    int B, N, V;
+    int32_t *out_tokens, *out_num, *out_path;
+    double *acc_margin;  /* [B, N] |u_c - p(tok_c)/(1 - p(R))| at tested nodes, NaN elsewhere */
+    double *samp_margin; /* [B] distance of u_0 to the nearest CDF boundary of the final pick */
+    int32_t *seq_status; /* [B] */
+} tree_args;
+
+static void tree_write_invalid(const tree_args *a, int b, int bits)
+{
+    for (int k = 0; k < a->N; ++k) {
+        a->out_tokens[(size_t)b * a->N + k] = -1;
+        if (a->out_path)
+            a->out_path[(size_t)b * a->N + k] = -1;
+    }
+    a->out_num[b] = 0;
+    if (a->seq_status)
+        a->seq_status[b] = bits;
+}
+
+static void tree_one(const tree_args *a, int b)
+{
+    const int N = a->N, V = a->V;
+    const int32_t *par = a->parent + (size_t)b * N;
+    const int32_t *tok = a->tokens + (size_t)b * N;
+    const float *u = a->uniforms + (size_t)b * N;
+    const int nn = a->num_nodes[b];
+    const float Tf = a->temperature[b];
+    if (a->acc_margin)
+        for (int k = 0; k < N; ++k)
+            a->acc_margin[(size_t)b * N + k] = NAN;
+    if (a->samp_margin)
+        a->samp_margin[b] = NAN;
+    if (a->seq_status)
+        a->seq_status[b] = 0;
+    if (nn < 1 || nn > N) {
+        tree_write_invalid(a, b, ORACLE_BAD_NUM_DRAFT);
+        return;
+    }
+    int bits = 0;
+    if (!temperature_is_valid(Tf))
+        bits |= ORACLE_BAD_TEMPERATURE;
+    for (int k = 1; k < nn; ++k) {
+        if (par[k] < 0 || par[k] >= k)
+            bits |= ORACLE_BAD_TREE;
+        if (tok[k] < 0 || tok[k] >= V)
+            bits |= ORACLE_BAD_TOKEN;
+    }
+    if (bits) {
+        tree_write_invalid(a, b, bits);
+        return;
+    }
+    int32_t *out = a->out_tokens + (size_t)b * N;
+    int32_t *path = a->out_path ? a->out_path + (size_t)b * N : NULL;
+    int *rej = (int *)malloc(sizeof(int) * (size_t)(nn > 1 ? nn : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!rej || !w) {
+        free(rej);
+        free(w);
+        tree_write_invalid(a, b, ORACLE_BAD_NUM_DRAFT);
+        return;
+    }
+    const double T = (double)Tf;
+    int node = 0, n = 0, emit = -1;
+    for (;;) {
+        const size_t off = ((size_t)b * N + node) * (size_t)V;
+        int next = -1;
+        if (Tf == 0.0f) {
+            const int am = row_argmax(a->target, a->dtype, off, V);
+            for (int c = node + 1; c < nn; ++c)
+                if (par[c] == node && tok[c] == am) {
+                    next = c;
+                    break;
+                }
+            if (next < 0)
+                emit = am;
+        } else {
+            const softmax_norm st = row_softmax_norm(a->target, a->dtype, off, V, T);
+            if (!norm_is_valid(st)) {
+                free(rej);
+                free(w);
+                tree_write_invalid(a, b, ORACLE_BAD_LOGITS);
+                return;
+            }
+            double pR = 0.0;
+            int nrej = 0;
+            for (int c = node + 1; c < nn; ++c) {
+                if (par[c] != node)
+                    continue;
+                int dup = 0;
+                for (int r = 0; r < nrej; ++r)
+                    dup |= rej[r] == tok[c];
+                const double pc = dup ? 0.0 : row_prob(a->target, a->dtype, off, tok[c], T, st);
+                const double left = 1.0 - pR;
+                if (a->acc_margin)
+                    a->acc_margin[(size_t)b * N + c] = left > 0.0 ? fabs((double)u[c] - pc / left) : INFINITY;
+                if ((double)u[c] * left < pc) {
+                    next = c;
+                    break;
+                }
+                if (!dup) {
+                    pR += pc;
+                    rej[nrej++] = tok[c];
+                }
+            }
+            if (next < 0) {
+                /* p without the rejected ids, by inverse CDF with u_0 */
+                double S = 0.0;
+                for (int j = 0; j < V; ++j) {
+                    int out_of = 0;
+                    for (int r = 0; r < nrej; ++r)
+                        out_of |= rej[r] == j;
+                    w[j] = out_of ? 0.0 : row_prob(a->target, a->dtype, off, j, T, st);
+                    S += w[j];
+                }
+                if (!(S > 1e-300)) {
+                    S = 0.0;
+                    for (int j = 0; j < V; ++j) {
+                        w[j] = row_prob(a->target, a->dtype, off, j, T, st);
+                        S += w[j];
+                    }
+                }
+                const double u0 = (double)u[0], thr = u0 * S;
+                double C = 0.0, Cprev = 0.0;
+                for (int j = 0; j < V; ++j) {
+                    Cprev = C;
+                    C += w[j];
+                    if (thr < C) {
+                        emit = j;
+                        break;
+                    }
+                }
+                if (emit < 0) {
+                    for (int j = V - 1; j >= 0; --j)
+                        if (w[j] > 0.0) {
+                            emit = j;
+                            break;
+                        }
+                    if (a->samp_margin)
+                        a->samp_margin[b] = 0.0;
+                } else if (a->samp_margin) {
+                    const double lo = u0 - Cprev / S, hi = C / S - u0;
+                    a->samp_margin[b] = lo < hi ? lo : hi;
+                }
+            }
+        }
+        if (next < 0)
+            break;
+        out[n] = tok[next];
+        if (path)
+            path[n] = next;
+        ++n;
+        node = next;
+    }
+    out[n] = emit;
+    for (int k = n + 1; k < N; ++k)
+        out[k] = -1;
+    if (path)
+        for (int k = n; k < N; ++k)
+            path[k] = -1;
+    a->out_num[b] = n;
+    free(rej);
+    free(w);
+}
+
+typedef struct {
+    const tree_args *a;
+    int b0, b1;
+} tree_slice;
+
+static void *run_tree_slice(void *p)
+{
+    const tree_slice *s = (const tree_slice *)p;
+    for (int b = s->b0; b < s->b1; ++b)
+        tree_one(s->a, b);
+    return NULL;
+}
+
+/* Entry point (host memory).  target [B, N, V]; parent, tokens, uniforms
+ * [B, N]; num_nodes, temperature [B]; out_tokens, out_path [B, N]; out_num,
+ * samp_margin, seq_status [B]; acc_margin [B, N].  Returns 0, or -1 on a bad
+ * argument. */
+int oracle_tree_verify(const void *target, int dtype, const int32_t *parent, const int32_t *tokens,
+                       const int32_t *num_nodes, const float *uniforms, const float *temperature, int B, int N,
+                       int V, int32_t *out_tokens, int32_t *out_num, int32_t *out_path, double *acc_margin,
+                       double *samp_margin, int32_t *seq_status, int nthreads)
+{
+    if (B < 0 || N < 1 || V < 1 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16))
+        return -1;
+    if (B == 0)
+        return 0;
+    if (!target || !parent || !tokens || !num_nodes || !uniforms || !temperature || !out_tokens || !out_num)
+        return -1;
+    tree_args a = {target, dtype, parent, tokens, num_nodes, uniforms, temperature, B, N, V,
+                   out_tokens, out_num, out_path, acc_margin, samp_margin, seq_status};
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > B)
+        nthreads = B;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    tree_slice *sl = (tree_slice *)malloc(sizeof(tree_slice) * (size_t)nthreads);
+    if (!th || !sl) {
+        free(th);
+        free(sl);
+        return -1;
+    }
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        sl[t].a = &a;
+        sl[t].b0 = (int)((long long)B * t / nthreads);
+        sl[t].b1 = (int)((long long)B * (t + 1) / nthreads);
+        if (nthreads > 1 && pthread_create(&th[started], NULL, run_tree_slice, &sl[t]) == 0)
+            ++started;
+        else
+            run_tree_slice(&sl[t]);
+    }
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(sl);
+    return 0;
+}

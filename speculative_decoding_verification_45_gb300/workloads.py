@@ -399,3 +399,145 @@ def ngram_contexts(B: int, L: int, vocab: int, seed: int, copy_prob: float = 0.5
             row.extend(int(t) for t in piece)
         ctx[b, :n] = row[:n]
     return ctx, lens
+
+
+# ----------------------------------------------------------------------------
+# Candidate trees (tree verification)
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class TreeBatch:
+    """One tree-verification call's inputs, host-resident.
+
+    target      [B, N, V]  float32, or uint16 bfloat16 bit patterns; row k is the
+                           target's next-token logits after the path to node k
+                           (rows of nodes >= num_nodes[b] poisoned with +inf)
+    parent      [B, N]     int32, parent[b, k] < k for 1 <= k < num_nodes[b]; -1 else
+    tokens      [B, N]     int32 candidate id of node k (-1 for the root and padding)
+    num_nodes   [B]        int32 in [1, N]
+    uniforms    [B, N]     float32 in [0, 1); column k tests node k, column 0 is
+                           the final sample's draw
+    temperature [B]        float32; 0 = greedy
+    """
+
+    target: np.ndarray
+    parent: np.ndarray
+    tokens: np.ndarray
+    num_nodes: np.ndarray
+    uniforms: np.ndarray
+    temperature: np.ndarray
+    dtype: str
+    name: str = "tree"
+
+    @property
+    def B(self) -> int:
+        return int(self.parent.shape[0])
+
+    @property
+    def N(self) -> int:
+        return int(self.parent.shape[1])
+
+    @property
+    def V(self) -> int:
+        return int(self.target.shape[2])
+
+    @property
+    def elem_size(self) -> int:
+        return 2 if self.dtype == BF16 else 4
+
+    def path_bytes(self, num_accepted) -> int:
+        """Logit bytes a walk must read given the accepted path lengths: the
+        n_b + 1 rows of the path (root included), plus the 4-byte inputs and
+        outputs."""
+        rows = int((np.asarray(num_accepted, np.int64) + 1).sum())
+        small = 4 * self.B * (5 * self.N + 3)
+        return rows * self.V * self.elem_size + small
+
+
+def tree_parents(shape: str, n: int, rng: np.random.Generator) -> np.ndarray:
+    """Parent array of an n-node tree (node 0 the root, parent[0] = -1).
+
+    'chain': one candidate per position; 'star': n-1 candidates for the first
+    position; 'random': parent[k] uniform over [0, k); 'medusa': breadth-first
+    levels with 4, 3, 2, 2, 1, 1, ... children per node (the top few tokens of
+    each head combined, "Speculative Decoding" ch.5), cut at n nodes.
+    """
+    par = np.full(n, -1, np.int32)
+    if shape == "chain":
+        par[1:] = np.arange(n - 1)
+    elif shape == "star":
+        par[1:] = 0
+    elif shape == "random":
+        for k in range(1, n):
+            par[k] = rng.integers(0, k)
+    elif shape == "medusa":
+        fan = [4, 3, 2, 2]
+        level, k, depth = [0], 1, 0
+        while k < n and level:
+            nxt = []
+            f = fan[depth] if depth < len(fan) else 1
+            for node in level:
+                for _ in range(f):
+                    if k >= n:
+                        break
+                    par[k] = node
+                    nxt.append(k)
+                    k += 1
+            level, depth = nxt, depth + 1
+    else:
+        raise ValueError(f"unknown tree shape {shape}")
+    return par
+
+
+def tree_batch(B: int, N: int, V: int, dtype: str = BF16, seed: int = 0, shape: str = "medusa",
+               temps=(0.0, 0.6, 1.0), sigma: float = 0.7, ragged: bool = True, zipf: bool = True) -> TreeBatch:
+    """Seeded candidate trees.  Per sequence: num_nodes = N (or uniform in
+    [1, N] when ragged), target rows t_k ~ N(0, 3^2) (+ the Zipf shift of the
+    large workloads when zipf), and the children of node k, in index order,
+    carry the best ids of a noisy proposer view d_k = t_k + N(0, sigma^2) (the
+    top candidates of a head, deterministic).  T_b = temps[b mod len(temps)]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if dtype == BF16:
+        target = np.full((B, N, V), BF16_POS_INF, dtype=np.uint16)
+    else:
+        target = np.full((B, N, V), np.inf, dtype=np.float32)
+    parent = np.full((B, N), -1, np.int32)
+    tokens = np.full((B, N), -1, np.int32)
+    num_nodes = (rng.integers(1, N + 1, size=B) if ragged else np.full(B, N)).astype(np.int32)
+    temp = np.array([temps[b % len(temps)] for b in range(B)], dtype=np.float32)
+    for b in range(B):
+        n = int(num_nodes[b])
+        par = tree_parents(shape, n, rng)
+        parent[b, :n] = par
+        t = rng.normal(0.0, 3.0, size=(n, V))
+        if zipf:
+            t += _zipf_shift(rng, V)
+        rows = _round(t, dtype)
+        target[b, :n] = rows
+        t_rounded = logits_as_f64(rows, dtype)
+        for k in range(n):
+            kids = np.nonzero(par == k)[0]
+            if kids.size == 0:
+                continue
+            d = t_rounded[k] + rng.normal(0.0, sigma, size=V)
+            best = np.argsort(-d, kind="stable")[: kids.size]
+            tokens[b, kids] = best.astype(np.int32)
+    uniforms = rng.random((B, N), dtype=np.float32)
+    return TreeBatch(target, parent, tokens, num_nodes, uniforms, temp, dtype, f"tree-{shape}")
+
+
+def tree_tiny(p_rows, parent, tokens, count: int, seed: int, temperature: float = 1.0) -> TreeBatch:
+    """count copies of one small tree with fixed node distributions p_rows
+    (probability vectors over a tiny vocabulary; logits = ln p * T in float32,
+    zero probabilities -inf) and fresh seeded uniforms per copy."""
+    p = np.asarray(p_rows, dtype=np.float64)
+    N, V = p.shape
+    rng = np.random.Generator(np.random.PCG64(seed))
+    with np.errstate(divide="ignore"):
+        tl = (np.log(p) * temperature).astype(np.float32)
+    target = np.broadcast_to(tl, (count, N, V)).copy()
+    par = np.broadcast_to(np.asarray(parent, np.int32), (count, N)).copy()
+    tok = np.broadcast_to(np.asarray(tokens, np.int32), (count, N)).copy()
+    uniforms = rng.random((count, N), dtype=np.float32)
+    return TreeBatch(target, par, tok, np.full(count, N, np.int32), uniforms,
+                     np.full(count, temperature, np.float32), F32, "tree-tiny")

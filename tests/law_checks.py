@@ -49,3 +49,12 @@ def mean_tokens_z(out_num_accepted: np.ndarray, expected: float) -> float:
     x = out_num_accepted.astype(np.float64) + 1.0
     se = x.std(ddof=1) / np.sqrt(x.size)
     return float((x.mean() - expected) / se)
+
+
+def tree_outcome_keys(out_tokens: np.ndarray, out_num_accepted: np.ndarray, out_path: np.ndarray):
+    """Tree rounds keyed (n, node_1..node_n, y_0..y_n) as in enumerate_law.tree_outcome_law."""
+    keys = []
+    for row, n, path in zip(out_tokens, out_num_accepted, out_path):
+        n = int(n)
+        keys.append((n,) + tuple(int(v) for v in path[:n]) + tuple(int(v) for v in row[: n + 1]))
+    return keys
