@@ -87,6 +87,7 @@ extern "C" {
 #define SPEC_MAX_GAMMA 16
 #define SPEC_MAX_VOCAB (1 << 24)
 #define SPEC_MAX_BATCH (1 << 26)
+#define SPEC_MAX_TREE_NODES 256
 
 typedef enum {
     SPEC_OK = 0,
@@ -105,6 +106,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 /* An internal wait of the kernel on its own asynchronous copies exceeded its
  * iteration limit (not expected on a healthy GPU): the sequence gets -1 tokens. */
 #define SPEC_STATUS_TIMEOUT 16u
+/* spec_tree_verify: a node's parent is not an earlier node. */
+#define SPEC_STATUS_BAD_TREE 32u
 
 /* One verification round for B independent sequences (see the top of this
  * file for the operation, layout, ownership and errors).
@@ -194,6 +197,54 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
 spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, const int32_t *context_len, int B,
                                int min_n, int max_n, int gamma_max, int32_t *draft_tokens, int32_t *num_draft,
                                void *stream);
+
+/* Candidate-tree verification: one round in which the target checked a tree
+ * of candidates in one forward ("Speculative Decoding" (atonlee.tistory.com/
+ * 330) ch.5: Medusa heads propose their top few tokens per position, the
+ * combinations form a tree checked through a tree attention mask; the EAGLE
+ * paragraph of "Speculative Decoding으로 LLM 추론 속도 높이기": EAGLE-2 drafts
+ * a tree).  For each sequence b with nn = num_nodes[b] nodes:
+ *   node 0 is the root (the last emitted token); node k in [1, nn) carries the
+ *   candidate id tokens[b, k] and hangs under parent[b, k] in [0, k);
+ *   target_logits[b, k, :] is the target's next-token logits after the path
+ *   root..k (row 0: after the root).
+ * The candidates are deterministic (a proposer's top tokens), i.e. point
+ * masses.  Walking from the root, the children of the current node are tried
+ * in index order with the single-candidate rule ("Speculative Decoding"
+ * ch.3) applied to p without the ids already rejected there (R): child c is
+ * accepted iff uniforms[b, c] * (1 - p(R)) < p(tokens[b, c]), p = softmax(row /
+ * T_b); the first accepted child becomes the current node.  When none is (or
+ * the node is a leaf), one token is sampled from p without R, renormalised,
+ * by inverse CDF with uniforms[b, 0] (smallest j with u*S < C_j on the exact
+ * fixed-point grid), which keeps the target's law at every step; with one
+ * child per node this is spec_verify with point-mass drafts.  T_b == 0: the
+ * accepted child is the first whose id is the argmax of the node's raw
+ * logits (lowest id on ties), and the walk ends by emitting that argmax.
+ * Only the rows on the accepted path are read.
+ *   target_logits  [B, max_nodes, V] dtype; rows of nodes >= nn are never read
+ *   parent, tokens [B, max_nodes] int32 (entries 0 and >= nn ignored)
+ *   num_nodes      [B] int32 in [1, max_nodes]
+ *   uniforms       [B, max_nodes] float32 in [0, 1): column c tests node c,
+ *                  column 0 drives the final sample
+ *   temperature    [B] float32 (0: greedy)
+ *   out_tokens     [B, max_nodes] int32: the n accepted ids, then the sampled
+ *                  (or argmax) id, then -1
+ *   out_num_accepted [B] int32: n, the accepted path length
+ *   out_path       [B, max_nodes] int32 or NULL: the accepted node indices,
+ *                  then -1 (for keeping their cache entries)
+ * Invalid data (num_nodes outside [1, max_nodes], a parent outside [0, k), a
+ * candidate id outside [0, V), a bad temperature, a sampled row on the path
+ * without a finite normaliser) gives -1 tokens, n = 0 and a status bit
+ * (SPEC_STATUS_BAD_NUM_DRAFT for num_nodes, SPEC_STATUS_BAD_TREE, ...).
+ * options: cluster_size and counters as for spec_verify_ex (counters add
+ * nn - 1 candidates, n accepted, 1 sequence); kernel must be 0.  Limits:
+ * 1 <= max_nodes <= SPEC_MAX_TREE_NODES, 1 <= V <= SPEC_MAX_VOCAB.  Same
+ * ownership, stream and error rules as spec_verify; allocates nothing. */
+spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, const int32_t *tokens,
+                             const int32_t *num_nodes, const float *uniforms, const float *temperature,
+                             int32_t *out_tokens, int32_t *out_num_accepted, int32_t *out_path, int B,
+                             int max_nodes, int V, spec_dtype dtype, uint32_t *status, void *stream,
+                             const spec_verify_options *options);
 
 /* Launch shape spec_verify would use on the current device for these sizes:
  * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any

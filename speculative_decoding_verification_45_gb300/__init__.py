@@ -29,8 +29,10 @@ STATUS_BAD_TEMPERATURE = 2
 STATUS_BAD_NUM_DRAFT = 4
 STATUS_BAD_LOGITS = 8
 STATUS_TIMEOUT = 16
+STATUS_BAD_TREE = 32
 
 MAX_GAMMA = 16
+MAX_TREE_NODES = 256
 
 
 class SpecVerifyError(RuntimeError):
@@ -171,6 +173,68 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
     d["out_tokens"] = out_tokens
     d["out_num_accepted"] = out_num
     return d
+
+
+def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens=None,
+                out_num_accepted=None, out_path=None, status=None, stream=None, cluster_size: int = 0,
+                counters=None):
+    """One candidate-tree round on the GPU (spec_tree_verify; asynchronous on ``stream``).
+
+    target_logits [B, N, V] (row k: the target after the path to node k);
+    parent, tokens [B, N] int32 (node 0 is the root); num_nodes [B] int32;
+    uniforms [B, N] float32 (column c tests node c, column 0 drives the final
+    sample); temperature [B] float32.  Returns (out_tokens [B, N],
+    out_num_accepted [B], out_path [B, N]), int32.
+    """
+    import torch
+
+    if not target_logits.is_cuda or target_logits.dim() != 3:
+        raise ValueError("target_logits must be a [B, N, V] CUDA tensor")
+    dev = target_logits.device
+    B, N, V = target_logits.shape
+    code = _dtype_code(target_logits)
+    _check(target_logits, "target_logits", target_logits.dtype, (B, N, V), dev)
+    _check(parent, "parent", torch.int32, (B, N), dev)
+    _check(tokens, "tokens", torch.int32, (B, N), dev)
+    _check(num_nodes, "num_nodes", torch.int32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, N), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out_tokens = torch.empty((B, N), **i32) if out_tokens is None else out_tokens
+    out_num_accepted = torch.empty((B,), **i32) if out_num_accepted is None else out_num_accepted
+    out_path = torch.empty((B, N), **i32) if out_path is None else out_path
+    _check(out_tokens, "out_tokens", torch.int32, (B, N), dev)
+    _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
+    _check(out_path, "out_path", torch.int32, (B, N), dev)
+    if counters is not None and (counters.numel() < 3 or counters.element_size() != 8 or not counters.is_cuda):
+        raise ValueError("counters must be a CUDA tensor of three 64-bit integers")
+    opts = _native.Options(int(cluster_size), 0, None if counters is None else ctypes.c_void_p(counters.data_ptr()))
+    lib = _native.load()
+    rc = lib.spec_tree_verify(_ptr(target_logits), _ptr(parent), _ptr(tokens), _ptr(num_nodes), _ptr(uniforms),
+                              _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,
+                              code, _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_tree_verify")
+    return out_tokens, out_num_accepted, out_path
+
+
+def tree_to_device(tb, device="cuda"):
+    """Copy a workloads.TreeBatch (host numpy arrays) to device tensors."""
+    import numpy as np
+    import torch
+
+    if tb.dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(tb.target).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(tb.target, dtype=np.float32))
+    return dict(
+        target_logits=t.to(device),
+        parent=torch.from_numpy(np.ascontiguousarray(tb.parent, dtype=np.int32)).to(device),
+        tokens=torch.from_numpy(np.ascontiguousarray(tb.tokens, dtype=np.int32)).to(device),
+        num_nodes=torch.from_numpy(np.ascontiguousarray(tb.num_nodes, dtype=np.int32)).to(device),
+        uniforms=torch.from_numpy(np.ascontiguousarray(tb.uniforms, dtype=np.float32)).to(device),
+        temperature=torch.from_numpy(np.ascontiguousarray(tb.temperature, dtype=np.float32)).to(device),
+    )
 
 
 def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=None, cluster_size: int = 0,

@@ -98,6 +98,8 @@ def load() -> ctypes.CDLL:
         lib.spec_ngram_propose.restype = i32
         lib.spec_sample.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         lib.spec_sample.restype = i32
+        lib.spec_tree_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_tree_verify.restype = i32
         lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
         lib.spec_verify_launch_shape.restype = i32
         lib.spec_status_string.argtypes = [i32]

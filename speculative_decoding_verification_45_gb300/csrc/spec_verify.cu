@@ -412,6 +412,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     const long long slots = (long long)shp.sms * (shp.kind == kKindRing ? 2 : 4);
     prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
+    prm.parent = nullptr;
+    prm.out_path = nullptr;
     const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
 
     cudaLaunchAttribute attr[1];
@@ -419,6 +421,75 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_for(dtype, shp.kind, point), args);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    return SPEC_OK;
+}
+
+// Candidate-tree verification (spec_tree_verify): one cluster per sequence,
+// the same automatic cluster size as the chain kernels.
+spec_status run_tree(const void *target, const int32_t *parent, const int32_t *tokens, const int32_t *num_nodes,
+                     const float *uniforms, const float *temperature, int32_t *out_tokens, int32_t *out_num,
+                     int32_t *out_path, int B, int N, int V, spec_dtype dtype, uint32_t *status, void *stream,
+                     const spec_verify_options *opt)
+{
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16)
+        return SPEC_ERR_UNSUPPORTED;
+    if (B < 0 || B > SPEC_MAX_BATCH || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_VOCAB)
+        return SPEC_ERR_INVALID_ARG;
+    int want_C = 0;
+    if (opt) {
+        want_C = opt->cluster_size;
+        if (want_C < 0 || want_C > kMaxCluster || opt->kernel != 0)
+            return SPEC_ERR_INVALID_ARG;
+        if ((uintptr_t)opt->counters & 7u)
+            return SPEC_ERR_INVALID_ARG;
+    }
+    if (B == 0)
+        return SPEC_OK;
+    if (!target || !parent || !tokens || !num_nodes || !uniforms || !temperature || !out_tokens || !out_num)
+        return SPEC_ERR_INVALID_ARG;
+    const uintptr_t es = (uintptr_t)elem_size(dtype);
+    if ((uintptr_t)target % es)
+        return SPEC_ERR_INVALID_ARG;
+    const void *four[] = {parent, tokens, num_nodes, uniforms, temperature, out_tokens, out_num, out_path, status};
+    for (const void *q : four)
+        if ((uintptr_t)q & 3u)
+            return SPEC_ERR_INVALID_ARG;
+    const bool aligned = aligned16(target) && ((size_t)V * (size_t)es) % 16 == 0;
+    Shape shp;
+    spec_status st = resolve_shape(B, V, dtype, aligned, aligned ? kKindTreeAligned : kKindTree, want_C, &shp);
+    if (st != SPEC_OK)
+        return st;
+    Params prm = {};
+    prm.target = target;
+    prm.draft = nullptr;
+    prm.tokens = tokens;
+    prm.num_draft = num_nodes;
+    prm.uniforms = uniforms;
+    prm.temperature = temperature;
+    prm.out_tokens = out_tokens;
+    prm.out_num = out_num;
+    prm.status = status;
+    prm.B = B;
+    prm.gmax = N - 1;
+    prm.V = V;
+    prm.num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
+    const int slice = (prm.num_chunks + shp.C - 1) / shp.C;
+    const int tiles = (slice + kThreads - 1) / kThreads;
+    prm.scan_tiles = tiles <= kMaxScanTiles ? tiles : 0;
+    prm.ordered = 0;
+    prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
+    prm.parent = parent;
+    prm.out_path = out_path;
+    const size_t dyn = (size_t)prm.scan_tiles * kThreads * 4;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg =
+        launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
+    void *args[] = {&prm};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_for(dtype, shp.kind, false), args);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
@@ -476,6 +547,16 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
         return SPEC_ERR_UNSUPPORTED;  // the ring kernel is a full-sweep A/B variant only
     return run(logits, nullptr, nullptr, nullptr, uniforms, temperature, out_tokens, nullptr, B, 0, V, dtype, status,
                stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, options);
+}
+
+spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, const int32_t *tokens,
+                             const int32_t *num_nodes, const float *uniforms, const float *temperature,
+                             int32_t *out_tokens, int32_t *out_num_accepted, int32_t *out_path, int B,
+                             int max_nodes, int V, spec_dtype dtype, uint32_t *status, void *stream,
+                             const spec_verify_options *options)
+{
+    return run_tree(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens, out_num_accepted,
+                    out_path, B, max_nodes, V, dtype, status, stream, options);
 }
 
 spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, const int32_t *context_len, int B,

@@ -64,6 +64,8 @@ struct Params {
     int scan_tiles;  // register kernel: tiles of kThreads chunk sums kept in shared memory (0 = none)
     int ordered;     // map clusters to sequences longest-first (small B only)
     unsigned long long *counters;  // optional: += drafted, accepted, verified sequences
+    const int32_t *parent;         // tree kernel: [B, gmax+1] parent of each node (num_draft = node count)
+    int32_t *out_path;             // tree kernel: [B, gmax+1] accepted node indices, or NULL
 };
 
 // ---------------------------------------------------------------------------
@@ -371,9 +373,11 @@ struct WeightParams {
     bool residual;  // max(0, p - q) with q from the draft row
     int zero_at;    // point-mass residual: p with this id removed (-1: none)
     int zero_chunk; // the chunk holding zero_at (-1: none)
+    const int *zset;  // ZSET weights: p with these nz ids removed (a tree node's rejected candidates)
+    int nz;
 };
 
-template <typename T>
+template <typename T, bool ZSET = false>
 __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, const WeightParams &wp,
                                               float (&w)[Elem<T>::W], int chunk = -2)
 {
@@ -397,6 +401,18 @@ __device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, 
         for (int e = 0; e < Elem<T>::W; ++e)
             if (chunk * Elem<T>::W + e == wp.zero_at)
                 w[e] = 0.0f;
+    }
+    if constexpr (ZSET) {  // several rejected ids (short list in shared memory)
+        const int lo = chunk * Elem<T>::W;
+        for (int z = 0; z < wp.nz; ++z) {
+            const int id = wp.zset[z];
+            if (id >= lo && id < lo + Elem<T>::W) {
+#pragma unroll
+                for (int e = 0; e < Elem<T>::W; ++e)
+                    if (lo + e == id)
+                        w[e] = 0.0f;
+            }
+        }
     }
 }
 
@@ -554,6 +570,20 @@ struct SharedState {
     int bits;
     int timeout;
     int stop;
+};
+
+// Tree kernel: the sequence's tree and the walk's state.
+constexpr int kMaxTree = SPEC_MAX_TREE_NODES;
+static_assert(kMaxTree <= kThreads, "one thread per tree node");
+struct TreeShared {
+    int parent[kMaxTree];
+    int token[kMaxTree];
+    int child[kMaxTree];  // children of the current node, in index order
+    int rej[kMaxTree];    // ids rejected at the current node (the final sample's zero set)
+    float glog[kMaxTree]; // target logit of each child's id
+    float uch[kMaxTree];  // each child's uniform
+    int wcnt[kWarps];
+    int next, nrej, bits;
 };
 
 struct Seq {
@@ -826,6 +856,8 @@ __device__ __forceinline__ WeightParams weight_params(const SharedState &sh, con
     wp.residual = rows;
     wp.zero_at = (residual && !s.drafts) ? xn : -1;
     wp.zero_chunk = wp.zero_at >= 0 ? wp.zero_at / chunk_width : -1;
+    wp.zset = nullptr;
+    wp.nz = 0;
     return wp;
 }
 
@@ -1066,7 +1098,7 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
 // own total (only on the bonus path, where the slice mass comes from the pass-1
 // partials), the last id of the slice with weight > 0 is taken.  All threads of
 // the CTA call it.
-template <typename T, bool ALIGNED>
+template <typename T, bool ALIGNED, bool ZSET = false>
 __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
                              const WeightParams &wp, bool keep, const float *chunk_sums, unsigned long long rel,
                              int32_t *outn)
@@ -1078,7 +1110,7 @@ __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, c
         const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
         const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
         float w[W];
-        chunk_weights<T>(tv, dv, wp, w, c);
+        chunk_weights<T, ZSET>(tv, dv, wp, w, c);
         *outn = c * W + pick_in_chunk<T>(w, r);
     };
     if (keep) {
@@ -1138,7 +1170,7 @@ __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, c
         if (c < s.c1) {
             const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
             const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
-            chunk_weights<T>(tv, dv, wp, w, c);
+            chunk_weights<T, ZSET>(tv, dv, wp, w, c);
             sigma = chunk_fixed<T>(w);
             if (chunk_sum<T>(w) > 0.0f)
                 last = c;
@@ -1207,30 +1239,26 @@ __device__ __forceinline__ void sweep_rows_batched(const Params &p, SharedState 
     }
 }
 
-// Pass 2 of the register-load kernels for a sampled, valid sequence whose cut
-// is n (sh.row holds the merged statistics of rows t_n and, if n < g, d_n).
-// parts[c * stride] is CTA c's pass-1 partial of row t_n.  All threads of the
-// CTA call it; the cluster's CTAs call it together.
-//   Residual row (n < g): every CTA sums its slice's weights max(0, p - q)
-//     (pass 2a, chunk sums kept in shared memory), the slice sums cross the
-//     cluster, and the CTA whose slice holds floor(u*S) searches it.
-//   Bonus row (n == g, and spec_sample): the weights are p itself, so CTA c's
-//     slice mass is its pass-1 partial over the row's normaliser, known to
-//     every CTA already; only the owner reads its slice again, and nothing
-//     crosses the cluster.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
-                             int stride)
+// Inverse-CDF sample of one decided row across the cluster (pass 2).  The
+// weights are wp's: max(0, p - q) with q from drow, p, or p without some ids.
+// bonus: the weights are p itself, so CTA c's slice mass is its pass-1 partial
+// parts[c * stride] over the row's merged statistics tot, already known to
+// every CTA; only the owner reads its slice again and nothing crosses the
+// cluster.  Otherwise every CTA sums its slice's weights (pass 2a, chunk sums
+// kept in shared memory), the slice sums cross the cluster, and the CTA whose
+// slice holds floor(u*S) searches it.  A zero total (unreachable in exact
+// arithmetic) samples p instead.  All threads of the CTA call it; the
+// cluster's CTAs call it together.  mass_out (rank 0, may be NULL) receives S.
+template <typename T, bool ALIGNED, bool ZSET>
+__device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, const Seq &s, const T *trow,
+                                           const T *drow, WeightParams wp, bool bonus, const RowStat &tot,
+                                           const RowStat *parts, int stride, float u, int32_t *outn,
+                                           float *mass_out)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
-    const int g = s.g, b = s.b, rank = s.rank;
+    const int rank = s.rank;
     extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
-    const bool residual = n < g;
-    const T *trow = row_ptr<T>(p, s, n);
-    const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    const int xn = (residual && !s.drafts) ? p.tokens[(size_t)b * s.gmax + n] : -1;  // point mode only
-    WeightParams wp = weight_params(sh, s, n, residual, xn, W);
     const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
     const bool keep = tiles <= p.scan_tiles;
     constexpr int U2 = kUnroll / 2;
@@ -1251,7 +1279,7 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
                 float sum = 0.0f;
                 if (c < s.c1) {
                     float w[W];
-                    chunk_weights<T>(tv[u], dv[u], wp, w, c);
+                    chunk_weights<T, ZSET>(tv[u], dv[u], wp, w, c);
                     sum = chunk_sum<T>(w);
                     acc += to_fixed60(sum);
                 }
@@ -1261,11 +1289,8 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
         }
         return acc;
     };
-    int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
-    const float u = final_uniform(p, s);
 
-    if (!residual) {
-        const RowStat tot = sh.row[n];
+    if (bonus) {
         const float z = tot.hi + tot.lo;
         unsigned long long S = 0, P = 0, mine = 0;
         for (int c = 0; c < s.C; ++c) {
@@ -1278,8 +1303,8 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
                 mine = f;
             S += f;
         }
-        if (rank == 0 && tid == 0 && p.resid_mass)
-            p.resid_mass[b] = (float)S * kFixedUnit;
+        if (rank == 0 && tid == 0 && mass_out)
+            *mass_out = (float)S * kFixedUnit;
         const unsigned long long theta = scaled_floor(u, S);
         if (S == 0 || !(P <= theta && theta < P + mine))
             return;  // another CTA owns the sample
@@ -1287,27 +1312,51 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
             slice_sums();
             __syncthreads();
         }
-        owner_search<T, ALIGNED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+        owner_search<T, ALIGNED, ZSET>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
         return;
     }
 
     unsigned long long S = 0, P = 0, mine = 0;
     bool timed_out = false;
-    bool use_residual = true;
+    bool use_weights = true;
     for (int attempt = 0; attempt < 2; ++attempt) {
         mine = block_sum_u64<kWarps>(slice_sums(), sh);
         exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
-        if (S > 0 || !use_residual)
+        if (S > 0 || !use_weights)
             break;
-        use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false, -1, W);
+        use_weights = false;  // degenerate residual (unreachable in exact arithmetic): sample p
+        wp.residual = false;
+        wp.zero_at = -1;
+        wp.zero_chunk = -1;
+        wp.nz = 0;
     }
-    if (rank == 0 && tid == 0 && p.resid_mass)
-        p.resid_mass[b] = (float)S * kFixedUnit;
+    if (rank == 0 && tid == 0 && mass_out)
+        *mass_out = (float)S * kFixedUnit;
     const unsigned long long theta = scaled_floor(u, S);  // pick: C_{j-1} <= theta < C_j
     if (S == 0 || !(P <= theta && theta < P + mine))
         return;  // another CTA owns the sample (S == 0 only for an all-zero row)
-    owner_search<T, ALIGNED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+    owner_search<T, ALIGNED, ZSET>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+}
+
+// Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n
+// (sh.row holds the merged statistics of rows t_n and, if n < g, d_n; parts
+// [c * stride] is CTA c's pass-1 partial of row t_n): the residual row after a
+// rejection (max(0, p - q), or p without x_n for point-mass drafts), the bonus
+// row t_g otherwise.
+template <typename T, bool ALIGNED>
+__device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
+                             int stride)
+{
+    constexpr int W = Elem<T>::W;
+    const int g = s.g, b = s.b;
+    const bool residual = n < g;
+    const T *trow = row_ptr<T>(p, s, n);
+    const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
+    const int xn = (residual && !s.drafts) ? p.tokens[(size_t)b * s.gmax + n] : -1;  // point mode only
+    const WeightParams wp = weight_params(sh, s, n, residual, xn, W);
+    int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
+    sample_row<T, ALIGNED, false>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
+                                  final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr);
 }
 
 // ===========================================================================
@@ -1512,6 +1561,233 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     if (!s.sampled || bits)
         return;  // uniform over the cluster; no DSMEM access follows
     stream_pass2<T, ALIGNED>(p, sh, s, n, &sh.recv_pos[n & 1][0][0], 2);
+}
+
+// ===========================================================================
+// Kernel 4: candidate-tree verification (point-mass candidates)
+// ===========================================================================
+// A proposer's top candidates per position form a tree that one target
+// forward checks ("Speculative Decoding", ch.5: Medusa heads and tree
+// attention; "Speculative Decoding으로 LLM 추론 속도 높이기", EAGLE paragraph:
+// EAGLE-2 drafts a tree).  Node 0 is the root, node k >= 1 carries candidate
+// tokens[b][k] under parent[b][k] < k, and target row k is the next-token
+// distribution after the path to k.  The walk starts at the root; at each node
+// the CTAs of the cluster sweep that one row (softmax statistics, or the argmax
+// at T = 0), merge it over DSMEM and test the children in index order with
+// the page's single-candidate rule for a point mass, applied to p without the
+// ids already rejected there (R): child c passes iff u_c * (1 - p(R)) < p(x_c)
+// ("Speculative Decoding", ch.3).  The first child to pass becomes the next
+// node; when none passes, one token is sampled from p without R by the same
+// exact inverse CDF as the chain kernels (sample_row, with R as a zero set),
+// using uniforms[b][0] (the root is never tested).  T = 0 follows the child
+// whose id is the argmax, and emits the argmax where none is.  Only the rows
+// on the accepted path are read.
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
+{
+    __shared__ SharedState sh;
+    __shared__ TreeShared tr;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = (int)(blockIdx.x / (unsigned)C);
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int N = p.gmax + 1;  // node slots per sequence (<= kThreads)
+    const int nn = p.num_draft[b];
+    const float temp = p.temperature[b];
+    const size_t base = (size_t)b * N;
+
+    // every CTA of the cluster reads the same inputs, so the verdict is uniform
+    uint32_t bad = (nn >= 1 && nn <= N) ? 0u : SPEC_STATUS_BAD_NUM_DRAFT;
+    if (isnan(temp) || isinf(temp) || temp < 0.0f || (temp > 0.0f && temp < FLT_MIN))
+        bad |= SPEC_STATUS_BAD_TEMPERATURE;
+    int pk = -1, xk = -1;
+    if (!bad && tid < nn) {
+        pk = p.parent[base + tid];
+        xk = p.tokens[base + tid];
+    }
+    const bool bad_tree = tid >= 1 && tid < nn && !bad && !(pk >= 0 && pk < tid);
+    const bool bad_token = tid >= 1 && tid < nn && !bad && !(xk >= 0 && xk < p.V);
+    if (__syncthreads_or(bad_tree))
+        bad |= SPEC_STATUS_BAD_TREE;
+    if (__syncthreads_or(bad_token))
+        bad |= SPEC_STATUS_BAD_TOKEN;
+    if (bad) {
+        write_invalid(p, b, rank, bad);
+        if (rank == 0 && p.out_path && tid < N)
+            p.out_path[base + tid] = -1;
+        return;
+    }
+    if (tid < kMaxTree) {
+        tr.parent[tid] = tid < nn ? pk : -1;
+        tr.token[tid] = tid < nn ? xk : -1;
+    }
+    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
+
+    Seq s;
+    s.b = b;
+    s.g = p.gmax;
+    s.gmax = p.gmax;
+    s.V = p.V;
+    s.rank = rank;
+    s.C = C;
+    s.c0 = (int)((long long)p.num_chunks * rank / C);
+    s.c1 = (int)((long long)p.num_chunks * (rank + 1) / C);
+    s.sampled = temp > 0.0f;
+    s.point = true;
+    s.drafts = false;
+    s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
+    s.rowlen = (size_t)p.V;
+    __syncthreads();
+
+    int node = 0, n = 0, step = 0;
+    uint32_t bits = 0;
+    for (;;) {
+        // children of the current node, in index order
+        const bool is_child = tid >= 1 && tid < nn && tr.parent[tid] == node;
+        const unsigned bal = __ballot_sync(0xffffffffu, is_child);
+        if (lane == 0)
+            tr.wcnt[wid] = __popc(bal);
+        __syncthreads();
+        int before = 0, m = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            before += w < wid ? tr.wcnt[w] : 0;
+            m += tr.wcnt[w];
+        }
+        if (is_child)
+            tr.child[before + __popc(bal & ((1u << lane) - 1u))] = tid;
+        __syncthreads();
+        // the decision's logits: loaded now, stored after the sweep
+        const T *row = row_ptr<T>(p, s, node);
+        float gl = 0.0f, uc = 0.0f;
+        if (s.sampled && tid < m) {
+            const int x = tr.token[tr.child[tid]];
+            uc = p.uniforms[base + tr.child[tid]];
+            if (sizeof(T) == 2)
+                gl = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[x]);
+            else
+                gl = reinterpret_cast<const float *>(row)[x];
+        }
+        const RowStat st = sweep_row<T, ALIGNED>(s, row);
+        if (lane == 0)
+            sh.warp_part[0][wid] = st;
+        __syncthreads();
+        if (step == 0)
+            cluster_wait();  // every CTA of the cluster is running: DSMEM is addressable
+        const int par = step & 1;
+        if (tid < C) {
+            RowStat v = sh.warp_part[0][0];
+            for (int w = 1; w < kWarps; ++w)
+                v = s.sampled ? soft_merge(v, sh.warp_part[0][w]) : arg_merge(v, sh.warp_part[0][w]);
+            *cluster.map_shared_rank(&sh.recv_pos[par][rank][0], tid) = v;
+        }
+        cluster_sync_all();
+        if (tid == 0) {
+            RowStat v = sh.recv_pos[par][0][0];
+            for (int src = 1; src < C; ++src)
+                v = s.sampled ? soft_merge(v, sh.recv_pos[par][src][0]) : arg_merge(v, sh.recv_pos[par][src][0]);
+            sh.row[0] = v;
+        }
+        if (tid < m) {
+            tr.glog[tid] = gl;
+            tr.uch[tid] = uc;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int next = -1, nrej = 0;
+            uint32_t bb = 0;
+            const RowStat rs = sh.row[0];
+            if (!s.sampled) {
+                for (int j = 0; j < m; ++j)
+                    if (tr.token[tr.child[j]] == rs.idx) {
+                        next = tr.child[j];
+                        break;
+                    }
+            } else if (!soft_row_ok(rs)) {
+                bb = SPEC_STATUS_BAD_LOGITS;
+            } else {
+                const float z = rs.hi + rs.lo;
+                float pr = 0.0f;  // p(R): mass of the ids rejected at this node
+                for (int j = 0; j < m; ++j) {
+                    const int c = tr.child[j], x = tr.token[c];
+                    bool dup = false;
+                    for (int r = 0; r < nrej; ++r)
+                        dup |= tr.rej[r] == x;
+                    const float pc = dup ? 0.0f : ex2_approx(fmaf(tr.glog[j], s.k, -rs.m)) / z;
+                    if (tr.uch[j] * (1.0f - pr) < pc) {
+                        next = c;
+                        break;
+                    }
+                    if (!dup) {
+                        pr += pc;
+                        tr.rej[nrej++] = x;
+                    }
+                }
+            }
+            tr.next = next;
+            tr.nrej = nrej;
+            tr.bits = (int)bb;
+        }
+        __syncthreads();
+        if (tr.bits) {
+            bits = (uint32_t)tr.bits;
+            break;
+        }
+        const int next = tr.next;
+        if (next < 0)
+            break;
+        if (rank == 0 && tid == 0) {
+            p.out_tokens[base + n] = tr.token[next];
+            if (p.out_path)
+                p.out_path[base + n] = next;
+        }
+        ++n;
+        node = next;
+        ++step;
+    }
+
+    if (bits) {
+        write_invalid(p, b, rank, bits);
+        if (rank == 0 && p.out_path && tid < N)
+            p.out_path[base + tid] = -1;
+        return;  // uniform over the cluster; no DSMEM access follows
+    }
+    if (rank == 0) {
+        if (tid > n && tid < N)
+            p.out_tokens[base + tid] = -1;
+        if (p.out_path && tid >= n && tid < N)
+            p.out_path[base + tid] = -1;
+        if (tid == 0) {
+            if (!s.sampled)
+                p.out_tokens[base + n] = sh.row[0].idx;
+            p.out_num[b] = n;
+            if (p.counters)
+                count_round(p.counters, nn - 1, n);
+        }
+    }
+    if (!s.sampled)
+        return;
+    const RowStat rs = sh.row[0];
+    WeightParams wp;
+    wp.k = s.k;
+    wp.negmt = -rs.m;
+    wp.invzt = 1.0f / (rs.hi + rs.lo);
+    wp.negmd = 0.0f;
+    wp.invzd = 0.0f;
+    wp.residual = false;
+    wp.zero_at = -1;
+    wp.zero_chunk = -1;
+    wp.zset = tr.rej;
+    wp.nz = tr.nrej;
+    float u = p.uniforms[base];
+    if (!(u >= 0.0f))
+        u = 0.0f;
+    if (u >= 1.0f)
+        u = __uint_as_float(0x3F7FFFFFu);
+    const T *row = row_ptr<T>(p, s, node);
+    sample_row<T, ALIGNED, true>(p, sh, s, row, row, wp, tr.nrej == 0, rs, &sh.recv_pos[step & 1][0][0], 2, u,
+                                 p.out_tokens + base + n, nullptr);
 }
 
 // ===========================================================================
@@ -1793,7 +2069,9 @@ enum KernelKind {
     kKindSmall1 = 5,         // full sweep, aligned, at most 1/2/4 chunks per thread and row
     kKindSmall2 = 6,
     kKindSmall4 = 7,
-    kKinds = 8
+    kKindTreeAligned = 8,    // candidate-tree walk, 16-byte aligned rows
+    kKindTree = 9,           // candidate-tree walk, any alignment
+    kKinds = 10
 };
 
 // The kernel of one variant, as the pointer the launch API takes (nullptr: no
@@ -1816,6 +2094,16 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 2>;
     case kKindSmall4:
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 4>;
+    case kKindTreeAligned:  // candidates are point masses already: one variant
+        if constexpr (POINT)
+            return nullptr;
+        else
+            return (const void *)spec_tree_kernel<T, true>;
+    case kKindTree:
+        if constexpr (POINT)
+            return nullptr;
+        else
+            return (const void *)spec_tree_kernel<T, false>;
     case kKindEarlyAligned:
         return (const void *)spec_verify_early_kernel<T, true, POINT>;
     default:

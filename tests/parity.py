@@ -104,3 +104,52 @@ def softmax_close(gpu_vals, ref_vals, rtol=SOFTMAX_RTOL, atol=1e-30, subset=Fals
     assert worst <= 1.0, (f"error {err[np.argmax(err / bound)]:.3e} at ref {r[has][np.argmax(err / bound)]:.6e} "
                           f"exceeds rtol {rtol} / atol {atol}")
     return worst
+
+
+def compare_tree(tb, gpu_tokens, gpu_num, gpu_path, ref) -> ParityReport:
+    """GPU-vs-oracle comparison of one tree round.  Exact match of the accepted
+    path, emitted ids and count, except where the walks part at a node whose
+    decision was near a boundary in the float64 oracle: a tested child there
+    with |u - p/(1 - p(R))| < NEAR, or (both walks stopped there) a final draw
+    within NEAR of a CDF boundary.  Greedy sequences must match exactly."""
+    rep = ParityReport()
+    for b in range(tb.B):
+        sampled = tb.temperature[b] > 0
+        n_ref, n_gpu = int(ref.out_num_accepted[b]), int(gpu_num[b])
+        if int(ref.seq_status[b]):
+            rep.positions += 1
+            ok = n_gpu == 0 and np.all(gpu_tokens[b] == -1) and np.all(gpu_path[b] == -1)
+            if not ok:
+                rep.mismatches_far += 1
+                rep.far_detail.append((b, "invalid-seq", gpu_tokens[b].tolist(), n_gpu))
+            continue
+        tested = ~np.isnan(ref.acc_margin[b])
+        rep.positions += int(tested.sum()) + 1
+        if sampled:
+            rep.near_positions += int(np.sum(ref.acc_margin[b][tested] < NEAR)) + int(ref.samp_margin[b] < NEAR)
+        same = (n_gpu == n_ref and np.array_equal(gpu_tokens[b], ref.out_tokens[b])
+                and np.array_equal(gpu_path[b], ref.out_path[b]))
+        if same:
+            continue
+        if not sampled:
+            rep.mismatches_far += 1
+            rep.far_detail.append((b, "greedy", gpu_path[b][:n_gpu + 1].tolist(), ref.out_path[b][:n_ref + 1].tolist()))
+            continue
+        # the node where the walks part: end of the common accepted prefix
+        j = 0
+        while j < min(n_gpu, n_ref) and gpu_path[b, j] == ref.out_path[b, j]:
+            j += 1
+        node = int(ref.out_path[b, j - 1]) if j else 0
+        kids = [c for c in range(1, int(tb.num_nodes[b])) if tb.parent[b, c] == node]
+        margins = [ref.acc_margin[b, c] for c in kids if not np.isnan(ref.acc_margin[b, c])]
+        near = any(m < NEAR for m in margins)
+        if j == n_gpu == n_ref:
+            near = near or ref.samp_margin[b] < NEAR
+        if near:
+            rep.mismatches_near += 1
+        else:
+            rep.mismatches_far += 1
+            rep.far_detail.append((b, f"part@node{node}", gpu_path[b][:n_gpu].tolist(),
+                                   ref.out_path[b][:n_ref].tolist(), gpu_tokens[b][:n_gpu + 1].tolist(),
+                                   ref.out_tokens[b][:n_ref + 1].tolist()))
+    return rep

@@ -26,7 +26,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_sample", "spec_ngram_propose",
-              "spec_verify_launch_shape", "spec_status_string"):
+              "spec_tree_verify", "spec_verify_launch_shape", "spec_status_string"):
         assert n in names
 
 
@@ -109,4 +109,25 @@ def test_ngram_argument_checks(lib, over, code):
     rc = lib.spec_ngram_propose(vp(a["context"]) if a["context"] else None, a["stride"],
                                 vp(a["lens"]) if a["lens"] else None, a["B"], a["min_n"], a["max_n"], a["gmax"],
                                 vp(a["toks"]) if a["toks"] else None, vp(a["num"]) if a["num"] else None, None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(target=0), 1), (dict(parent=0), 1), (dict(tokens=0), 1), (dict(num_nodes=0), 1),
+    (dict(uniforms=0), 1), (dict(temperature=0), 1), (dict(out_tokens=0), 1), (dict(out_num=0), 1),
+    (dict(out_path=0x10002), 1), (dict(N=0), 1), (dict(N=257), 1), (dict(V=0), 1), (dict(B=-1), 1),
+    (dict(dtype=5), 2), (dict(target=0x10001), 1), (dict(kernel=2), 1), (dict(cluster=17), 1), (dict(B=0), 0),
+])
+def test_tree_host_argument_checks(lib, over, code):
+    # Never dereferenced: every case fails validation (or is B = 0) before a launch.
+    fake = 0x10000
+    a = dict(target=fake, parent=fake, tokens=fake, num_nodes=fake, uniforms=fake, temperature=fake,
+             out_tokens=fake, out_num=fake, out_path=None, B=4, N=16, V=1024, dtype=1, kernel=0, cluster=0)
+    a.update(over)
+    vp = ctypes.c_void_p
+    opts = _native.Options(a["cluster"], a["kernel"])
+    rc = lib.spec_tree_verify(vp(a["target"]), vp(a["parent"]), vp(a["tokens"]), vp(a["num_nodes"]),
+                              vp(a["uniforms"]), vp(a["temperature"]), vp(a["out_tokens"]), vp(a["out_num"]),
+                              vp(a["out_path"]) if a["out_path"] else None, a["B"], a["N"], a["V"], a["dtype"],
+                              None, None, ctypes.byref(opts))
     assert rc == code
