@@ -428,6 +428,45 @@ def run_ours(args):
                   "verify_point_frac_of_peak": vbytes / (times["verify_point"] / 1e3) / 1e9 / peak_l,
                   "gpu_launches": 2 * args.steps}
 
+    # candidate-tree verification: 32 sequences with 64-node Medusa-style trees
+    # over the same vocabulary, half greedy and half T = 1; the walk reads the
+    # rows on the accepted path only
+    tree = None
+    if args.kernel == "auto" and not args.quick:
+        import numpy as np
+
+        tb = workloads.tree_batch(32, 64, batch.V, dtype=batch.dtype, seed=workloads.default_seed(args.config) + 11,
+                                  shape="medusa", temps=(0.0, 1.0), ragged=False)
+        tdev = sv.tree_to_device(tb, dev)
+        t_tok = torch.empty((tb.B, tb.N), dtype=torch.int32, device=dev)
+        t_num = torch.empty((tb.B,), dtype=torch.int32, device=dev)
+        t_path = torch.empty((tb.B, tb.N), dtype=torch.int32, device=dev)
+
+        def step_tree():
+            sv.tree_verify(**tdev, out_tokens=t_tok, out_num_accepted=t_num, out_path=t_path, stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step_tree()
+        torch.cuda.synchronize()
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step_tree()
+        z.record(stream)
+        torch.cuda.synchronize()
+        t_ms = reduce_max(a.elapsed_time(z), backend) / args.steps
+        acc = t_num.cpu().numpy().astype(np.int64)
+        need = tb.path_bytes(acc)
+        peak_t, _ = measured_peaks()
+        tree = {"value": aggregate_value(tb.B, ws, 1, t_ms / 1e3), "unit": UNIT, "ms_per_step": t_ms,
+                "workload": f"B={tb.B}, 64-node Medusa-style trees (4,3,2,2 children per level), V={tb.V} "
+                            f"{tb.dtype}, half greedy / half T=1.0",
+                "mean_accepted": float(acc.mean()), "rows_read_per_step": int((acc + 1).sum()),
+                "needed_bytes_per_step": need, "hbm_gbs_needed": need / (t_ms / 1e3) / 1e9,
+                "frac_of_peak": need / (t_ms / 1e3) / 1e9 / peak_t, "gpu_launches": args.steps}
+        del tdev
+
     # end to end through the public API with host buffers: pinned H2D of every
     # input each step, the call, D2H of the outputs
     e2e = None
@@ -490,6 +529,7 @@ def run_ours(args):
         "early_exit_variant": early,
         "target_only_sampling": sampling,
         "prompt_lookup": lookup,
+        "tree_verify": tree,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -511,7 +551,7 @@ def main(argv=None):
     ap.add_argument("--kernel", choices=["auto", "stream", "ring", "early"], default="auto",
                     help="kernel choice (A/B measurement; auto = the library's default full sweep; "
                          "early = row-ordered early exit)")
-    ap.add_argument("--cluster", type=int, default=0, choices=[0, 1, 2, 4, 8, 16],
+    ap.add_argument("--cluster", type=int, default=0, choices=list(range(17)),
                     help="CTAs per sequence (0 = the library's default)")
     ap.add_argument("--quick", action="store_true", help="skip e2e, clocks and the CPU baseline (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
