@@ -570,6 +570,7 @@ struct SharedState {
     int bits;
     int timeout;
     int stop;
+    int drafted[SPEC_MAX_GAMMA];  // the sequence's drafted ids (full-sweep decision)
 };
 
 // Tree kernel: the sequence's tree and the walk's state.
@@ -718,17 +719,29 @@ __device__ __forceinline__ void count_round(unsigned long long *counters, int g,
 // so the loads overlap the sweep: the drafted id and (sampled) the target and
 // draft logits at it.
 struct Gathered {
-    int x;
-    float lt, ld;
+    int x;      // drafted id
+    float lt, ld;  // target and draft logits at x (sampled sequences)
+    float u;    // the position's accept-test uniform (sampled sequences)
 };
 
-template <typename T> __device__ __forceinline__ Gathered gather_position(const Params &p, const Seq &s, int i)
+// Position i's drafted id and uniform (lane i of warp 0).  Issued in the
+// prologue and not waited for: the values are first used at the decision.
+__device__ __forceinline__ Gathered gather_ids(const Params &p, const Seq &s, int i)
 {
-    Gathered gt{-1, 0.0f, 0.0f};
-    if (i >= s.g)
-        return gt;
-    gt.x = p.tokens[(size_t)s.b * s.gmax + i];
-    if (s.sampled && gt.x >= 0 && gt.x < s.V) {
+    Gathered gt{-1, 0.0f, 0.0f, 0.0f};
+    if (i < s.g) {
+        gt.x = p.tokens[(size_t)s.b * s.gmax + i];
+        if (s.sampled)
+            gt.u = p.uniforms[(size_t)s.b * (s.gmax + 1) + i];
+    }
+    return gt;
+}
+
+// The logits at the drafted id, once the id has arrived: issued after pass 1,
+// so they land during the cluster exchange.
+template <typename T> __device__ __forceinline__ void gather_logits(const Params &p, const Seq &s, int i, Gathered &gt)
+{
+    if (i < s.g && s.sampled && gt.x >= 0 && gt.x < s.V) {
         const T *tr = row_ptr<T>(p, s, i);
         if (sizeof(T) == 2)
             gt.lt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(tr)[gt.x]);
@@ -742,6 +755,12 @@ template <typename T> __device__ __forceinline__ Gathered gather_position(const 
                 gt.ld = reinterpret_cast<const float *>(dr)[gt.x];
         }
     }
+}
+
+template <typename T> __device__ __forceinline__ Gathered gather_position(const Params &p, const Seq &s, int i)
+{
+    Gathered gt = gather_ids(p, s, i);
+    gather_logits<T>(p, s, i, gt);
     return gt;
 }
 
@@ -770,7 +789,7 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
                     valid = valid && soft_row_ok(sd);
                     qhat = ex2_approx(fmaf(gt.ld, s.k, -sd.m)) / (sd.hi + sd.lo);
                 }
-                ok = valid && (p.uniforms[(size_t)b * (gmax + 1) + lane] * qhat < phat);
+                ok = valid && (gt.u * qhat < phat);
             }
         }
         const unsigned pass = __ballot_sync(0xffffffffu, ok);
@@ -792,6 +811,8 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
             sh.n = n;
             sh.bits = (int)bits;
         }
+        if (lane < g)
+            sh.drafted[lane] = gt.x;
         if (s.rank == 0 && s.sampled && lane < g) {
             if (p.p_hat)
                 p.p_hat[(size_t)b * gmax + lane] = phat;
@@ -817,7 +838,7 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
             int v = -1;
             if (!bits) {
                 if (tid < n)
-                    v = p.tokens[(size_t)b * gmax + tid];
+                    v = sh.drafted[tid];
                 else if (tid == n)
                     v = s.sampled ? INT_MIN : sh.row[n].idx;  // sampled: written by pass 2
             }
@@ -994,17 +1015,30 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
         if (cost[e] >= 0)
             atomicAdd(&sh.hist[cost[e]], 1);
     __syncthreads();
-    if (tid == 0) {
-        int run = 0, bin = 0;
-        for (int c = kMaxRows; c >= 0; --c) {
-            if (k < run + sh.hist[c]) {
-                bin = c;
-                break;
+    if (tid < 32) {  // bins by decreasing cost: lane j holds bins kMaxRows - j and, for j < 2, 1 - j
+        const int h0 = sh.hist[kMaxRows - tid];
+        const int h1 = tid < 2 ? sh.hist[1 - tid] : 0;
+        int inc0 = h0, inc1 = h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y0 = __shfl_up_sync(0xffffffffu, inc0, o);
+            const int y1 = __shfl_up_sync(0xffffffffu, inc1, o);
+            if (tid >= o) {
+                inc0 += y0;
+                inc1 += y1;
             }
-            run += sh.hist[c];
         }
-        sh.bin = bin;
-        sh.rank_in_bin = k - run;
+        inc1 += __shfl_sync(0xffffffffu, inc0, 31);
+        const unsigned in0 = __ballot_sync(0xffffffffu, k < inc0);
+        const unsigned in1 = __ballot_sync(0xffffffffu, tid < 2 && k < inc1);
+        const int j = in0 ? __ffs(in0) - 1 : 32 + __ffs(in1) - 1;  // k < B, so some bin holds it
+        const int src = j & 31;
+        const int inc = __shfl_sync(0xffffffffu, j < 32 ? inc0 : inc1, src);
+        const int h = __shfl_sync(0xffffffffu, j < 32 ? h0 : h1, src);
+        if (tid == 0) {
+            sh.bin = kMaxRows - j;
+            sh.rank_in_bin = k - (inc - h);
+        }
     }
     __syncthreads();
     const int bin = sh.bin, want = sh.rank_in_bin;
@@ -1068,7 +1102,12 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
 
 // One row of pass 1 over this CTA's slice, reduced over the warp: online
 // softmax statistics (sampled) or the lowest argmax (greedy).  Eight 16-byte
-// loads per thread are issued before the batch is reduced.
+// loads per thread are issued before the batch is reduced.  When the slice
+// gives a thread more than one batch of a row, the next batch is first
+// requested into L2 (prefetch.global.L2: no registers held), so the row's
+// bytes are in flight while a batch is reduced (B=256, V=128256: 86.2 us
+// against 89.7 us without; prefetching across rows or two batches ahead was
+// slower).
 template <typename T, bool ALIGNED>
 __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
 {
@@ -1076,7 +1115,16 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
     const int tid = threadIdx.x;
     RowAcc acc;
     acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
+    const bool multi = ALIGNED && s.c1 - s.c0 > kUnroll * kThreads;
     for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
+        if (multi) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int c = ch + (kUnroll + u) * kThreads;
+                if (c < s.c1)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + (size_t)c * Elem<T>::W));
+            }
+        }
         uint4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -1352,7 +1400,7 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
     const bool residual = n < g;
     const T *trow = row_ptr<T>(p, s, n);
     const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    const int xn = (residual && !s.drafts) ? p.tokens[(size_t)b * s.gmax + n] : -1;  // point mode only
+    const int xn = (residual && !s.drafts) ? sh.drafted[n] : -1;  // point mode only
     const WeightParams wp = weight_params(sh, s, n, residual, xn, W);
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
     sample_row<T, ALIGNED, false>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
@@ -1388,7 +1436,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const P
 
     const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
     const int nrows = s.drafts ? 2 * g + 1 : g + 1;
-    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
+    Gathered gt = wid == 0 ? gather_ids(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
 
     // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
     if constexpr (KB > 0) {
@@ -1401,6 +1449,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const P
                 sh.warp_part[r][wid] = st;
         }
     }
+    if (wid == 0)
+        gather_logits<T>(p, s, lane, gt);
     exchange_rows(sh, s, nrows);
     if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; no DSMEM access follows
@@ -1460,7 +1510,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     for (int i = 0; i <= g; ++i) {
         const int nslot = (s.drafts && i < g) ? 2 : 1;
         // the decision's logits at x_i, loaded ahead of the rows
-        const Gathered gt = tid == 0 ? gather_position<T>(p, s, i) : Gathered{-1, 0.0f, 0.0f};
+        const Gathered gt = tid == 0 ? gather_position<T>(p, s, i) : Gathered{-1, 0.0f, 0.0f, 0.0f};
         for (int slot = 0; slot < nslot; ++slot) {
             const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, slot ? g + 1 + i : i));
             if (lane == 0)
@@ -1487,6 +1537,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
         if (tid == 0) {
             int stop = 0;
             uint32_t bb = (uint32_t)sh.bits;
+            if (i < g)
+                sh.drafted[i] = gt.x;  // pass 2 reads the rejected id from here (point mode)
             if (bb) {
                 stop = 1;  // invalid drafted id
             } else if (i == g) {
@@ -1886,7 +1938,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const 
     const int nseg = (slice + kSegChunks - 1) / kSegChunks;  // segments per row slice
     const RingState rs{ring_mem, full_bar, empty_bar};
     uint32_t k = 0;  // segment counter, identical on both sides
-    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f};
+    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
 
     // ---- pass 1: every needed row slice in one continuous copy stream
     if (producer) {
