@@ -318,6 +318,42 @@ def run_ours(args):
     value = aggregate_value(B, ws, args.steps, ms_max / 1e3)
     ms_step = ms_max / args.steps
 
+    # the same steps replayed from a CUDA graph (how a serving loop launches a
+    # fixed-shape step): the kernels and bytes are identical; the host launch
+    # path is not in the way
+    graph = None
+    if not args.quick:
+        n_cap = 20
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        with torch.cuda.stream(gstream):
+            for _ in range(3):
+                sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=gstream,
+                          cluster_size=args.cluster, kernel=kernel)
+        torch.cuda.synchronize()
+        cg_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg_, stream=gstream):
+            for _ in range(n_cap):
+                sv.verify(**inputs, out_tokens=out_tokens, out_num_accepted=out_num, stream=gstream,
+                          cluster_size=args.cluster, kernel=kernel)
+        reps = max(1, args.steps // n_cap)
+        for _ in range(3):
+            cg_.replay()
+        torch.cuda.synchronize()
+        barrier()
+        cur = torch.cuda.current_stream(dev)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(reps):
+            cg_.replay()
+        z.record(cur)
+        torch.cuda.synchronize()
+        g_ms = reduce_max(a.elapsed_time(z), backend) / (reps * n_cap)
+        graph = {"value": aggregate_value(B, ws, 1, g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
+                 "hbm_gbs_algorithmic": algo_bytes / (g_ms / 1e3) / 1e9, "steps": reps * n_cap,
+                 "gpu_launches": reps * n_cap}
+        del cg_
+
     # the row-ordered early-exit variant on the same inputs (same outputs; it
     # reads n+1 target and min(n+1, g) draft rows per sequence)
     early = None
@@ -526,6 +562,7 @@ def run_ours(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": algo_bytes},
         "gpu_launches": args.steps,
+        "graph_replay": graph,
         "early_exit_variant": early,
         "target_only_sampling": sampling,
         "prompt_lookup": lookup,
