@@ -71,12 +71,17 @@ namespace {
 // ends at e exactly when l(e) >= n).  One CTA per sequence.
 constexpr int kMaxNgram = 64;
 constexpr int kNgramThreads = 256;
+constexpr int kNgramTile = 8192;  // context tokens staged in shared memory per step (32 KB)
 
+// The context is staged in shared memory a tile at a time (coalesced loads,
+// plus max_n tokens of halo before the tile), so every comparison reads
+// shared memory instead of a chain of dependent global loads.
 __global__ void __launch_bounds__(kNgramThreads)
     spec_ngram_kernel(const int32_t *context, long long stride, const int32_t *context_len, int min_n, int max_n,
                       int gmax, int32_t *out_tokens, int32_t *out_num)
 {
-    __shared__ int suffix[kMaxNgram];  // suffix[t] = context[L - 1 - t]
+    __shared__ int tile[kMaxNgram + kNgramTile];  // context[t0 - kMaxNgram, t0 + kNgramTile)
+    __shared__ int suffix[kMaxNgram];             // suffix[t] = context[L - 1 - t]
     __shared__ unsigned long long best_warp[kNgramThreads / 32];
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int32_t *ctx = context + (size_t)b * (size_t)stride;
@@ -84,16 +89,25 @@ __global__ void __launch_bounds__(kNgramThreads)
     L = L < 0 ? 0 : (L > stride ? (int)stride : L);
     if (tid < max_n && tid < L)
         suffix[tid] = ctx[L - 1 - tid];
-    __syncthreads();
     // (l << 32) | e, larger is better; 0 = no candidate
     unsigned long long best = 0;
-    for (int e = L - 1 - tid; e >= 1; e -= kNgramThreads) {
-        int l = 0;
-        while (l < max_n && l < e && ctx[e - 1 - l] == suffix[l])
-            ++l;
-        if (l >= min_n) {
-            const unsigned long long key = ((unsigned long long)l << 32) | (unsigned)e;
-            best = key > best ? key : best;
+    for (int t0 = 0; t0 < L - 1; t0 += kNgramTile) {  // candidate ends e in [t0 + 1, t0 + kNgramTile]
+        __syncthreads();  // the previous tile's readers are done (and suffix is written)
+        for (int i = tid; i < kMaxNgram + kNgramTile; i += kNgramThreads) {
+            const int pos = t0 - kMaxNgram + i;
+            tile[i] = (pos >= 0 && pos < L) ? ctx[pos] : -1;
+        }
+        __syncthreads();
+        const int e_hi = min(t0 + kNgramTile, L - 1);
+        const int *at = tile + kMaxNgram - t0 - 1;  // at[e - l] = context[e - 1 - l]
+        for (int e = t0 + 1 + tid; e <= e_hi; e += kNgramThreads) {
+            int l = 0;
+            while (l < max_n && l < e && at[e - l] == suffix[l])
+                ++l;
+            if (l >= min_n) {
+                const unsigned long long key = ((unsigned long long)l << 32) | (unsigned)e;
+                best = key > best ? key : best;
+            }
         }
     }
 #pragma unroll

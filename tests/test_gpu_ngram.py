@@ -29,7 +29,8 @@ def _propose(sv, ctx, lens, mn, mx, gmax):
 
 @gpu
 @pytest.mark.parametrize("L,vocab,mn,mx,gmax", [(64, 4, 1, 3, 4), (1000, 20, 2, 4, 5), (4096, 50, 1, 8, 7),
-                                                (3000, 1000, 3, 3, 16), (7, 3, 1, 64, 2)])
+                                                (3000, 1000, 3, 3, 16), (7, 3, 1, 64, 2),
+                                                (20000, 40, 1, 6, 5)])
 def test_proposals_match_oracle(sv, L, vocab, mn, mx, gmax):
     ctx, lens = workloads.ngram_contexts(48, L, vocab, seed=L + vocab)
     lens[:3] = [0, 1, 2]
