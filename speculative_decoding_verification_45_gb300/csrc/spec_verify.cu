@@ -324,12 +324,14 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
                 out->kind = kinds[i];
                 out->C = C;
                 out->sms = sms;
-                if (kinds[i] == kKindScalarAligned) {  // narrow slices: the multi-row variant
+                if (kinds[i] == kKindScalarAligned) {  // narrow slices: the multi-row variants
                     const int per_thread = ((num_chunks + C - 1) / C + kThreads - 1) / kThreads;
-                    const int small = per_thread <= 1 ? kKindSmall1
-                                      : per_thread <= 2 ? kKindSmall2
-                                      : per_thread <= 4 ? kKindSmall4
-                                                        : -1;
+                    const bool two_per_sm = (long long)B * C <= 2LL * sms;  // resident at 2 CTAs per SM
+                    const int small = per_thread <= 1                        ? kKindSmall1
+                                      : per_thread <= 2                      ? kKindSmall2
+                                      : per_thread <= 4                      ? kKindSmall4
+                                      : (per_thread <= 8 && two_per_sm) ? kKindWide8
+                                                                             : -1;
                     if (small >= 0 && cluster_launchable(dev, dt, small, C, point))
                         out->kind = small;
                 }
@@ -423,7 +425,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     // Longest-first order matters only when clusters wait for a free slot: a
     // grid that is resident at once (at most 4 CTAs per SM; 2 for the ring
     // kernel) skips it and its prologue.
-    const long long slots = (long long)shp.sms * (shp.kind == kKindRing ? 2 : 4);
+    const long long slots = (long long)shp.sms * ((shp.kind == kKindRing || shp.kind == kKindWide8) ? 2 : 4);
     prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.parent = nullptr;

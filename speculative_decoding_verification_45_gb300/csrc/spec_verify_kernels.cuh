@@ -1247,15 +1247,16 @@ __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, c
 }
 
 // Pass 1 when every thread holds at most K chunks of each row (small slices:
-// small vocabularies or large clusters): the loads of 8/K rows are issued
-// together and each row is reduced after they land, so a round needs about
-// nrows*K/8 memory round trips instead of nrows.  Same per-row results as
-// sweep_row (same chunks, same order per thread).
-template <typename T, bool ALIGNED, int K>
+// small vocabularies or large clusters): the loads of U/K rows are issued
+// together (U = 8 loads in flight, 16 for the two-CTAs-per-SM variant) and
+// each row is reduced after they land, so a round needs about nrows*K/U
+// memory round trips instead of nrows.  Same per-row results as sweep_row
+// (same chunks, same order per thread).
+template <typename T, bool ALIGNED, int K, int U = kUnroll>
 __device__ __forceinline__ void sweep_rows_batched(const Params &p, SharedState &sh, const Seq &s, int nrows)
 {
     constexpr int W = Elem<T>::W;
-    constexpr int RB = kUnroll / K;  // rows per batch
+    constexpr int RB = U / K;  // rows per batch
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int first = s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX;
     for (int step0 = 0; step0 < nrows; step0 += RB) {
@@ -1410,10 +1411,12 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
 // ===========================================================================
 // Kernel 1: register loads (any alignment; the default)
 // ===========================================================================
-// KB > 0: the slice gives every thread at most KB chunks of a row, and pass 1
-// reads 8/KB rows per round trip (sweep_rows_batched); KB == 0: one row at a time.
+// KB = 1, 2, 4: the slice gives every thread at most KB chunks of a row, and
+// pass 1 reads 8/KB rows per round trip (sweep_rows_batched); KB = 8: at most
+// 8 chunks, two rows per round trip with 16 loads in flight per thread, for
+// grids that fit in two CTAs per SM (small batches); KB = 0: one row at a time.
 template <typename T, bool ALIGNED, bool POINT, int KB>
-__global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const Params p)
+__global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_kernel(const Params p)
 {
     __shared__ SharedState sh;
     cg::cluster_group cluster = cg::this_cluster();
@@ -1439,7 +1442,9 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_stream_kernel(const P
     Gathered gt = wid == 0 ? gather_ids(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
 
     // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
-    if constexpr (KB > 0) {
+    if constexpr (KB == 8) {
+        sweep_rows_batched<T, ALIGNED, 8, 2 * kUnroll>(p, sh, s, nrows);
+    } else if constexpr (KB > 0) {
         sweep_rows_batched<T, ALIGNED, KB>(p, sh, s, nrows);
     } else {
         for (int step = 0; step < nrows; ++step) {
@@ -2123,7 +2128,8 @@ enum KernelKind {
     kKindSmall4 = 7,
     kKindTreeAligned = 8,    // candidate-tree walk, 16-byte aligned rows
     kKindTree = 9,           // candidate-tree walk, any alignment
-    kKinds = 10
+    kKindWide8 = 10,         // full sweep, aligned, at most 8 chunks per thread and row, 2 CTAs/SM
+    kKinds = 11
 };
 
 // The kernel of one variant, as the pointer the launch API takes (nullptr: no
@@ -2146,6 +2152,8 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 2>;
     case kKindSmall4:
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 4>;
+    case kKindWide8:
+        return (const void *)spec_verify_stream_kernel<T, true, POINT, 8>;
     case kKindTreeAligned:  // candidates are point masses already: one variant
         if constexpr (POINT)
             return nullptr;

@@ -133,10 +133,11 @@ def test_deterministic_and_stream(sv):
 
 
 @gpu
-@pytest.mark.parametrize("dtype,V,Cs", [("bf16", 32000, (4, 8, 16)), ("f32", 4096, (1, 2, 4)), ("f32", 1024, (1, 2))])
+@pytest.mark.parametrize("dtype,V,Cs", [("bf16", 32000, (2, 3, 4, 8, 16)), ("f32", 4096, (1, 2, 4)), ("f32", 1024, (1, 2)),
+                                        ("f32", 8192, (1, 2))])
 def test_narrow_slice_variants(sv, oracle_mod, dtype, V, Cs):
-    """Slices of at most 4, 2 or 1 chunks per thread and row select the variants
-    that read several rows per round trip.  At every such cluster size the
+    """Slices of at most 8 (small grids), 4, 2 or 1 chunks per thread and row
+    select the variants that read several rows per round trip.  At every such cluster size the
     results and diagnostics stay the oracle's, for draft rows and for point-mass
     proposals, with sampled and greedy sequences and ragged draft counts."""
     import torch
