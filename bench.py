@@ -190,6 +190,21 @@ def workload_desc(cfg: int):
     return workloads.CONFIG_NAMES[cfg]
 
 
+def make_batch(args, rank=0):
+    """The timed workload: a config with its default seed (or --seed), shifted per
+    rank; --greedy sets every temperature to 0 (config 2 has its own greedy
+    variant with argmax drafts)."""
+    from speculative_decoding_verification_45_gb300 import workloads
+
+    seed = (workloads.default_seed(args.config) if args.seed is None else args.seed) + rank
+    if args.greedy and args.config == 2:
+        return workloads.make_config(2, seed=seed, greedy=True)
+    batch = workloads.make_config(args.config, seed=seed)
+    if args.greedy:
+        batch.temperature[:] = 0.0
+    return batch
+
+
 def run_reference(args):
     """Reference arm: the float64 oracle timed on the host cores."""
     ws, rank, _ = dist_env()
@@ -198,7 +213,7 @@ def run_reference(args):
     import oracle
     from speculative_decoding_verification_45_gb300 import workloads
 
-    batch = workloads.make_config(args.config)
+    batch = make_batch(args)
     oracle.build()
     cores = os.cpu_count() or 1
     # size one step's sample so the whole run stays within ~60 s of oracle time
@@ -262,7 +277,7 @@ def run_ours(args):
     barrier()
     sv._native.load()
 
-    batch = workloads.make_config(args.config, seed=workloads.default_seed(args.config) + rank)
+    batch = make_batch(args, rank)
     B = batch.B
     inputs = sv.to_device(batch, dev)
     out_tokens = torch.empty((B, batch.gmax + 1), dtype=torch.int32, device=dev)
@@ -503,6 +518,26 @@ def run_ours(args):
                 "frac_of_peak": need / (t_ms / 1e3) / 1e9 / peak_t, "gpu_launches": args.steps}
         del tdev
 
+    # acceptance statistics of this batch (outside the timed region): the counts
+    # a serving engine exports, and E = (1 - a^(g+1)) / (1 - a) at the measured a
+    acceptance = None
+    if not args.quick:
+        import numpy as np
+
+        cnt = torch.zeros(3, dtype=torch.int64, device=dev)
+        hist = torch.zeros(sv.MAX_GAMMA + 1, dtype=torch.int64, device=dev)
+        sv.verify(**inputs, stream=stream, counters=cnt, accept_hist=hist)
+        torch.cuda.synchronize()
+        c, h = cnt.cpu().numpy(), hist.cpu().numpy()
+        drafted, accepted, seqs = int(c[0]), int(c[1]), int(c[2])
+        a_hat = accepted / drafted if drafted else 0.0
+        g = batch.gmax
+        acceptance = {"drafted": drafted, "accepted": accepted, "sequences": seqs,
+                      "alpha_hat": a_hat, "mean_tokens_per_round": (accepted + seqs) / seqs if seqs else 0.0,
+                      "E_at_alpha_hat": (1 - a_hat ** (g + 1)) / (1 - a_hat) if a_hat < 1 else g + 1.0,
+                      "accepted_count_hist": [int(x) for x in h[: g + 1]],
+                      "note": "alpha_hat pools all positions; E assumes one alpha for every position"}
+
     # end to end through the public API with host buffers: pinned H2D of every
     # input each step, the call, D2H of the outputs
     e2e = None
@@ -567,6 +602,7 @@ def run_ours(args):
         "target_only_sampling": sampling,
         "prompt_lookup": lookup,
         "tree_verify": tree,
+        "acceptance": acceptance,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -585,6 +621,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--seed", type=int, default=None, help="workload seed (default: 1234 + config)")
+    ap.add_argument("--greedy", action="store_true", help="every temperature 0 (argmax verification)")
     ap.add_argument("--kernel", choices=["auto", "stream", "ring", "early"], default="auto",
                     help="kernel choice (A/B measurement; auto = the library's default full sweep; "
                          "early = row-ordered early exit)")

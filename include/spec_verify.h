@@ -135,6 +135,9 @@ typedef struct spec_verify_options {
                            Their ratio is the acceptance rate; accepted / sequences + 1 the mean
                            tokens per round (the counts a serving engine exports, per
                            "Speculative Decoding으로 LLM 추론 속도 높이기", vLLM section).  NULL: none. */
+    uint64_t *accept_hist; /* optional device array [SPEC_MAX_GAMMA + 1] (8-byte aligned): += 1 at
+                              index n (accepted count; min(n, SPEC_MAX_GAMMA) for trees) for each
+                              verified sequence, the distribution behind the mean.  NULL: none. */
 } spec_verify_options;
 
 /* Same round, plus optional float32 diagnostics for tests (any may be NULL):

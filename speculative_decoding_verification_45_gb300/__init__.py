@@ -96,6 +96,15 @@ def _prepare(target, draft, tokens, num_draft, uniforms, temperature, out_tokens
     return B, gmax, V, code, out_tokens, out_num
 
 
+def _counter_ptr(t, n, name):
+    """Device pointer of an optional int64 CUDA tensor of at least n elements."""
+    if t is None:
+        return None
+    if not t.is_cuda or t.element_size() != 8 or t.numel() < n or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of at least {n} 64-bit integers")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream_handle(stream, device):
     import torch
 
@@ -111,7 +120,7 @@ KERNEL_EARLY = 3     # row-ordered early exit: no row after the first rejection 
 
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
            out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO,
-           counters=None):
+           counters=None, accept_hist=None):
     """One verification round on the GPU (asynchronous on ``stream``).
 
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
@@ -122,7 +131,8 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     ``draft_logits=None``: point-mass proposals (a deterministic proposer such
     as ngram_propose): accept iff u < p(x), a rejection samples p without x.
     ``counters``: optional uint64 (int64) CUDA tensor [3], += drafted ids,
-    accepted ids, verified sequences.
+    accepted ids, verified sequences.  ``accept_hist``: optional int64 CUDA
+    tensor [MAX_GAMMA + 1], += 1 at each verified sequence's accepted count.
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
@@ -130,11 +140,9 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     args = [_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft), _ptr(uniforms),
             _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code, _ptr(status),
             _stream_handle(stream, target_logits.device)]
-    if cluster_size or kernel or counters is not None:
-        if counters is not None and (counters.numel() < 3 or counters.element_size() != 8 or not counters.is_cuda):
-            raise ValueError("counters must be a CUDA tensor of three 64-bit integers")
-        opts = _native.Options(int(cluster_size), int(kernel),
-                               None if counters is None else ctypes.c_void_p(counters.data_ptr()))
+    if cluster_size or kernel or counters is not None or accept_hist is not None:
+        opts = _native.Options(int(cluster_size), int(kernel), _counter_ptr(counters, 3, "counters"),
+                               _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
         rc = lib.spec_verify_ex(*args, ctypes.byref(opts))
     else:
         rc = lib.spec_verify(*args)
@@ -177,7 +185,7 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
 
 def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens=None,
                 out_num_accepted=None, out_path=None, status=None, stream=None, cluster_size: int = 0,
-                counters=None):
+                counters=None, accept_hist=None):
     """One candidate-tree round on the GPU (spec_tree_verify; asynchronous on ``stream``).
 
     target_logits [B, N, V] (row k: the target after the path to node k);
@@ -206,9 +214,8 @@ def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature,
     _check(out_tokens, "out_tokens", torch.int32, (B, N), dev)
     _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
     _check(out_path, "out_path", torch.int32, (B, N), dev)
-    if counters is not None and (counters.numel() < 3 or counters.element_size() != 8 or not counters.is_cuda):
-        raise ValueError("counters must be a CUDA tensor of three 64-bit integers")
-    opts = _native.Options(int(cluster_size), 0, None if counters is None else ctypes.c_void_p(counters.data_ptr()))
+    opts = _native.Options(int(cluster_size), 0, _counter_ptr(counters, 3, "counters"),
+                           _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
     lib = _native.load()
     rc = lib.spec_tree_verify(_ptr(target_logits), _ptr(parent), _ptr(tokens), _ptr(num_nodes), _ptr(uniforms),
                               _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,

@@ -27,7 +27,8 @@ _lib = None
 class Options(ctypes.Structure):
     """spec_verify_options of include/spec_verify.h."""
 
-    _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int), ("counters", ctypes.c_void_p)]
+    _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int), ("counters", ctypes.c_void_p),
+                ("accept_hist", ctypes.c_void_p)]
 
 
 def nvcc_path() -> str:
@@ -65,7 +66,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     try:
         with ThreadPoolExecutor(max_workers=len(cmds)) as pool:
             logs = list(pool.map(_run, cmds))
-        logs.append(_run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]))
+        logs.append(_run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs, "-ldl"]))
     finally:
         for obj in objs:
             if os.path.exists(obj):

@@ -55,6 +55,8 @@
 
 #include "spec_verify_kernels.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace {
 
 // ===========================================================================
@@ -382,7 +384,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         return SPEC_ERR_INVALID_ARG;
     const void *four[] = {tokens, num_draft, uniforms, temperature, out_tokens, out_num, status,
                           p_hat,  q_hat,     logz_t,   logz_d,      resid_mass, seq_status};
-    if (opt && ((uintptr_t)opt->counters & 7u))
+    if (opt && (((uintptr_t)opt->counters & 7u) || ((uintptr_t)opt->accept_hist & 7u)))
         return SPEC_ERR_INVALID_ARG;
     for (const void *q : four)
         if ((uintptr_t)q & 3u)
@@ -428,6 +430,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     const long long slots = (long long)shp.sms * ((shp.kind == kKindRing || shp.kind == kKindWide8) ? 2 : 4);
     prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
+    prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
     prm.out_path = nullptr;
     const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
@@ -460,7 +463,7 @@ spec_status run_tree(const void *target, const int32_t *parent, const int32_t *t
         want_C = opt->cluster_size;
         if (want_C < 0 || want_C > kMaxCluster || opt->kernel != 0)
             return SPEC_ERR_INVALID_ARG;
-        if ((uintptr_t)opt->counters & 7u)
+        if (((uintptr_t)opt->counters & 7u) || ((uintptr_t)opt->accept_hist & 7u))
             return SPEC_ERR_INVALID_ARG;
     }
     if (B == 0)
@@ -498,6 +501,7 @@ spec_status run_tree(const void *target, const int32_t *parent, const int32_t *t
     prm.scan_tiles = tiles <= kMaxScanTiles ? tiles : 0;
     prm.ordered = 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
+    prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = parent;
     prm.out_path = out_path;
     const size_t dyn = (size_t)prm.scan_tiles * kThreads * 4;
@@ -513,6 +517,15 @@ spec_status run_tree(const void *target, const int32_t *parent, const int32_t *t
     return SPEC_OK;
 }
 
+// An NVTX range around each entry point (launch side), so that a profiler's
+// timeline names the calls; header-only NVTX, a no-op without a tool attached.
+struct NvtxScope {
+    explicit NvtxScope(const char *name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope &) = delete;
+    NvtxScope &operator=(const NvtxScope &) = delete;
+};
+
 }  // namespace
 
 extern "C" {
@@ -522,6 +535,7 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
                         int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                         spec_dtype dtype, uint32_t *status, void *stream)
 {
+    NvtxScope nvtx("spec_verify");
     if (B > 0 && (!num_draft || !out_num_accepted))
         return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
@@ -536,6 +550,7 @@ spec_status spec_verify_debug(const void *target_logits, const void *draft_logit
                               float *logz_t, float *logz_d, float *resid_mass, int32_t *seq_status,
                               const spec_verify_options *options)
 {
+    NvtxScope nvtx("spec_verify_debug");
     if (B > 0 && (!num_draft || !out_num_accepted))
         return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
@@ -548,6 +563,7 @@ spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, 
                            int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                            spec_dtype dtype, uint32_t *status, void *stream, const spec_verify_options *options)
 {
+    NvtxScope nvtx("spec_verify_ex");
     if (B > 0 && (!num_draft || !out_num_accepted))
         return SPEC_ERR_INVALID_ARG;
     return run(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens,
@@ -559,6 +575,7 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
                         int B, int V, spec_dtype dtype, uint32_t *status, void *stream,
                         const spec_verify_options *options)
 {
+    NvtxScope nvtx("spec_sample");
     if (options && options->kernel == 1)
         return SPEC_ERR_UNSUPPORTED;  // the ring kernel is a full-sweep A/B variant only
     return run(logits, nullptr, nullptr, nullptr, uniforms, temperature, out_tokens, nullptr, B, 0, V, dtype, status,
@@ -571,6 +588,7 @@ spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, c
                              int max_nodes, int V, spec_dtype dtype, uint32_t *status, void *stream,
                              const spec_verify_options *options)
 {
+    NvtxScope nvtx("spec_tree_verify");
     return run_tree(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens, out_num_accepted,
                     out_path, B, max_nodes, V, dtype, status, stream, options);
 }
@@ -579,6 +597,7 @@ spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, c
                                int min_n, int max_n, int gamma_max, int32_t *draft_tokens, int32_t *num_draft,
                                void *stream)
 {
+    NvtxScope nvtx("spec_ngram_propose");
     if (B < 0 || B > SPEC_MAX_BATCH || gamma_max < 0 || gamma_max > SPEC_MAX_GAMMA || min_n < 1 ||
         max_n < min_n || max_n > kMaxNgram || context_stride < 1 || context_stride > (int64_t)INT_MAX)
         return SPEC_ERR_INVALID_ARG;

@@ -64,6 +64,7 @@ struct Params {
     int scan_tiles;  // register kernel: tiles of kThreads chunk sums kept in shared memory (0 = none)
     int ordered;     // map clusters to sequences longest-first (small B only)
     unsigned long long *counters;  // optional: += drafted, accepted, verified sequences
+    unsigned long long *hist;      // optional: [SPEC_MAX_GAMMA + 1] += 1 at the accepted count
     const int32_t *parent;         // tree kernel: [B, gmax+1] parent of each node (num_draft = node count)
     int32_t *out_path;             // tree kernel: [B, gmax+1] accepted node indices, or NULL
 };
@@ -708,8 +709,12 @@ __device__ __forceinline__ void exchange_rows(SharedState &sh, const Seq &s, int
 // Acceptance counters of a verified sequence: drafted ids, accepted ids, and
 // one round (the page on vLLM exports the same two counts; their ratio is the
 // acceptance rate a, and accepted / rounds + 1 the tokens per round).
-__device__ __forceinline__ void count_round(unsigned long long *counters, int g, int n)
+__device__ __forceinline__ void count_round(unsigned long long *counters, unsigned long long *hist, int g, int n)
 {
+    if (hist)
+        atomicAdd(&hist[n < SPEC_MAX_GAMMA ? n : SPEC_MAX_GAMMA], 1ull);
+    if (!counters)
+        return;
     atomicAdd(&counters[0], (unsigned long long)g);
     atomicAdd(&counters[1], (unsigned long long)n);
     atomicAdd(&counters[2], 1ull);
@@ -852,8 +857,8 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
                 atomicOr(p.status, bits);
-            if (!bits && p.counters)
-                count_round(p.counters, g, n);
+            if (!bits && (p.counters || p.hist))
+                count_round(p.counters, p.hist, g, n);
         }
     }
     return s.sampled && !bits;
@@ -1611,8 +1616,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 p.seq_status[b] = (int32_t)bits;
             if (bits && p.status)
                 atomicOr(p.status, bits);
-            if (!bits && p.counters)
-                count_round(p.counters, g, n);
+            if (!bits && (p.counters || p.hist))
+                count_round(p.counters, p.hist, g, n);
         }
     }
     if (!s.sampled || bits)
@@ -1819,8 +1824,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
             if (!s.sampled)
                 p.out_tokens[base + n] = sh.row[0].idx;
             p.out_num[b] = n;
-            if (p.counters)
-                count_round(p.counters, nn - 1, n);
+            if (p.counters || p.hist)
+                count_round(p.counters, p.hist, nn - 1, n);
         }
     }
     if (!s.sampled)

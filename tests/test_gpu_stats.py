@@ -106,3 +106,27 @@ def test_greedy_is_argmax_agreement(sv):
         assert num[b] == n
         assert list(toks[b, :n]) == list(tokens[b, :n]) and toks[b, n] == am[b, n]
         assert np.all(toks[b, n + 1:] == -1)
+
+
+@gpu
+def test_counters_and_accept_hist(sv, oracle_mod):
+    """The optional counters and the accepted-count histogram agree with the
+    accepted counts the call returns, on a ragged, mixed-temperature batch with
+    an invalid sequence (which adds nothing), for both kernels."""
+    import torch
+
+    batch = workloads.make_config(4, B=40, seed=17)
+    batch.num_draft[0] = -1                      # invalid: no counts
+    ref = oracle_mod.verify_batch(batch, diagnostics=False)
+    cnt = torch.zeros(3, dtype=torch.int64, device="cuda")
+    hist = torch.zeros(sv.MAX_GAMMA + 1, dtype=torch.int64, device="cuda")
+    for kernel in (0, 3):
+        cnt.zero_()
+        hist.zero_()
+        toks, num = sv.verify(**sv.to_device(batch), kernel=kernel, counters=cnt, accept_hist=hist)
+        torch.cuda.synchronize()
+        valid = ref.seq_status == 0
+        n = num.cpu().numpy()
+        c = cnt.cpu().numpy()
+        assert c[0] == int(batch.num_draft[valid].sum()) and c[1] == int(n[valid].sum()) and c[2] == valid.sum()
+        np.testing.assert_array_equal(hist.cpu().numpy(), np.bincount(n[valid], minlength=sv.MAX_GAMMA + 1))
