@@ -114,3 +114,24 @@ def test_misaligned_logits_take_scalar_path(sv, oracle_mod):
     ref = oracle_mod.verify_batch(batch)
     rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref)
     assert rep.mismatches_far == 0, rep.far_detail
+
+
+@pytest.fixture(scope="module")
+def max_vocab_batch():
+    return workloads.edge_batch("mixed", V=1 << 24, gamma=1, B=2, dtype="bf16", seed=24)
+
+
+@gpu
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_maximum_vocabulary(sv, oracle_mod, max_vocab_batch, kernel):
+    """V = SPEC_MAX_VOCAB (2^24): slices far larger than the shared-memory chunk
+    sums (pass 2 rescans its tiles from global memory)."""
+    check_batch(sv, oracle_mod, max_vocab_batch, kernel=kernel)
+
+
+@gpu
+def test_large_batch_many_ctas(sv, oracle_mod):
+    """70000 sequences (more than the longest-first ordering handles, and a grid
+    of 70000 clusters) of a tiny vocabulary."""
+    batch = workloads.edge_batch("mixed", V=64, gamma=2, B=70000, dtype="f32", seed=70)
+    check_batch(sv, oracle_mod, batch, diagnostics=False)
