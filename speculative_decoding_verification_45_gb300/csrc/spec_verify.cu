@@ -1,57 +1,10 @@
-// spec_verify.cu -- speculative-decoding verification round on GB300 (sm_103a).
+// spec_verify.cu -- host side of libspec_verify (GB300, sm_103a).
 //
-// The operation is the modified rejection sampler stated in
-//   "Speculative Decoding" (atonlee.tistory.com/330), ch.2-3;
-//   "Speculative Decoding으로 LLM 추론 속도 높이기" (donmain.dev), section
-//   "품질은 rejection sampling이 지킨다";
-//   "Fast Inference from Transformers via Speculative Decoding" notes, method
-//   details steps 2-3;
-//   "투기적 디코딩 — 초안 모델을 무엇으로 세울 것인가", section on why the output
-//   does not change;
-// and is specified in full in include/spec_verify.h.
-//
-// Design (one kernel launch per call):
-//   * One thread-block cluster of C CTAs per sequence (C in {1,2,4,8,16},
-//     chosen from B and V).  CTA c of the cluster owns the contiguous slice
-//     [c*NC/C, (c+1)*NC/C) of 16-byte chunks of every row the sequence needs.
-//   * Pass 1 streams those slices once.  Target and draft rows of sampled
-//     sequences (T > 0) keep an online (max, sum of 2^(a-m)) per thread,
-//     a = logit * log2(e)/T, with m an integer so that rescaling is an exact
-//     power of two and the sum compensated; greedy rows (T = 0) keep
-//     (max, lowest argmax) of the raw logits.  Partials are reduced over the
-//     warp (shuffles), the CTA (shared memory) and the cluster (every CTA pushes
-//     its row partials into every other CTA's shared memory, DSMEM).
-//   * After one cluster barrier each CTA holds all partials, merges them in
-//     rank order (identical bits in every CTA) and takes the accept decision
-//     itself: one lane per draft position, a warp ballot gives the first
-//     rejection.  No second barrier is needed to broadcast it.
-//   * Pass 2 (sampled sequences only) touches the one decided row (target,
-//     plus draft when a draft was rejected): weights max(0, p - q) or p as
-//     unsigned 64-bit fixed point (2^-60 units), so every sum is exact and
-//     order-free.  Slice sums are exchanged over DSMEM; the CTA whose slice
-//     holds floor(u*S) scans its chunks and writes the sampled id.
-//
-// Two kernels share that protocol:
-//   spec_verify_stream_kernel (default) 128-bit loads straight into registers,
-//                             eight per thread in flight, 32 reducing warps per
-//                             SM; element loads when rows are not 16-byte
-//                             aligned.  Pass 2a keeps each chunk's weight sum in
-//                             shared memory, so pass 2b is a scan there plus one
-//                             reload.
-//   spec_verify_ring_kernel   16-byte-aligned rows only.  A producer warp streams
-//                             the CTA's slices through an 8-stage shared-memory
-//                             ring with cp.async.bulk (the bulk-copy engine)
-//                             and mbarriers; eight reducing warps read shared
-//                             memory.  All rows of a CTA form one copy stream
-//                             (64 KB in flight across row boundaries).  On GB300
-//                             it is slower here: the reduction is issue-bound,
-//                             and the ring's 78 KB of shared memory leaves only
-//                             16 reducing warps per SM.  Kept for A/B runs.
-// Clusters take sequences longest-first (rows to read), so the grid's tail is
-// short work.  Neither kernel uses global scratch memory, atomics on the data
-// path (only the optional status word) or unbounded waits: mbarrier waits give
-// up after a fixed number of tries and report SPEC_STATUS_TIMEOUT, and the only
-// other waits are hardware barriers that every thread reaches.
+// Argument checks, the launch shape (cluster size and kernel variant per call,
+// from B, V, the alignment and the device's SM count), the C entry points of
+// include/spec_verify.h, and the prompt-lookup kernel.  The verification
+// kernels and their design notes are in spec_verify_kernels.cuh; the
+// operation is specified in include/spec_verify.h.
 
 #include "spec_verify_kernels.cuh"
 

@@ -5,6 +5,59 @@
 // instantiates that variant's kernels (kernels_*.cu), so nvcc compiles them in
 // parallel.  Everything here has internal linkage; the variant units export
 // only the kernel lookup functions declared at the end.
+//
+// The operation is the modified rejection sampler stated in
+//   "Speculative Decoding" (atonlee.tistory.com/330), ch.2-3;
+//   "Speculative Decoding으로 LLM 추론 속도 높이기" (donmain.dev), section
+//   "품질은 rejection sampling이 지킨다";
+//   "Fast Inference from Transformers via Speculative Decoding" notes, method
+//   details steps 2-3;
+//   "투기적 디코딩 — 초안 모델을 무엇으로 세울 것인가", section on why the output
+//   does not change;
+// and is specified in full in include/spec_verify.h.
+//
+// Design (one kernel launch per call):
+//   * One thread-block cluster of C CTAs per sequence (1 <= C <= 16, chosen
+//     from B, V and the SM count).  CTA c of the cluster owns the contiguous
+//     slice [c*NC/C, (c+1)*NC/C) of 16-byte chunks of every row the sequence
+//     needs.  Grids longer than one wave take sequences longest-first.
+//   * Pass 1 streams those slices once, in batches of eight 16-byte loads per
+//     thread (the row's next batch requested into L2 first).  Target and draft
+//     rows of sampled sequences (T > 0) keep an online (max, sum of 2^(a-m))
+//     per thread, a = logit * log2(e)/T, with m an integer so that rescaling is
+//     an exact power of two and the sum compensated; greedy rows (T = 0) keep
+//     (max, lowest argmax) of the raw logits.  Partials are reduced over the
+//     warp (shuffles), the CTA (shared memory) and the cluster (every CTA
+//     pushes its row partials into every other CTA's shared memory, DSMEM).
+//   * After one cluster barrier each CTA holds all partials, merges them in
+//     rank order (identical bits in every CTA) and takes the accept decision
+//     itself: one lane per draft position, a warp ballot gives the first
+//     rejection.  No second barrier is needed to broadcast it.
+//   * Pass 2 (sampled sequences only) touches the one decided row (target,
+//     plus draft when a draft was rejected): weights max(0, p - q), p, or p
+//     without some ids, as unsigned 64-bit fixed point (2^-60 units), so every
+//     sum is exact and order-free.  Slice sums are exchanged over DSMEM; the
+//     CTA whose slice holds floor(u*S) scans its chunks and writes the id.
+//
+// Kernels sharing that protocol:
+//   spec_verify_stream_kernel (default) 128-bit loads straight into registers,
+//                             32 reducing warps per SM; element loads when rows
+//                             are not 16-byte aligned; variants that read
+//                             several rows per round trip for narrow slices.
+//   spec_verify_early_kernel  positions in order, no row after the first
+//                             rejection read.
+//   spec_tree_kernel          a walk down a tree of candidates, one row per level.
+//   spec_verify_ring_kernel   16-byte-aligned rows only.  A producer warp streams
+//                             the CTA's slices through an 8-stage shared-memory
+//                             ring with cp.async.bulk (the bulk-copy engine)
+//                             and mbarriers; eight reducing warps read shared
+//                             memory.  On GB300 it is slower here: the ring's
+//                             78 KB of shared memory leaves only 16 reducing
+//                             warps per SM.  Kept for A/B runs.
+// No kernel uses global scratch memory, atomics on the data path (only the
+// optional status word and counters) or unbounded waits: mbarrier waits give up
+// after a fixed number of tries and report SPEC_STATUS_TIMEOUT, and the only
+// other waits are hardware barriers that every thread reaches.
 
 #pragma once
 
