@@ -20,7 +20,7 @@
  *   [P4] "투기적 디코딩 — 초안 모델을 무엇으로 세울 것인가" (ailab.paldyn.com),
  *        section on why the output does not change (rule, greedy argmax).
  *
- * Readings where the pages leave a step open (each also listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - p and q are softmax(logits / T) with the sequence's own T; "/T" is a
  *     true float64 division (the pages only say that a low T sharpens both).
  *   - The accept test is evaluated as  r * q(x) < p(x), which equals the
@@ -452,7 +452,7 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
  * attention mask) and its glossary entry on tree attention; [P2]'s EAGLE
  * paragraph (EAGLE-2 draws the candidates as a tree and checks it in one
  * forward).  The pages state the acceptance rule for one candidate per
- * position only ([P1] ch.3).  Readings used here (also listed in the design doc):
+ * position only ([P1] ch.3).  Readings used here:
  *   - Node 0 is the root (the last emitted token); node k >= 1 carries the
  *     candidate token tokens[b][k] and hangs under parent[b][k] < k.  Row k of
  *     the target logits is the target's next-token distribution after the
