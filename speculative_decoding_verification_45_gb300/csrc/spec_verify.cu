@@ -353,6 +353,14 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp, point);
     if (st != SPEC_OK)
         return st;
+    if (gmax == 0 && !point && shp.kind == kKindScalarAligned) {  // the sampler: pass 1 keeps the chunk sums
+        const int chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
+        const int slice_tiles = ((chunks + shp.C - 1) / shp.C + kThreads - 1) / kThreads;
+        int dev = 0;
+        if (slice_tiles <= kMaxScanTiles && current_device(&dev) == SPEC_OK &&
+            cluster_launchable(dev, dtype, kKindSample, shp.C, false))
+            shp.kind = kKindSample;
+    }
 
     Params prm;
     prm.target = target;

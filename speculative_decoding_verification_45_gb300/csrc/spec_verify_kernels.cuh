@@ -373,6 +373,46 @@ struct RowAcc {
             t = __fadd2_rn(t, acc[q]);
         compensated_add(hi, lo, t.x + t.y);
     }
+    // add_soft that also leaves each chunk's sum of 2^(a - m) in cs[j * kThreads]
+    // (j = j0 + u: the chunk's tile in the slice, for j < tiles), rescaling the
+    // entries stored earlier when m rises.  Used for a row that pass 2 samples
+    // from as p itself (the sampler), so that its owner needs no second sweep.
+    template <typename T, int N>
+    __device__ __forceinline__ void add_soft_store(const uint4 (&v)[N], float k, float *cs, int j0, int tiles)
+    {
+        const float amax = chunks_max<T, N>(v) * k;
+        if (amax > m) {
+            const float mn = ceilf(amax);
+            const float sc = pow2_int(m - mn);
+            hi *= sc;
+            lo *= sc;
+            for (int j = 0; j < j0 && j < tiles; ++j)
+                cs[j * kThreads] *= sc;
+            m = mn;
+        }
+        if (m == -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < N; ++u)
+                if (j0 + u < tiles)
+                    cs[(j0 + u) * kThreads] = 0.0f;
+            return;
+        }
+        constexpr int P = Elem<T>::W / 2;
+        const float2 k2 = make_float2(k, k), nm2 = make_float2(-m, -m);
+        float t = 0.0f;
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            float2 a = ex2_pair(__ffma2_rn(pair<T>(v[u], 0), k2, nm2));
+#pragma unroll
+            for (int q = 1; q < P; ++q)
+                a = __fadd2_rn(a, ex2_pair(__ffma2_rn(pair<T>(v[u], q), k2, nm2)));
+            const float cu = a.x + a.y;
+            if (j0 + u < tiles)
+                cs[(j0 + u) * kThreads] = cu;
+            t += cu;
+        }
+        compensated_add(hi, lo, t);
+    }
     // Adds chunks v[0..N) of a greedy row; chunk u starts at element index
     // base + u * stride.  Chunks arrive in increasing index order, so a strict
     // improvement keeps the lowest index of the maximum.
@@ -1166,15 +1206,18 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
 // bytes are in flight while a batch is reduced (B=256, V=128256: 86.2 us
 // against 89.7 us without; prefetching across rows or two batches ahead was
 // slower).
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
+// STORE (sampled rows): each chunk's sum also goes to cs[tile * kThreads + tid],
+// relative to the warp's merged maximum once the row is done.
+template <typename T, bool ALIGNED, bool STORE = false>
+__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *cs = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
     RowAcc acc;
     acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
     const bool multi = ALIGNED && s.c1 - s.c0 > kUnroll * kThreads;
-    for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
+    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
+    for (int ch = s.c0 + tid, j0 = 0; ch < s.c1; ch += kUnroll * kThreads, j0 += kUnroll) {
         if (multi) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
@@ -1189,12 +1232,20 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row)
             const int c = ch + u * kThreads;
             v[u] = c < s.c1 ? load_chunk<T, ALIGNED>(row, c, s.V) : neg_inf_chunk<T>();
         }
-        if (s.sampled)
+        if (STORE && s.sampled)
+            acc.add_soft_store<T, kUnroll>(v, s.k, cs + tid, j0, tiles);
+        else if (s.sampled)
             acc.add_soft<T, kUnroll>(v, s.k);
         else
             acc.add_arg<T, kUnroll>(v, ch * W, kThreads * W);
     }
-    return warp_reduce(acc.stat(), s.sampled);
+    const RowStat w = warp_reduce(acc.stat(), s.sampled);
+    if (STORE && s.sampled) {  // this thread's entries, relative to the warp's maximum
+        const float sc = pow2_int(acc.m - w.m);
+        for (int j = 0; j < tiles; ++j)
+            cs[j * kThreads + tid] *= sc;
+    }
+    return w;
 }
 
 // The owner CTA's search for theta inside its slice (rel = theta - P, the
@@ -1360,7 +1411,7 @@ template <typename T, bool ALIGNED, bool ZSET>
 __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, const Seq &s, const T *trow,
                                            const T *drow, WeightParams wp, bool bonus, const RowStat &tot,
                                            const RowStat *parts, int stride, float u, int32_t *outn,
-                                           float *mass_out)
+                                           float *mass_out, const RowStat *stored = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
@@ -1416,7 +1467,13 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
         if (S == 0 || !(P <= theta && theta < P + mine))
             return;  // another CTA owns the sample
         if (keep) {
-            slice_sums();
+            if (stored) {  // pass 1 kept the chunk sums: scale them to p
+                const float f = pow2_int(stored[threadIdx.x >> 5].m - tot.m) / z;
+                for (int j = 0; j < tiles; ++j)
+                    chunk_sums[j * kThreads + tid] *= f;
+            } else {
+                slice_sums();
+            }
             __syncthreads();
         }
         owner_search<T, ALIGNED, ZSET>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
@@ -1450,9 +1507,10 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
 // [c * stride] is CTA c's pass-1 partial of row t_n): the residual row after a
 // rejection (max(0, p - q), or p without x_n for point-mass drafts), the bonus
 // row t_g otherwise.
+// stored: the row's pass-1 warp partials when pass 1 kept its chunk sums (the sampler).
 template <typename T, bool ALIGNED>
 __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
-                             int stride)
+                             int stride, const RowStat *stored = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int g = s.g, b = s.b;
@@ -1463,7 +1521,8 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
     const WeightParams wp = weight_params(sh, s, n, residual, xn, W);
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
     sample_row<T, ALIGNED, false>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
-                                  final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr);
+                                  final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr,
+                                  residual ? nullptr : stored);
 }
 
 // ===========================================================================
@@ -1472,7 +1531,9 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
 // KB = 1, 2, 4: the slice gives every thread at most KB chunks of a row, and
 // pass 1 reads 8/KB rows per round trip (sweep_rows_batched); KB = 8: at most
 // 8 chunks, two rows per round trip with 16 loads in flight per thread, for
-// grids that fit in two CTAs per SM (small batches); KB = 0: one row at a time.
+// grids that fit in two CTAs per SM (small batches); KB = 16: the sampler (one
+// row, gamma_max = 0), whose pass 1 keeps the chunk sums for pass 2; KB = 0:
+// one row at a time.
 template <typename T, bool ALIGNED, bool POINT, int KB>
 __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_kernel(const Params p)
 {
@@ -1500,7 +1561,15 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     Gathered gt = wid == 0 ? gather_ids(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
 
     // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
-    if constexpr (KB == 8) {
+    bool stored = false;
+    if constexpr (KB == 16) {
+        extern __shared__ float chunk_sums[];
+        stored = (s.c1 - s.c0 + kThreads - 1) / kThreads <= p.scan_tiles;  // room for every tile
+        const T *row = row_ptr<T>(p, s, 0);
+        const RowStat st = stored ? sweep_row<T, ALIGNED, true>(s, row, chunk_sums) : sweep_row<T, ALIGNED>(s, row);
+        if (lane == 0)
+            sh.warp_part[0][wid] = st;
+    } else if constexpr (KB == 8) {
         sweep_rows_batched<T, ALIGNED, 8, 2 * kUnroll>(p, sh, s, nrows);
     } else if constexpr (KB > 0) {
         sweep_rows_batched<T, ALIGNED, KB>(p, sh, s, nrows);
@@ -1517,7 +1586,7 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     exchange_rows(sh, s, nrows);
     if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED>(p, sh, s, sh.n, &sh.recv[0][sh.n], kMaxRows);
+    stream_pass2<T, ALIGNED>(p, sh, s, sh.n, &sh.recv[0][sh.n], kMaxRows, stored ? sh.warp_part[0] : nullptr);
 }
 
 // ===========================================================================
@@ -2187,7 +2256,8 @@ enum KernelKind {
     kKindTreeAligned = 8,    // candidate-tree walk, 16-byte aligned rows
     kKindTree = 9,           // candidate-tree walk, any alignment
     kKindWide8 = 10,         // full sweep, aligned, at most 8 chunks per thread and row, 2 CTAs/SM
-    kKinds = 11
+    kKindSample = 11,        // the sampler (gamma_max = 0), aligned: pass 1 keeps the chunk sums
+    kKinds = 12
 };
 
 // The kernel of one variant, as the pointer the launch API takes (nullptr: no
@@ -2212,6 +2282,11 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 4>;
     case kKindWide8:
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 8>;
+    case kKindSample:
+        if constexpr (POINT)
+            return nullptr;
+        else
+            return (const void *)spec_verify_stream_kernel<T, true, false, 16>;
     case kKindTreeAligned:  // candidates are point masses already: one variant
         if constexpr (POINT)
             return nullptr;
