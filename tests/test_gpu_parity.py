@@ -161,3 +161,24 @@ def test_narrow_slice_variants(sv, oracle_mod, dtype, V, Cs):
         torch.cuda.synchronize()
         rep = parity.compare(batch, toks.cpu().numpy(), num.cpu().numpy(), ref_point)
         assert rep.mismatches_far == 0, (C, "point", str(rep), rep.far_detail[:3])
+
+
+def _as_f32(batch):
+    """The same workload with float32 logits (the bf16 values, exactly)."""
+    import dataclasses
+
+    if batch.dtype == "f32":
+        return batch
+    t = workloads.logits_as_f64(batch.target, "bf16").astype(np.float32)
+    d = workloads.logits_as_f64(batch.draft, "bf16").astype(np.float32)
+    return dataclasses.replace(batch, target=t, draft=d, dtype="f32", name=batch.name + "-f32")
+
+
+@gpu
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_fp32_full_vocabulary(sv, oracle_mod, kernel):
+    """float32 logits at V=128256 (32064 chunks of four values per row: several
+    batches per thread, the L2 prefetch of the next batch) and at V=151936 with
+    ragged draft counts."""
+    for cfg, B in ((3, 12), (4, 12)):
+        check_batch(sv, oracle_mod, _as_f32(workloads.make_config(cfg, B=B)), kernel=kernel)
