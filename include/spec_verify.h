@@ -40,8 +40,8 @@
  * i > g (target) and i >= g (draft), and every draft row of a greedy
  * sequence, are never read.
  *
- * Layout.  All arrays are dense, row-major, on the device of the calling
- * thread's current CUDA context:
+ * Layout.  All arrays are dense, row-major, and readable by the device of the
+ * calling thread's current CUDA context:
  *   target_logits  [B, gamma_max + 1, V]   dtype (SPEC_F32 or SPEC_BF16)
  *   draft_logits   [B, gamma_max, V]       dtype, or NULL for point-mass proposals
  *   draft_tokens   [B, gamma_max]          int32
@@ -54,6 +54,17 @@
  * taken when both are 16-byte aligned and V * element size is a multiple of
  * 16 bytes, a scalar-load path otherwise.  int32/float32 arrays must be
  * 4-byte aligned.  Outputs must not overlap inputs.
+ * Where the inputs live.  Arrays the kernels only read (logits, tokens,
+ * num_draft, uniforms, temperature) may be device memory or page-locked host
+ * memory mapped into the device's address space (cudaHostAlloc, or
+ * cudaHostRegister with cudaHostRegisterMapped); pass the address that
+ * spec_device_pointer returns for it.  The kernels then read those bytes over
+ * the host link while they run ("zero copy"): no staging copy is made, and the
+ * early-exit kernel (options.kernel 3) moves only the rows it needs across
+ * the link.  The caller keeps such memory unchanged until the stream has
+ * passed the call.  Everything the kernels write (outputs, status, counters,
+ * diagnostics) must be device memory.  The bulk-copy ring (options.kernel 1)
+ * takes device-memory logits only (else SPEC_ERR_UNSUPPORTED).
  *
  * Ownership and execution.  The caller owns every buffer.  The call enqueues
  * one kernel on 'stream' (a cudaStream_t; NULL = legacy default stream) and
@@ -190,7 +201,8 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
  * j < L - n wins, and among its occurrences the most recent one; the proposal
  * is the min(gamma_max, L - (j + n)) tokens after it.  No occurrence: no
  * drafts.
- *   context        int32, row b starts at b * context_stride (device)
+ *   context        int32, row b starts at b * context_stride (device memory,
+ *                  or mapped host memory as for spec_verify)
  *   context_len    [B] int32, clamped to [0, context_stride]
  *   draft_tokens   [B, gamma_max] int32 (written; -1 after the proposal)
  *   num_draft      [B] int32 (written)
@@ -255,6 +267,14 @@ spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, c
  * enqueues nothing. */
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
                                      int *num_ctas, int *threads_per_cta);
+
+/* The address the kernels use for ptr: ptr itself for this device's memory,
+ * the device alias for page-locked host memory mapped into the device's
+ * address space (with unified addressing, the same value).  Returns
+ * SPEC_ERR_INVALID_ARG (and leaves *device_ptr unchanged) for pageable or
+ * unregistered host memory, another device's memory or a NULL argument, and
+ * SPEC_ERR_CUDA if the runtime query fails.  Enqueues nothing. */
+spec_status spec_device_pointer(const void *ptr, const void **device_ptr);
 
 /* Static description of a status code. */
 const char *spec_status_string(spec_status s);

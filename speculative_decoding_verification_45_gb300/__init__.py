@@ -8,7 +8,9 @@ CPU fallback: if the library is missing, every call raises.
     out_tokens, out_num = verify(target_logits, draft_logits, draft_tokens,
                                  num_draft, uniforms, temperature)
 
-See include/spec_verify.h for the operation, layouts and error behaviour.
+Inputs are CUDA tensors, or page-locked host tensors (``pin_memory()``) that
+the kernels read over the host link without a staging copy; outputs are CUDA
+tensors.  See include/spec_verify.h for the operation, layouts and error behaviour.
 """
 from __future__ import annotations
 
@@ -71,22 +73,55 @@ def _check(t, name, dtype, shape, device):
         raise ValueError(f"{name} must live on {device}, found {t.device}")
 
 
+def _check_input(t, name, dtype, shape, device):
+    """An array the kernels only read: a tensor on ``device``, or a page-locked
+    host tensor that the kernels read over the host link (zero copy)."""
+    if t.device.type == "cpu":
+        _check(t, name, dtype, shape, t.device)
+        if not t.is_pinned():
+            raise ValueError(f"{name}: a host tensor must be page-locked (pin_memory()) for the GPU to read it")
+    else:
+        _check(t, name, dtype, shape, device)
+
+
+def _in_ptr(t):
+    """Address the kernels use for an input: the CUDA tensor's own, or the
+    device alias of a page-locked host tensor (spec_device_pointer)."""
+    if t is None or t.is_cuda or t.numel() == 0:
+        return _ptr(t)
+    out = ctypes.c_void_p()
+    rc = _native.load().spec_device_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(out))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_device_pointer")
+    return out
+
+
+def _device_of(*tensors):
+    """The CUDA device of the first CUDA tensor given, else the current one."""
+    import torch
+
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def _prepare(target, draft, tokens, num_draft, uniforms, temperature, out_tokens, out_num):
     import torch
 
-    if not target.is_cuda:
-        raise ValueError("target_logits must be a CUDA tensor")
-    dev = target.device
+    if target.dim() != 3:
+        raise ValueError("target_logits must be a [B, gamma_max + 1, V] tensor")
+    dev = _device_of(target, draft, tokens, num_draft, uniforms, temperature, out_tokens, out_num)
     B, g1, V = target.shape
     gmax = g1 - 1
     code = _dtype_code(target)
-    _check(target, "target_logits", target.dtype, (B, gmax + 1, V), dev)
+    _check_input(target, "target_logits", target.dtype, (B, gmax + 1, V), dev)
     if draft is not None:  # None: point-mass proposals (q_i is 1 at the drafted id)
-        _check(draft, "draft_logits", target.dtype, (B, gmax, V), dev)
-    _check(tokens, "draft_tokens", torch.int32, (B, gmax), dev)
-    _check(num_draft, "num_draft", torch.int32, (B,), dev)
-    _check(uniforms, "uniforms", torch.float32, (B, gmax + 1), dev)
-    _check(temperature, "temperature", torch.float32, (B,), dev)
+        _check_input(draft, "draft_logits", target.dtype, (B, gmax, V), dev)
+    _check_input(tokens, "draft_tokens", torch.int32, (B, gmax), dev)
+    _check_input(num_draft, "num_draft", torch.int32, (B,), dev)
+    _check_input(uniforms, "uniforms", torch.float32, (B, gmax + 1), dev)
+    _check_input(temperature, "temperature", torch.float32, (B,), dev)
     if out_tokens is None:
         out_tokens = torch.empty((B, gmax + 1), dtype=torch.int32, device=dev)
     if out_num is None:
@@ -130,6 +165,8 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     ``kernel``: KERNEL_AUTO, KERNEL_RING, KERNEL_REGISTER or KERNEL_EARLY.
     ``draft_logits=None``: point-mass proposals (a deterministic proposer such
     as ngram_propose): accept iff u < p(x), a rejection samples p without x.
+    Inputs may be page-locked host tensors (zero copy; with KERNEL_EARLY only
+    the rows up to the first rejection cross the host link).
     ``counters``: optional uint64 (int64) CUDA tensor [3], += drafted ids,
     accepted ids, verified sequences.  ``accept_hist``: optional int64 CUDA
     tensor [MAX_GAMMA + 1], += 1 at each verified sequence's accepted count.
@@ -137,9 +174,9 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
     lib = _native.load()
-    args = [_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft), _ptr(uniforms),
-            _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code, _ptr(status),
-            _stream_handle(stream, target_logits.device)]
+    args = [_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens), _in_ptr(num_draft),
+            _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code,
+            _ptr(status), _stream_handle(stream, out_tokens.device)]
     if cluster_size or kernel or counters is not None or accept_hist is not None:
         opts = _native.Options(int(cluster_size), int(kernel), _counter_ptr(counters, 3, "counters"),
                                _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
@@ -158,7 +195,7 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
 
     B, gmax, V, code, out_tokens, out_num = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, None, None)
-    dev = target_logits.device
+    dev = out_tokens.device
     f32 = dict(dtype=torch.float32, device=dev)
     d = {
         "p_hat": torch.empty((B, gmax), **f32),
@@ -170,8 +207,9 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
         "status": torch.zeros((1,), dtype=torch.int32, device=dev),
     }
     lib = _native.load()
-    rc = lib.spec_verify_debug(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(num_draft),
-                               _ptr(uniforms), _ptr(temperature), _ptr(out_tokens), _ptr(out_num), B, gmax, V,
+    rc = lib.spec_verify_debug(_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens),
+                               _in_ptr(num_draft), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens),
+                               _ptr(out_num), B, gmax, V,
                                code, _ptr(d["status"]), _stream_handle(stream, dev), _ptr(d["p_hat"]),
                                _ptr(d["q_hat"]), _ptr(d["logz_t"]), _ptr(d["logz_d"]), _ptr(d["resid_mass"]),
                                _ptr(d["seq_status"]),
@@ -196,17 +234,18 @@ def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature,
     """
     import torch
 
-    if not target_logits.is_cuda or target_logits.dim() != 3:
-        raise ValueError("target_logits must be a [B, N, V] CUDA tensor")
-    dev = target_logits.device
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be a [B, N, V] tensor")
+    dev = _device_of(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens, out_num_accepted,
+                     out_path)
     B, N, V = target_logits.shape
     code = _dtype_code(target_logits)
-    _check(target_logits, "target_logits", target_logits.dtype, (B, N, V), dev)
-    _check(parent, "parent", torch.int32, (B, N), dev)
-    _check(tokens, "tokens", torch.int32, (B, N), dev)
-    _check(num_nodes, "num_nodes", torch.int32, (B,), dev)
-    _check(uniforms, "uniforms", torch.float32, (B, N), dev)
-    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check_input(target_logits, "target_logits", target_logits.dtype, (B, N, V), dev)
+    _check_input(parent, "parent", torch.int32, (B, N), dev)
+    _check_input(tokens, "tokens", torch.int32, (B, N), dev)
+    _check_input(num_nodes, "num_nodes", torch.int32, (B,), dev)
+    _check_input(uniforms, "uniforms", torch.float32, (B, N), dev)
+    _check_input(temperature, "temperature", torch.float32, (B,), dev)
     i32 = dict(dtype=torch.int32, device=dev)
     out_tokens = torch.empty((B, N), **i32) if out_tokens is None else out_tokens
     out_num_accepted = torch.empty((B,), **i32) if out_num_accepted is None else out_num_accepted
@@ -217,8 +256,8 @@ def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature,
     opts = _native.Options(int(cluster_size), 0, _counter_ptr(counters, 3, "counters"),
                            _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
     lib = _native.load()
-    rc = lib.spec_tree_verify(_ptr(target_logits), _ptr(parent), _ptr(tokens), _ptr(num_nodes), _ptr(uniforms),
-                              _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,
+    rc = lib.spec_tree_verify(_in_ptr(target_logits), _in_ptr(parent), _in_ptr(tokens), _in_ptr(num_nodes),
+                              _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,
                               code, _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_tree_verify")
@@ -251,20 +290,20 @@ def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=N
     a proposer, or target-only decoding.  Returns out_tokens [B] int32."""
     import torch
 
-    if not logits.is_cuda or logits.dim() != 2:
-        raise ValueError("logits must be a [B, V] CUDA tensor")
-    dev = logits.device
+    if logits.dim() != 2:
+        raise ValueError("logits must be a [B, V] tensor")
+    dev = _device_of(logits, uniforms, temperature, out_tokens)
     B, V = logits.shape
     code = _dtype_code(logits)
-    _check(logits, "logits", logits.dtype, (B, V), dev)
-    _check(uniforms, "uniforms", torch.float32, (B,), dev)
-    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check_input(logits, "logits", logits.dtype, (B, V), dev)
+    _check_input(uniforms, "uniforms", torch.float32, (B,), dev)
+    _check_input(temperature, "temperature", torch.float32, (B,), dev)
     if out_tokens is None:
         out_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
     _check(out_tokens, "out_tokens", torch.int32, (B,), dev)
     lib = _native.load()
     opts = _native.Options(int(cluster_size), int(kernel))
-    rc = lib.spec_sample(_ptr(logits), _ptr(uniforms), _ptr(temperature), _ptr(out_tokens), B, V, code,
+    rc = lib.spec_sample(_in_ptr(logits), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), B, V, code,
                          _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_sample")
@@ -278,13 +317,17 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
     num_draft [B]) for spec_verify with draft_logits=None."""
     import torch
 
-    if not context.is_cuda or context.dim() != 2 or context.dtype != torch.int32:
-        raise ValueError("context must be an int32 [B, S] CUDA tensor")
-    dev = context.device
+    if context.dim() != 2 or context.dtype != torch.int32:
+        raise ValueError("context must be an int32 [B, S] tensor")
+    dev = _device_of(context, context_len, out_tokens, out_num)
     B, S = context.shape
     if context.stride(1) != 1:
         raise ValueError("context rows must be contiguous")
-    _check(context_len, "context_len", torch.int32, (B,), dev)
+    if context.device.type == "cpu" and not context.is_pinned():
+        raise ValueError("context: a host tensor must be page-locked (pin_memory()) for the GPU to read it")
+    if context.is_cuda and context.device != dev:
+        raise ValueError(f"context must live on {dev}, found {context.device}")
+    _check_input(context_len, "context_len", torch.int32, (B,), dev)
     if out_tokens is None:
         out_tokens = torch.empty((B, gamma_max), dtype=torch.int32, device=dev)
     if out_num is None:
@@ -292,8 +335,9 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
     _check(out_tokens, "draft_tokens", torch.int32, (B, gamma_max), dev)
     _check(out_num, "num_draft", torch.int32, (B,), dev)
     lib = _native.load()
-    rc = lib.spec_ngram_propose(_ptr(context), int(context.stride(0)), _ptr(context_len), B, int(min_n), int(max_n),
-                                int(gamma_max), _ptr(out_tokens), _ptr(out_num), _stream_handle(stream, dev))
+    rc = lib.spec_ngram_propose(_in_ptr(context), int(context.stride(0)), _in_ptr(context_len), B, int(min_n),
+                                int(max_n), int(gamma_max), _ptr(out_tokens), _ptr(out_num),
+                                _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_ngram_propose")
     return out_tokens, out_num

@@ -302,6 +302,19 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// True when p lies in device (or managed) memory.  The bulk-copy ring reads
+// its rows with cp.async.bulk, which is given device memory only; the other
+// kernels read with ordinary loads and also take page-locked host memory.
+bool device_memory(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
 spec_status run(const void *target, const void *draft, const int32_t *tokens, const int32_t *num_draft,
                 const float *uniforms, const float *temperature, int32_t *out_tokens, int32_t *out_num, int B,
                 int gmax, int V, spec_dtype dtype, uint32_t *status, void *stream, float *p_hat, float *q_hat,
@@ -344,6 +357,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
     const bool point = gmax > 0 && !draft;
+    if (want_kind == kKindRing && (!device_memory(target) || (draft && !device_memory(draft))))
+        return SPEC_ERR_UNSUPPORTED;
     if (!aligned && want_kind == kKindScalarAligned)
         want_kind = kKindScalar;  // register loads work at any alignment
     if (!aligned && want_kind == kKindEarlyAligned)
@@ -596,6 +611,29 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
         *num_ctas = B * shp.C;
     if (threads_per_cta)
         *threads_per_cta = kernel_threads(shp.kind);
+    return SPEC_OK;
+}
+
+spec_status spec_device_pointer(const void *ptr, const void **device_ptr)
+{
+    if (!ptr || !device_ptr)
+        return SPEC_ERR_INVALID_ARG;
+    int dev = 0;
+    spec_status st = current_device(&dev);
+    if (st != SPEC_OK)
+        return st;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    if (!a.devicePointer)
+        return SPEC_ERR_INVALID_ARG;  // pageable or unregistered host memory
+    if ((a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device != dev)
+        return SPEC_ERR_INVALID_ARG;  // another GPU's memory
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged && a.type != cudaMemoryTypeHost)
+        return SPEC_ERR_INVALID_ARG;
+    *device_ptr = a.devicePointer;
     return SPEC_OK;
 }
 

@@ -1,0 +1,163 @@
+"""Inputs in page-locked host memory ("zero copy"): the kernels read the logits,
+ids, uniforms and temperatures over the host link with no staging copy.  The
+results must be the bits of the device-resident call (itself checked against
+the float64 oracle in the other parity tests) and agree with the oracle; the
+host checks of the binding and of spec_device_pointer reject what the GPU
+cannot read."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_45_gb300 import workloads
+from tests import parity
+from tests.test_gpu_parity import sv  # noqa: F401
+
+gpu = pytest.mark.gpu
+
+
+def _pinned(dev):
+    return {k: v.cpu().pin_memory() for k, v in dev.items()}
+
+
+def _verify(sv, inputs, kernel, point=False):
+    import torch
+
+    args = dict(inputs)
+    if point:
+        args["draft_logits"] = None
+    t, n = sv.verify(**args, kernel=kernel)
+    torch.cuda.synchronize()
+    return t.cpu().numpy(), n.cpu().numpy()
+
+
+@gpu
+@pytest.mark.parametrize("kernel", [0, 2, 3])
+@pytest.mark.parametrize("cfg,B", [(1, None), (3, 24), (4, 16)])
+def test_host_inputs_match_device_and_oracle(sv, oracle_mod, cfg, B, kernel):
+    batch = workloads.make_config(cfg, B=B)
+    dev = sv.to_device(batch)
+    ref_t, ref_n = _verify(sv, dev, kernel)
+    got_t, got_n = _verify(sv, _pinned(dev), kernel)
+    np.testing.assert_array_equal(got_t, ref_t)
+    np.testing.assert_array_equal(got_n, ref_n)
+    rep = parity.compare(batch, got_t, got_n, oracle_mod.verify_batch(batch))
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
+
+
+@gpu
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_host_inputs_point_mass(sv, kernel):
+    batch = workloads.make_config(3, B=16)
+    dev = sv.to_device(batch)
+    ref = _verify(sv, dev, kernel, point=True)
+    got = _verify(sv, _pinned(dev), kernel, point=True)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+
+
+@gpu
+def test_host_inputs_mixed_with_device_inputs(sv):
+    """Only the logits on the host, the small arrays on the device."""
+    batch = workloads.make_config(4, B=8)
+    dev = sv.to_device(batch)
+    ref = _verify(sv, dev, 0)
+    mixed = dict(dev)
+    mixed["target_logits"] = dev["target_logits"].cpu().pin_memory()
+    mixed["draft_logits"] = dev["draft_logits"].cpu().pin_memory()
+    got = _verify(sv, mixed, 3)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+
+
+@gpu
+def test_host_inputs_full_size_early_exit(sv):
+    """The 256-sequence, 128256-id workload the benchmark reads over the link."""
+    batch = workloads.make_config(5)
+    dev = sv.to_device(batch)
+    ref = _verify(sv, dev, 2)
+    host = _pinned(dev)
+    for kernel in (3, 2):
+        got = _verify(sv, host, kernel)
+        np.testing.assert_array_equal(got[0], ref[0])
+        np.testing.assert_array_equal(got[1], ref[1])
+
+
+@gpu
+def test_host_inputs_debug_diagnostics_identical(sv):
+    import torch
+
+    batch = workloads.make_config(3, B=8)
+    dev = sv.to_device(batch)
+    a = sv.verify_debug(**dev)
+    b = sv.verify_debug(**_pinned(dev))
+    torch.cuda.synchronize()
+    for k in a:
+        np.testing.assert_array_equal(a[k].cpu().numpy(), b[k].cpu().numpy(), err_msg=k)
+
+
+@gpu
+def test_host_inputs_sample_tree_ngram(sv):
+    import torch
+
+    batch = workloads.make_config(3, B=32)
+    dev = sv.to_device(batch)
+    logits = dev["target_logits"][:, 0].contiguous()
+    u = dev["uniforms"][:, 0].contiguous()
+    a = sv.sample(logits, u, dev["temperature"])
+    b = sv.sample(logits.cpu().pin_memory(), u.cpu().pin_memory(), dev["temperature"].cpu().pin_memory())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+
+    tb = workloads.tree_batch(8, 24, 4099, "bf16", seed=3, shape="random")
+    tdev = sv.tree_to_device(tb)
+    ra = sv.tree_verify(**tdev)
+    rb = sv.tree_verify(**_pinned(tdev))
+    torch.cuda.synchronize()
+    for x, y in zip(ra, rb):
+        np.testing.assert_array_equal(x.cpu().numpy(), y.cpu().numpy())
+
+    ctx, lens = workloads.ngram_contexts(16, 1024, 500, seed=5)
+    ca = sv.ngram_propose(torch.from_numpy(ctx).cuda(), torch.from_numpy(lens).cuda(), 1, 4, 6)
+    cb = sv.ngram_propose(torch.from_numpy(ctx).pin_memory(), torch.from_numpy(lens).pin_memory(), 1, 4, 6)
+    torch.cuda.synchronize()
+    for x, y in zip(ca, cb):
+        np.testing.assert_array_equal(x.cpu().numpy(), y.cpu().numpy())
+
+
+@gpu
+def test_pageable_host_tensor_rejected(sv):
+    batch = workloads.make_config(1)
+    dev = sv.to_device(batch)
+    args = dict(dev)
+    args["target_logits"] = dev["target_logits"].cpu()  # not page-locked
+    with pytest.raises(ValueError, match="page-locked"):
+        sv.verify(**args)
+
+
+@gpu
+def test_ring_kernel_takes_device_logits_only(sv):
+    batch = workloads.make_config(3, B=4)
+    dev = sv.to_device(batch)
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.verify(**_pinned(dev), kernel=sv.KERNEL_RING)
+    assert e.value.code == sv.SPEC_ERR_UNSUPPORTED
+
+
+@gpu
+def test_spec_device_pointer(sv):
+    import torch
+
+    lib = sv._native.load()
+    out = ctypes.c_void_p()
+    d = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    assert lib.spec_device_pointer(ctypes.c_void_p(d.data_ptr()), ctypes.byref(out)) == sv.SPEC_OK
+    assert out.value == d.data_ptr()
+    h = torch.empty(4096, dtype=torch.uint8).pin_memory()
+    assert lib.spec_device_pointer(ctypes.c_void_p(h.data_ptr() + 256), ctypes.byref(out)) == sv.SPEC_OK
+    assert out.value is not None  # with unified addressing the alias equals the host address
+    pageable = np.zeros(4096, np.uint8)
+    out = ctypes.c_void_p(7)
+    rc = lib.spec_device_pointer(ctypes.c_void_p(pageable.ctypes.data), ctypes.byref(out))
+    assert rc == sv.SPEC_ERR_INVALID_ARG and out.value == 7
+    assert lib.spec_device_pointer(None, ctypes.byref(out)) == sv.SPEC_ERR_INVALID_ARG
