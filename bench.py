@@ -333,6 +333,23 @@ def run_ours(args):
     value = aggregate_value(B, ws, args.steps, ms_max / 1e3)
     ms_step = ms_max / args.steps
 
+    # the distribution of single calls: each of 200 back-to-back calls between
+    # its own CUDA events (median, p10 and p90 of the device time)
+    per_call = None
+    if not args.quick:
+        import numpy as np
+
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(200)]
+        torch.cuda.synchronize()
+        for a, z in pairs:
+            a.record(stream)
+            step()
+            z.record(stream)
+        torch.cuda.synchronize()
+        us = np.array([a.elapsed_time(z) * 1e3 for a, z in pairs])
+        per_call = {"median_us": float(np.median(us)), "p10_us": float(np.percentile(us, 10)),
+                    "p90_us": float(np.percentile(us, 90)), "calls": len(pairs)}
+
     # the same steps replayed from a CUDA graph (how a serving loop launches a
     # fixed-shape step): the kernels and bytes are identical; the host launch
     # path is not in the way
@@ -633,6 +650,7 @@ def run_ours(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": algo_bytes},
         "gpu_launches": args.steps,
+        "per_call_us": per_call,
         "graph_replay": graph,
         "early_exit_variant": early,
         "target_only_sampling": sampling,
