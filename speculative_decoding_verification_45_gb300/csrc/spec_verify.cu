@@ -101,9 +101,15 @@ const void *kernel_for(spec_dtype dt, int kind, bool point)
 }
 
 int kernel_threads(int kind) { return kind == kKindRing ? kTmaThreads : kThreads; }
-// Largest dynamic shared memory a kernel kind is launched with: the ring, or
-// the register kernel's chunk sums.
-int kernel_dyn_smem(int kind) { return kind == kKindRing ? kRingBytes : kMaxScanTiles * kThreads * 4; }
+// Dynamic shared memory of the staged early-exit kernel at most: its chunk sums
+// and its copies of the decided rows' slices (one CTA per SM).
+constexpr int kStagedDynMax = 200 * 1024;
+// Largest dynamic shared memory a kernel kind is launched with: the ring, the
+// staged early exit, or the register kernels' chunk sums.
+int kernel_dyn_smem(int kind)
+{
+    return kind == kKindRing ? kRingBytes : kind == kKindEarlyStaged ? kStagedDynMax : kMaxScanTiles * kThreads * 4;
+}
 int variant_slot(spec_dtype dt, int kind, bool point)
 {
     return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
@@ -357,7 +363,9 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
     const bool point = gmax > 0 && !draft;
-    if (want_kind == kKindRing && (!device_memory(target) || (draft && !device_memory(draft))))
+    const bool host_rows = (want_kind == kKindRing || (want_kind == kKindEarlyAligned && aligned)) &&
+                           (!device_memory(target) || (draft && !device_memory(draft)));
+    if (want_kind == kKindRing && host_rows)
         return SPEC_ERR_UNSUPPORTED;
     if (!aligned && want_kind == kKindScalarAligned)
         want_kind = kKindScalar;  // register loads work at any alignment
@@ -368,6 +376,28 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp, point);
     if (st != SPEC_OK)
         return st;
+    const int nslot = point ? 1 : 2;  // rows a position reads: t_i, and d_i unless point-mass
+    if (host_rows && shp.kind == kKindEarlyAligned) {
+        // Rows read over the host link reach no cache, so the early exit keeps
+        // each position's slices in shared memory for pass 2: the smallest
+        // cluster (from the automatic or requested one) whose slices fit.
+        int dev = 0;
+        if (current_device(&dev) == SPEC_OK) {
+            const int chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
+            for (int C = shp.C; C <= kMaxCluster; ++C) {
+                if (want_C > 0 && C != want_C)
+                    break;
+                const long long cap = (chunks + C - 1) / C;
+                const long long tiles = (cap + kThreads - 1) / kThreads;
+                const long long need = (tiles <= kMaxScanTiles ? tiles * kThreads * 4 : 0) + nslot * cap * 16;
+                if (need <= kStagedDynMax && cluster_launchable(dev, dtype, kKindEarlyStaged, C, point)) {
+                    shp.kind = kKindEarlyStaged;
+                    shp.C = C;
+                    break;
+                }
+            }
+        }
+    }
     if (gmax == 0 && !point && shp.kind == kKindScalarAligned) {  // the sampler: pass 1 keeps the chunk sums
         const int chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
         const int slice_tiles = ((chunks + shp.C - 1) / shp.C + kThreads - 1) / kThreads;
@@ -403,13 +433,17 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     // Longest-first order matters only when clusters wait for a free slot: a
     // grid that is resident at once (at most 4 CTAs per SM; 2 for the ring
     // kernel) skips it and its prologue.
-    const long long slots = (long long)shp.sms * ((shp.kind == kKindRing || shp.kind == kKindWide8) ? 2 : 4);
+    const long long slots = (long long)shp.sms * (shp.kind == kKindEarlyStaged                          ? 1
+                                                  : (shp.kind == kKindRing || shp.kind == kKindWide8) ? 2
+                                                                                                      : 4);
     prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
     prm.out_path = nullptr;
-    const size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
+    size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
+    if (shp.kind == kKindEarlyStaged)
+        dyn += (size_t)nslot * (size_t)slice * 16;
 
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg =

@@ -1208,8 +1208,11 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
 // slower).
 // STORE (sampled rows): each chunk's sum also goes to cs[tile * kThreads + tid],
 // relative to the warp's merged maximum once the row is done.
-template <typename T, bool ALIGNED, bool STORE = false>
-__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *cs = nullptr)
+// STAGE: every chunk of the slice is also kept in shared memory, stage[c - c0],
+// for a pass 2 that must not read the row again (rows in host memory).
+template <typename T, bool ALIGNED, bool STORE = false, bool STAGE = false>
+__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *cs = nullptr,
+                                             uint4 *stage = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
@@ -1232,6 +1235,14 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *
             const int c = ch + u * kThreads;
             v[u] = c < s.c1 ? load_chunk<T, ALIGNED>(row, c, s.V) : neg_inf_chunk<T>();
         }
+        if constexpr (STAGE) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int c = ch + u * kThreads;
+                if (c < s.c1)
+                    stage[c - s.c0] = v[u];
+            }
+        }
         if (STORE && s.sampled)
             acc.add_soft_store<T, kUnroll>(v, s.k, cs + tid, j0, tiles);
         else if (s.sampled)
@@ -1248,6 +1259,17 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *
     return w;
 }
 
+// Chunk c of a decided row's slice for pass 2: loaded from the row, or (STAGED)
+// taken from the copy pass 1 left in shared memory.
+template <typename T, bool ALIGNED, bool STAGED>
+__device__ __forceinline__ uint4 slice_chunk(const T *row, const uint4 *stage, int c, const Seq &s)
+{
+    if constexpr (STAGED)
+        return stage[c - s.c0];
+    else
+        return load_chunk<T, ALIGNED>(row, c, s.V);
+}
+
 // The owner CTA's search for theta inside its slice (rel = theta - P, the
 // offset from the slice's start on the exact grid).  With 'keep', chunk_sums
 // holds the slice's chunk sums ([tile][lane]); otherwise the slice is scanned
@@ -1255,17 +1277,17 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *
 // own total (only on the bonus path, where the slice mass comes from the pass-1
 // partials), the last id of the slice with weight > 0 is taken.  All threads of
 // the CTA call it.
-template <typename T, bool ALIGNED, bool ZSET = false>
+template <typename T, bool ALIGNED, bool ZSET = false, bool STAGED = false>
 __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
                              const WeightParams &wp, bool keep, const float *chunk_sums, unsigned long long rel,
-                             int32_t *outn)
+                             int32_t *outn, const uint4 *tst = nullptr, const uint4 *dst = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
     auto pick_at = [&](int c, unsigned long long r) {
-        const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
-        const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+        const uint4 tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
+        const uint4 dv = wp.residual ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s) : tv;
         float w[W];
         chunk_weights<T, ZSET>(tv, dv, wp, w, c);
         *outn = c * W + pick_in_chunk<T>(w, r);
@@ -1325,8 +1347,8 @@ __device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, c
         float w[W];
         unsigned long long sigma = 0;
         if (c < s.c1) {
-            const uint4 tv = load_chunk<T, ALIGNED>(trow, c, s.V);
-            const uint4 dv = wp.residual ? load_chunk<T, ALIGNED>(drow, c, s.V) : tv;
+            const uint4 tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
+            const uint4 dv = wp.residual ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s) : tv;
             chunk_weights<T, ZSET>(tv, dv, wp, w, c);
             sigma = chunk_fixed<T>(w);
             if (chunk_sum<T>(w) > 0.0f)
@@ -1407,11 +1429,14 @@ __device__ __forceinline__ void sweep_rows_batched(const Params &p, SharedState 
 // slice holds floor(u*S) searches it.  A zero total (unreachable in exact
 // arithmetic) samples p instead.  All threads of the CTA call it; the
 // cluster's CTAs call it together.  mass_out (rank 0, may be NULL) receives S.
-template <typename T, bool ALIGNED, bool ZSET>
+// STAGED: the slices of trow and drow are read from the shared-memory copies
+// tst and dst that pass 1 made (sweep_row with STAGE), never from the rows.
+template <typename T, bool ALIGNED, bool ZSET, bool STAGED = false>
 __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, const Seq &s, const T *trow,
                                            const T *drow, WeightParams wp, bool bonus, const RowStat &tot,
                                            const RowStat *parts, int stride, float u, int32_t *outn,
-                                           float *mass_out, const RowStat *stored = nullptr)
+                                           float *mass_out, const RowStat *stored = nullptr,
+                                           const uint4 *tst = nullptr, const uint4 *dst = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
@@ -1428,8 +1453,9 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
 #pragma unroll
             for (int u = 0; u < U2; ++u) {
                 const int c = s.c0 + (j0 + u) * kThreads + tid;
-                tv[u] = c < s.c1 ? load_chunk<T, ALIGNED>(trow, c, s.V) : neg_inf_chunk<T>();
-                dv[u] = (wp.residual && c < s.c1) ? load_chunk<T, ALIGNED>(drow, c, s.V) : neg_inf_chunk<T>();
+                tv[u] = c < s.c1 ? slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s) : neg_inf_chunk<T>();
+                dv[u] = (wp.residual && c < s.c1) ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s)
+                                                  : neg_inf_chunk<T>();
             }
 #pragma unroll
             for (int u = 0; u < U2; ++u) {
@@ -1476,7 +1502,8 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
             }
             __syncthreads();
         }
-        owner_search<T, ALIGNED, ZSET>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+        owner_search<T, ALIGNED, ZSET, STAGED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn, tst,
+                                                 dst);
         return;
     }
 
@@ -1499,7 +1526,8 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
     const unsigned long long theta = scaled_floor(u, S);  // pick: C_{j-1} <= theta < C_j
     if (S == 0 || !(P <= theta && theta < P + mine))
         return;  // another CTA owns the sample (S == 0 only for an all-zero row)
-    owner_search<T, ALIGNED, ZSET>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn);
+    owner_search<T, ALIGNED, ZSET, STAGED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn, tst,
+                                                 dst);
 }
 
 // Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n
@@ -1508,9 +1536,12 @@ __device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, con
 // rejection (max(0, p - q), or p without x_n for point-mass drafts), the bonus
 // row t_g otherwise.
 // stored: the row's pass-1 warp partials when pass 1 kept its chunk sums (the sampler).
-template <typename T, bool ALIGNED>
+// STAGED: tst and dst hold this CTA's slices of rows t_n and d_n (early exit
+// with rows in host memory), so pass 2 reads neither row again.
+template <typename T, bool ALIGNED, bool STAGED = false>
 __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
-                             int stride, const RowStat *stored = nullptr)
+                             int stride, const RowStat *stored = nullptr, const uint4 *tst = nullptr,
+                             const uint4 *dst = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int g = s.g, b = s.b;
@@ -1520,9 +1551,10 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
     const int xn = (residual && !s.drafts) ? sh.drafted[n] : -1;  // point mode only
     const WeightParams wp = weight_params(sh, s, n, residual, xn, W);
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
-    sample_row<T, ALIGNED, false>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
-                                  final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr,
-                                  residual ? nullptr : stored);
+    sample_row<T, ALIGNED, false, STAGED>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
+                                          final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr,
+                                          residual ? nullptr : stored, tst,
+                                          (residual && s.drafts) ? dst : tst);
 }
 
 // ===========================================================================
@@ -1599,10 +1631,15 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
 // "Speculative Decoding", ch.2), so a round reads n+1 target rows and
 // min(n+1, g) draft rows instead of g+1 and g.  The outputs are those of the
 // full sweep; diagnostics exist only for the rows read.
-template <typename T, bool ALIGNED, bool POINT>
+// STAGED (rows in page-locked host memory, read over the host link, where L2
+// keeps no copy): each position's slices also go to shared memory, after the
+// chunk sums, cap = ceil(num_chunks / C) chunks per row (t_i, then d_i), and
+// pass 2 takes the decided rows from there instead of the link.
+template <typename T, bool ALIGNED, bool POINT, bool STAGED = false>
 __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Params p)
 {
     __shared__ SharedState sh;
+    extern __shared__ __align__(16) unsigned char early_dyn[];
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -1624,6 +1661,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
     const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
     const int gmax = s.gmax;
+    const int cap = (p.num_chunks + C - 1) / C;
+    uint4 *stage = STAGED ? reinterpret_cast<uint4 *>(early_dyn + (size_t)p.scan_tiles * kThreads * 4) : nullptr;
     // every drafted id is checked, as in the full sweep (lane-parallel)
     if (wid == 0) {
         const bool tb = lane < g && !(p.tokens[(size_t)b * gmax + lane] >= 0 &&
@@ -1644,7 +1683,11 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
         // the decision's logits at x_i, loaded ahead of the rows
         const Gathered gt = tid == 0 ? gather_position<T>(p, s, i) : Gathered{-1, 0.0f, 0.0f, 0.0f};
         for (int slot = 0; slot < nslot; ++slot) {
-            const RowStat st = sweep_row<T, ALIGNED>(s, row_ptr<T>(p, s, slot ? g + 1 + i : i));
+            const T *row = row_ptr<T>(p, s, slot ? g + 1 + i : i);
+            // greedy rows need no pass 2: only sampled sequences keep a copy
+            const RowStat st = (STAGED && s.sampled)
+                                   ? sweep_row<T, ALIGNED, false, true>(s, row, nullptr, stage + (size_t)slot * cap)
+                                   : sweep_row<T, ALIGNED>(s, row);
             if (lane == 0)
                 sh.warp_part[slot][wid] = st;
         }
@@ -1744,7 +1787,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     }
     if (!s.sampled || bits)
         return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED>(p, sh, s, n, &sh.recv_pos[n & 1][0][0], 2);
+    stream_pass2<T, ALIGNED, STAGED>(p, sh, s, n, &sh.recv_pos[n & 1][0][0], 2, nullptr, stage,
+                                     STAGED ? stage + cap : nullptr);
 }
 
 // ===========================================================================
@@ -2257,7 +2301,8 @@ enum KernelKind {
     kKindTree = 9,           // candidate-tree walk, any alignment
     kKindWide8 = 10,         // full sweep, aligned, at most 8 chunks per thread and row, 2 CTAs/SM
     kKindSample = 11,        // the sampler (gamma_max = 0), aligned: pass 1 keeps the chunk sums
-    kKinds = 12
+    kKindEarlyStaged = 12,   // early exit, aligned, decided rows kept in shared memory (rows in host memory)
+    kKinds = 13
 };
 
 // The kernel of one variant, as the pointer the launch API takes (nullptr: no
@@ -2299,6 +2344,8 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
             return (const void *)spec_tree_kernel<T, false>;
     case kKindEarlyAligned:
         return (const void *)spec_verify_early_kernel<T, true, POINT>;
+    case kKindEarlyStaged:
+        return (const void *)spec_verify_early_kernel<T, true, POINT, true>;
     default:
         return (const void *)spec_verify_early_kernel<T, false, POINT>;
     }

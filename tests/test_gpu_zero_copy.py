@@ -84,6 +84,52 @@ def test_host_inputs_full_size_early_exit(sv):
 
 
 @gpu
+@pytest.mark.parametrize("cluster", [0, 2, 8, 16])
+def test_host_inputs_early_exit_cluster_sizes(sv, cluster):
+    """Early exit on host rows keeps the decided slices in shared memory where
+    they fit (clusters of 8 and 16, and the automatic size) and reads the rows
+    again where they do not (2 CTAs per sequence): the same bits either way."""
+    import torch
+
+    batch = workloads.make_config(3, B=12)
+    dev = sv.to_device(batch)
+    ref_t, ref_n = sv.verify(**dev)
+    host = _pinned(dev)
+    t, n = sv.verify(**host, kernel=sv.KERNEL_EARLY, cluster_size=cluster)
+    pt, pn = sv.verify(**{**host, "draft_logits": None}, kernel=sv.KERNEL_EARLY, cluster_size=cluster)
+    qt, qn = sv.verify(**{**dev, "draft_logits": None})
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(t.cpu().numpy(), ref_t.cpu().numpy())
+    np.testing.assert_array_equal(n.cpu().numpy(), ref_n.cpu().numpy())
+    np.testing.assert_array_equal(pt.cpu().numpy(), qt.cpu().numpy())
+    np.testing.assert_array_equal(pn.cpu().numpy(), qn.cpu().numpy())
+
+
+@gpu
+def test_host_inputs_early_exit_rows_too_wide_to_stage(sv, oracle_mod):
+    """float32 rows of 600000 ids (2.4 MB): two slices do not fit in shared
+    memory at any cluster size, so pass 2 reads the rows again."""
+    import torch
+
+    rng = np.random.default_rng(17)
+    B, g, V = 2, 3, 600_000
+    target = (rng.standard_normal((B, g + 1, V)) * 2).astype(np.float32)
+    draft = (target[:, :g] + rng.standard_normal((B, g, V)) * 0.5).astype(np.float32)
+    tokens = np.stack([np.argmax(draft[b], axis=1) for b in range(B)]).astype(np.int32)
+    batch = workloads.Batch(target, draft, tokens, np.full(B, g, np.int32),
+                            rng.random((B, g + 1)).astype(np.float32), np.array([1.0, 0.8], np.float32), "f32",
+                            "wide f32 rows")
+    dev = sv.to_device(batch)
+    ref = _verify(sv, dev, 2)
+    got = _verify(sv, _pinned(dev), 3)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+    rep = parity.compare(batch, got[0], got[1], oracle_mod.verify_batch(batch))
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
+    torch.cuda.synchronize()
+
+
+@gpu
 def test_host_inputs_debug_diagnostics_identical(sv):
     import torch
 
