@@ -1,10 +1,13 @@
 """Run one path of the library a few times on a fixed seeded workload, for
 profilers (ncu) and quick timing:
 
-    python -m speculative_decoding_verification_45_gb300.profile_case {verify,early,tree,sample,ngram} [--reps N]
+    python -m speculative_decoding_verification_45_gb300.profile_case \
+        {verify,early,tree,sample,ngram} [--reps N] [--host]
 
 verify / early : spec_verify (full sweep / row-ordered early exit) on the
-                 B=256, gamma=4, V=128256 bf16 workload
+                 B=256, gamma=4, V=128256 bf16 workload; with --host the
+                 inputs stay in page-locked host memory and the kernels read
+                 them over the host link (zero copy)
 tree           : spec_tree_verify, 32 sequences of 64-node Medusa-style trees
                  over V=128256 (half greedy, half T=1)
 sample         : spec_sample, 256 rows of V=128256 (target-only round)
@@ -26,12 +29,15 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("case", choices=["verify", "early", "tree", "sample", "ngram"])
     ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--host", action="store_true", help="verify/early: inputs in page-locked host memory")
     args = ap.parse_args(argv)
     sv.build()
     torch.cuda.set_device(0)
     batch = workloads.make_config(5)
     if args.case in ("verify", "early", "sample"):
         dev = sv.to_device(batch)
+        if args.host and args.case != "sample":
+            dev = {k: v.cpu().pin_memory() for k, v in dev.items()}
     if args.case == "verify":
         def call():
             sv.verify(**dev)
