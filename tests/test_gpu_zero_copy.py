@@ -130,16 +130,34 @@ def test_host_inputs_early_exit_rows_too_wide_to_stage(sv, oracle_mod):
 
 
 @gpu
-def test_host_inputs_debug_diagnostics_identical(sv):
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_host_inputs_debug_diagnostics_identical(sv, kernel):
+    """Diagnostics too: the staged early exit computes them from the same rows."""
     import torch
 
-    batch = workloads.make_config(3, B=8)
+    batch = workloads.make_config(4, B=12)
     dev = sv.to_device(batch)
-    a = sv.verify_debug(**dev)
-    b = sv.verify_debug(**_pinned(dev))
+    a = sv.verify_debug(**dev, kernel=kernel)
+    b = sv.verify_debug(**_pinned(dev), kernel=kernel)
     torch.cuda.synchronize()
     for k in a:
         np.testing.assert_array_equal(a[k].cpu().numpy(), b[k].cpu().numpy(), err_msg=k)
+
+
+@gpu
+@pytest.mark.parametrize("kind", ["mixed", "reject_first", "accept_all", "neg_inf"])
+def test_host_inputs_unaligned_rows(sv, oracle_mod, kind):
+    """V = 1023 bf16: rows are not 16-byte multiples, so the element-load path
+    runs (no staging); host rows give the device-resident bits."""
+    batch = workloads.edge_batch(kind, V=1023)
+    dev = sv.to_device(batch)
+    for kernel in (0, 3):
+        ref = _verify(sv, dev, kernel)
+        got = _verify(sv, _pinned(dev), kernel)
+        np.testing.assert_array_equal(got[0], ref[0])
+        np.testing.assert_array_equal(got[1], ref[1])
+    rep = parity.compare(batch, got[0], got[1], oracle_mod.verify_batch(batch))
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
 
 
 @gpu
