@@ -128,8 +128,13 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
                         int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,
                         spec_dtype dtype, uint32_t *status, void *stream);
 
-/* Launch options (tuning, A/B measurement and the early-exit variant; the
- * emitted tokens do not depend on them). */
+/* Launch options (tuning, A/B measurement and the early-exit variant).  They
+ * change no decision except one that lies within float32 rounding of its
+ * boundary: the normalisers are merged from per-CTA partials, so the split of a
+ * row (the cluster size) and the kernel variant move p-hat, q-hat and the CDF
+ * by about 1e-7 relative, and an accept test or a sampled pick that close to
+ * its boundary may come out differently.  Greedy (T == 0) results never
+ * change. */
 typedef struct spec_verify_options {
     int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1 to 16 */
     int kernel;       /* 0 = automatic (full sweep, register loads);
