@@ -85,7 +85,7 @@ def test_host_inputs_full_size_early_exit(sv):
 
 @gpu
 @pytest.mark.parametrize("cluster", [0, 2, 8, 16])
-def test_host_inputs_early_exit_cluster_sizes(sv, cluster):
+def test_host_inputs_early_exit_cluster_sizes(sv, oracle_mod, cluster):
     """Early exit on host rows keeps the decided slices in shared memory where
     they fit (clusters of 8 and 16, and the automatic size) and reads the rows
     again where they do not (2 CTAs per sequence): the same bits either way."""
@@ -93,16 +93,19 @@ def test_host_inputs_early_exit_cluster_sizes(sv, cluster):
 
     batch = workloads.make_config(3, B=12)
     dev = sv.to_device(batch)
-    ref_t, ref_n = sv.verify(**dev)
+    early = dict(kernel=sv.KERNEL_EARLY, cluster_size=cluster)
+    ref_t, ref_n = sv.verify(**dev, **early)
     host = _pinned(dev)
-    t, n = sv.verify(**host, kernel=sv.KERNEL_EARLY, cluster_size=cluster)
-    pt, pn = sv.verify(**{**host, "draft_logits": None}, kernel=sv.KERNEL_EARLY, cluster_size=cluster)
-    qt, qn = sv.verify(**{**dev, "draft_logits": None})
+    t, n = sv.verify(**host, **early)
+    pt, pn = sv.verify(**{**host, "draft_logits": None}, **early)
+    qt, qn = sv.verify(**{**dev, "draft_logits": None}, **early)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(t.cpu().numpy(), ref_t.cpu().numpy())
     np.testing.assert_array_equal(n.cpu().numpy(), ref_n.cpu().numpy())
     np.testing.assert_array_equal(pt.cpu().numpy(), qt.cpu().numpy())
     np.testing.assert_array_equal(pn.cpu().numpy(), qn.cpu().numpy())
+    rep = parity.compare(batch, t.cpu().numpy(), n.cpu().numpy(), oracle_mod.verify_batch(batch))
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
 
 
 @gpu
