@@ -240,6 +240,26 @@ int auto_cluster(int B, int num_chunks, int sms)
     return C;
 }
 
+// Automatic cluster size for one row per sequence (gamma_max = 0: the
+// sampler).  Every cluster then does the same work, and a few long CTAs that
+// are all resident at once beat a grid of several waves: the largest power of
+// two with B*C <= 2 * SMs (at most 8; 16 for one or two rows), but no smaller
+// than the size at which a slice's chunk sums fit in shared memory (pass 1
+// keeps them, so pass 2 reads no row again).  Measured on GB300, 20-call graphs:
+// B=128, V=128256 bf16: 20.2 us at 8 -> 15.9 at 2; B=1024: 111 -> 65 us;
+// B=256, V=32000: 17.8 -> 10.7 us.
+int sampler_cluster(int B, int num_chunks, int sms)
+{
+    int keep = 1;
+    while (keep < kMaxCluster && per_thread_chunks(num_chunks, keep) > kMaxScanTiles)
+        ++keep;
+    const int cap = B <= 2 ? 16 : 8;
+    int C = 1;
+    while (C < cap && (long long)B * C * 2 <= 2LL * sms)
+        C *= 2;
+    return C > keep ? C : keep;
+}
+
 struct Shape {
     int kind;
     int C;
@@ -250,7 +270,7 @@ struct Shape {
 // Picks the kernel and cluster size.  want_kind: -1 automatic, else a KernelKind.
 // point: point-mass proposals, which the ring kernel does not handle.
 spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_kind, int want_C, Shape *out,
-                          bool point = false)
+                          bool point = false, bool one_row = false)
 {
     int dev = 0, sms = 0;
     spec_status st = current_device(&dev);
@@ -279,7 +299,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     const int W = chunk_width(dt);
     const int num_chunks = (V + W - 1) / W;
     for (int i = 0; i < nk; ++i) {
-        int C = want_C > 0 ? want_C : auto_cluster(B, num_chunks, sms);
+        int C = want_C > 0 ? want_C : one_row ? sampler_cluster(B, num_chunks, sms) : auto_cluster(B, num_chunks, sms);
         for (;;) {
             if (cluster_launchable(dev, dt, kinds[i], C, point)) {
                 out->kind = kinds[i];
@@ -373,7 +393,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         want_kind = kKindEarly;
 
     Shape shp;
-    spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp, point);
+    spec_status st = resolve_shape(B, V, dtype, aligned, want_kind, want_C, &shp, point, gmax == 0);
     if (st != SPEC_OK)
         return st;
     const int nslot = point ? 1 : 2;  // rows a position reads: t_i, and d_i unless point-mass
@@ -436,7 +456,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     const long long slots = (long long)shp.sms * (shp.kind == kKindEarlyStaged                          ? 1
                                                   : (shp.kind == kKindRing || shp.kind == kKindWide8) ? 2
                                                                                                       : 4);
-    prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
+    // (one row per sequence: every cost is equal, so the order is the identity)
+    prm.ordered = (gmax > 0 && B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
@@ -636,7 +657,7 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
         return SPEC_ERR_INVALID_ARG;
     const bool aligned = ((size_t)V * (size_t)elem_size(dtype)) % 16 == 0;
     Shape shp;
-    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, -1, 0, &shp);
+    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, -1, 0, &shp, false, gamma_max == 0);
     if (st != SPEC_OK)
         return st;
     if (cluster_size)

@@ -26,7 +26,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("spec_verify", "spec_verify_debug", "spec_verify_ex", "spec_sample", "spec_ngram_propose",
-              "spec_tree_verify", "spec_verify_launch_shape", "spec_status_string"):
+              "spec_tree_verify", "spec_device_pointer", "spec_verify_launch_shape", "spec_status_string"):
         assert n in names
 
 
