@@ -260,6 +260,21 @@ int sampler_cluster(int B, int num_chunks, int sms)
     return C > keep ? C : keep;
 }
 
+// Automatic cluster size of a candidate-tree walk.  Each level of the walk is
+// one row read and one cluster exchange, so a walk is latency-bound, and a grid
+// resident in one wave (at most 4 CTAs per SM) beats a second wave as long as
+// each tree keeps at least 4 CTAs: the chain rule's size, halved while that
+// holds.  Measured on GB300, 20-call graphs, V = 128256: 128 trees of 16 or 32
+// nodes take 34.9 / 41.2 us at 8 and 30.3 / 32.9 us at 4; 256 trees stay at 4
+// (49.5 us, against 52.1 at 2); 8 to 64 trees stay at 8.
+int tree_cluster(int B, int num_chunks, int sms)
+{
+    int C = auto_cluster(B, num_chunks, sms);
+    while ((long long)B * C > 4LL * sms && C / 2 >= 4)
+        C /= 2;
+    return C;
+}
+
 struct Shape {
     int kind;
     int C;
@@ -299,7 +314,11 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     const int W = chunk_width(dt);
     const int num_chunks = (V + W - 1) / W;
     for (int i = 0; i < nk; ++i) {
-        int C = want_C > 0 ? want_C : one_row ? sampler_cluster(B, num_chunks, sms) : auto_cluster(B, num_chunks, sms);
+        const bool walk = kinds[i] == kKindTreeAligned || kinds[i] == kKindTree;
+        int C = want_C > 0 ? want_C
+                : walk     ? tree_cluster(B, num_chunks, sms)
+                : one_row  ? sampler_cluster(B, num_chunks, sms)
+                           : auto_cluster(B, num_chunks, sms);
         for (;;) {
             if (cluster_launchable(dev, dt, kinds[i], C, point)) {
                 out->kind = kinds[i];
