@@ -1,6 +1,7 @@
 /* A plain C caller of libspec_verify: builds a small greedy batch whose answer
  * is fixed by construction, runs spec_verify and spec_sample through the C ABI
- * (device memory from the CUDA runtime), and checks the outputs.  Exit code 0
+ * (device memory from the CUDA runtime, then the logits in mapped page-locked
+ * host memory through spec_device_pointer), and checks the outputs.  Exit code 0
  * on success; the test in test_gpu_c_abi.py compiles and runs it.
  *
  * Rows: logit_j = -|j - peak| in float32, so the argmax of a row is its peak
@@ -9,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "spec_verify.h"
 
@@ -103,6 +105,32 @@ int main(void)
         return 4;
     for (int b = 0; b < B; ++b)
         bad |= n[b] != peaks[b][0];
+    /* zero copy: the logits in mapped page-locked host memory, read by the
+     * early-exit kernel over the host link; same answer as from device memory */
+    void *ht, *hd;
+    const void *at = NULL, *ad = NULL;
+    if (check(cudaHostAlloc(&ht, sizeof target, cudaHostAllocMapped), "host alloc") ||
+        check(cudaHostAlloc(&hd, sizeof draft, cudaHostAllocMapped), "host alloc"))
+        return 2;
+    memcpy(ht, target, sizeof target);
+    memcpy(hd, draft, sizeof draft);
+    bad |= spec_device_pointer(ht, &at) != SPEC_OK || spec_device_pointer(hd, &ad) != SPEC_OK;
+    bad |= spec_device_pointer(target, &at) != SPEC_ERR_INVALID_ARG;  /* pageable: refused, at unchanged */
+    spec_verify_options opt = {0, 3, NULL, NULL};
+    st = spec_verify_ex(at, ad, (const int32_t *)dtok, (const int32_t *)dnum, (const float *)du, (const float *)dT,
+                        (int32_t *)dout, (int32_t *)dn, B, G, V, SPEC_F32, NULL, NULL, &opt);
+    if (st != SPEC_OK) {
+        fprintf(stderr, "spec_verify_ex (host rows): %s\n", spec_status_string(st));
+        return 3;
+    }
+    int out2[B][G + 1], n2[B];
+    if (check(cudaMemcpy(out2, dout, sizeof out2, cudaMemcpyDeviceToHost), "copy") ||
+        check(cudaMemcpy(n2, dn, sizeof n2, cudaMemcpyDeviceToHost), "copy"))
+        return 4;
+    bad |= memcmp(out, out2, sizeof out) != 0 || memcmp(n2, want_n, sizeof n2) != 0;
+    printf("host rows: %s\n", memcmp(out, out2, sizeof out) ? "differ" : "same tokens");
+    cudaFreeHost(ht);
+    cudaFreeHost(hd);
     /* a rejected argument: B < 0 */
     bad |= spec_verify(dt, dd, (const int32_t *)dtok, (const int32_t *)dnum, (const float *)du, (const float *)dT,
                        (int32_t *)dout, (int32_t *)dn, -1, G, V, SPEC_F32, NULL, NULL) != SPEC_ERR_INVALID_ARG;
