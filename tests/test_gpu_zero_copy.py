@@ -109,6 +109,33 @@ def test_host_inputs_early_exit_cluster_sizes(sv, oracle_mod, cluster):
 
 
 @gpu
+@pytest.mark.parametrize("point", [False, True])
+def test_host_inputs_early_exit_float32_staged(sv, oracle_mod, point):
+    """float32 rows of 128256 ids: two slices fit in shared memory from
+    clusters of 8 up, so the host rows are staged; same bits as device rows at
+    the same launch shape, and the oracle's answer outside its tolerance."""
+    import torch
+
+    src = workloads.make_config(4, B=12)  # ragged drafts, mixed temperatures
+    f32 = lambda a: workloads.logits_as_f64(a, src.dtype).astype(np.float32)  # noqa: E731
+    batch = workloads.Batch(f32(src.target), f32(src.draft), src.tokens.copy(), src.num_draft.copy(),
+                            src.uniforms.copy(), src.temperature.copy(), "f32", "config 4 rows in float32")
+    dev = sv.to_device(batch)
+    if point:
+        dev["draft_logits"] = None
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in dev.items()}
+    early = dict(kernel=sv.KERNEL_EARLY, cluster_size=8)
+    ref = sv.verify(**dev, **early)
+    got = sv.verify(**host, **early)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
+    np.testing.assert_array_equal(got[1].cpu().numpy(), ref[1].cpu().numpy())
+    if not point:
+        rep = parity.compare(batch, got[0].cpu().numpy(), got[1].cpu().numpy(), oracle_mod.verify_batch(batch))
+        assert rep.mismatches_far == 0, rep.far_detail[:3]
+
+
+@gpu
 def test_host_inputs_early_exit_rows_too_wide_to_stage(sv, oracle_mod):
     """float32 rows of 600000 ids (2.4 MB): two slices do not fit in shared
     memory at any cluster size, so pass 2 reads the rows again."""
