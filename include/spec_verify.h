@@ -281,6 +281,15 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
  * SPEC_ERR_CUDA if the runtime query fails.  Enqueues nothing. */
 spec_status spec_device_pointer(const void *ptr, const void **device_ptr);
 
+/* Self-test of the kernels' bounded waits (diagnostic).  Launches one small
+ * kernel that waits on a shared-memory mbarrier which nothing completes, with
+ * the limit every wait inside the kernels has (2^18 tries or 0.2 s of wall
+ * time, whichever comes first); the wait gives up, SPEC_STATUS_TIMEOUT is
+ * OR-ed into *status (a device word, 4-byte aligned, zeroed by the caller) and
+ * the kernel returns, leaving the context usable.  Asynchronous on 'stream';
+ * returns SPEC_ERR_INVALID_ARG for a NULL or misaligned status. */
+spec_status spec_selftest_bounded_wait(uint32_t *status, void *stream);
+
 /* Static description of a status code. */
 const char *spec_status_string(spec_status s);
 

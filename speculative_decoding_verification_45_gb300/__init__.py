@@ -343,6 +343,19 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
     return out_tokens, out_num
 
 
+def selftest_bounded_wait(stream=None) -> int:
+    """Run spec_selftest_bounded_wait and return the status bits it set
+    (STATUS_TIMEOUT when a wait that cannot finish gave up as it should)."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = _native.load().spec_selftest_bounded_wait(_ptr(status), _stream_handle(stream, dev))
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_selftest_bounded_wait")
+    return int(status.cpu().item())
+
+
 def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):
     """(cluster size, CTAs, threads per CTA) the library picks for these sizes on the current device."""
     lib = _native.load()

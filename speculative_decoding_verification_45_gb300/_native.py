@@ -103,6 +103,8 @@ def load() -> ctypes.CDLL:
         lib.spec_tree_verify.restype = i32
         lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
         lib.spec_verify_launch_shape.restype = i32
+        lib.spec_selftest_bounded_wait.argtypes = [vp, vp]
+        lib.spec_selftest_bounded_wait.restype = i32
         lib.spec_device_pointer.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
         lib.spec_device_pointer.restype = i32
         lib.spec_status_string.argtypes = [i32]

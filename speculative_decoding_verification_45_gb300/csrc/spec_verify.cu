@@ -89,6 +89,21 @@ __global__ void __launch_bounds__(kNgramThreads)
     }
 }
 
+// Self-test of the bounded wait the bulk-copy ring kernel uses: one thread
+// waits on an mbarrier that nothing arrives at, so its first phase never
+// completes; the wait gives up after its limit and the status bit is set, and
+// the kernel returns like any other.
+__global__ void spec_wait_selftest_kernel(uint32_t *status)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(&bar, 0))
+            atomicOr(status, SPEC_STATUS_TIMEOUT);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -708,6 +723,17 @@ spec_status spec_device_pointer(const void *ptr, const void **device_ptr)
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged && a.type != cudaMemoryTypeHost)
         return SPEC_ERR_INVALID_ARG;
     *device_ptr = a.devicePointer;
+    return SPEC_OK;
+}
+
+spec_status spec_selftest_bounded_wait(uint32_t *status, void *stream)
+{
+    NvtxScope nvtx("spec_selftest_bounded_wait");
+    if (!status || ((uintptr_t)status & 3u))
+        return SPEC_ERR_INVALID_ARG;
+    spec_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status);
+    if (cudaGetLastError() != cudaSuccess)
+        return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 

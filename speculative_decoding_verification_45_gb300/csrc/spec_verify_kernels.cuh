@@ -87,6 +87,7 @@ constexpr int kChunksPerThread = kSegChunks / kThreads;
 constexpr int kStages = 8;  // ring depth: 64 KB
 constexpr int kRingBytes = kStages * kSegChunks * 16;
 constexpr int kMaxSpin = 1 << 18;  // tries of one mbarrier wait before giving up
+constexpr unsigned long long kMaxWaitNs = 200000000ull;  // ... or this much wall time (0.2 s)
 constexpr int kMaxScanTiles = 48;  // register kernel: at most 48 * kThreads chunk sums (48 KB) in shared memory
 constexpr int kMaxOrdered = 1024;  // longest-first scheduling for B up to this
 constexpr float kLog2e = 1.4426950408889634f;
@@ -613,10 +614,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, u
                  "r"(bytes)
                  : "memory");
 }
-// Waits for the phase of the given parity to complete; false after kMaxSpin tries.
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase of the given parity to complete; false after kMaxSpin
+// tries or kMaxWaitNs of wall time, whichever comes first (one try may suspend
+// the thread for a hardware-defined time, so the tries alone bound the count,
+// not the duration).
 __device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity)
 {
     const uint32_t a = smem_addr(bar);
+    const unsigned long long t0 = global_ns();
     for (int i = 0; i < kMaxSpin; ++i) {
         uint32_t done;
         asm volatile(
@@ -628,6 +639,8 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t pari
             : "memory");
         if (done)
             return true;
+        if ((i & 63) == 63 && global_ns() - t0 > kMaxWaitNs)
+            break;
     }
     return false;
 }

@@ -35,6 +35,12 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_selftest_rejects_a_missing_status_word(lib):
+    # checked on the host before anything is launched
+    assert lib.spec_selftest_bounded_wait(None, None) == 1
+    assert lib.spec_selftest_bounded_wait(ctypes.c_void_p(6), None) == 1  # misaligned
+
+
 def test_status_strings(lib):
     for code in range(4):
         assert lib.spec_status_string(code)
