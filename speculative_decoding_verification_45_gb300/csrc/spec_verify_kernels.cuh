@@ -45,7 +45,10 @@
 //                             are not 16-byte aligned; variants that read
 //                             several rows per round trip for narrow slices.
 //   spec_verify_early_kernel  positions in order, no row after the first
-//                             rejection read.
+//                             rejection read; its staged form (rows in
+//                             page-locked host memory, which L2 does not
+//                             cache) keeps each position's slices in shared
+//                             memory so pass 2 reads nothing over the link.
 //   spec_tree_kernel          a walk down a tree of candidates, one row per level.
 //   spec_verify_ring_kernel   16-byte-aligned rows only.  A producer warp streams
 //                             the CTA's slices through an 8-stage shared-memory
@@ -56,8 +59,8 @@
 //                             warps per SM.  Kept for A/B runs.
 // No kernel uses global scratch memory, atomics on the data path (only the
 // optional status word and counters) or unbounded waits: mbarrier waits give up
-// after a fixed number of tries and report SPEC_STATUS_TIMEOUT, and the only
-// other waits are hardware barriers that every thread reaches.
+// after a fixed number of tries or 0.2 s and report SPEC_STATUS_TIMEOUT, and
+// the only other waits are hardware barriers that every thread reaches.
 
 #pragma once
 
