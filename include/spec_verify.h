@@ -166,7 +166,9 @@ typedef struct spec_verify_options {
  *                            sequence (residual mass, or ~1 for a bonus row)
  *   seq_status [B]           SPEC_STATUS_* bits of each sequence (0 = valid)
  * The diagnostic rows are computed for every i <= g, also after the cut (with
- * the full-sweep kernels).  options: as for spec_verify_ex (NULL = automatic). */
+ * the full-sweep kernels).  A sequence with a data problem (seq_status != 0)
+ * may carry partial diagnostics: the rows swept before the problem was found.
+ * options: as for spec_verify_ex (NULL = automatic). */
 spec_status spec_verify_debug(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                               const int32_t *num_draft, const float *uniforms, const float *temperature,
                               int32_t *out_tokens, int32_t *out_num_accepted, int B, int gamma_max, int V,

@@ -365,6 +365,54 @@ def edge_batch(kind: str, V: int = 1023, gamma: int = 3, B: int = 8, seed: int =
     return Batch(target, draft, tokens, num_draft, uniforms, temp, dtype, f"edge-{kind}")
 
 
+def random_batch(seed: int) -> Batch:
+    """A seeded batch of random shape and content, for broad parity sweeps.
+
+    B in [1, 48]; gamma_max in [0, 9] with num_draft ragged in [0, gamma_max];
+    V tiny, mid-sized or up to 70000 (odd sizes included); bf16 (60 %) or
+    float32; a temperature per sequence from {0, 0.05, 0.3, 0.7, 1, 1.7, 4};
+    target rows N(0, s^2) with s in [0.5, 6] (plus the Zipf shift of the large
+    workloads half the time), draft rows the target plus N(0, sigma^2); drafted
+    ids drawn from the draft rows as the proposer stand-in does; uniforms
+    U[0, 1).  About one sequence in twenty carries a data problem (a drafted id
+    outside [0, V), a negative or NaN temperature, or num_draft above
+    gamma_max), which must give -1 tokens and a status bit.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B = int(rng.integers(1, 49))
+    gmax = int(rng.integers(0, 10))
+    pick = int(rng.integers(0, 5))
+    V = [int(rng.integers(2, 64)), int(rng.integers(64, 5000)), int(rng.integers(5000, 70000)), 32000, 4097][pick]
+    dtype = BF16 if rng.random() < 0.6 else F32
+    target, draft, tokens = _empty(B, gmax, V, dtype)
+    num_draft = rng.integers(0, gmax + 1, size=B).astype(np.int32)
+    temp = rng.choice(np.array([0.0, 0.05, 0.3, 0.7, 1.0, 1.7, 4.0], np.float32), size=B).astype(np.float32)
+    scale = float(rng.uniform(0.5, 6.0))
+    zipf = rng.random() < 0.5
+    for b in range(B):
+        g = int(num_draft[b])
+        t = rng.normal(0.0, scale, size=(g + 1, V))
+        if zipf:
+            t = t + _zipf_shift(rng, V)
+        d = t[:g] + rng.normal(0.0, float(rng.uniform(0.1, 2.5)), size=(g, V))
+        target[b, : g + 1] = _round(t, dtype)
+        draft[b, :g] = _round(d, dtype)
+        for i in range(g):
+            tokens[b, i] = _draft_token(rng, draft[b, i], dtype, float(temp[b]))
+    for b in range(B):
+        if rng.random() >= 0.05:
+            continue
+        kind = int(rng.integers(0, 3))
+        if kind == 0 and num_draft[b] > 0:
+            tokens[b, int(rng.integers(0, num_draft[b]))] = int(rng.choice([-1, V, V + 7]))
+        elif kind == 1:
+            temp[b] = np.float32(rng.choice([-1.0, np.nan]))
+        else:
+            num_draft[b] = gmax + 1
+    uniforms = rng.random((B, gmax + 1), dtype=np.float32)
+    return Batch(target, draft, tokens, num_draft, uniforms, temp, dtype, f"random{seed}")
+
+
 def describe(batch: Batch) -> str:
     return (f"{batch.name}: B={batch.B} gmax={batch.gmax} V={batch.V} dtype={batch.dtype} "
             f"logit bytes={batch.algorithmic_bytes()} (nominal {batch.nominal_bytes()})")

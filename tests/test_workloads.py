@@ -71,3 +71,33 @@ def test_greedy_drafts_are_draft_argmax_and_sampled_drafts_follow_q():
     w /= w.sum()
     freq = np.bincount(draws, minlength=3) / draws.size
     assert np.all(np.abs(freq - w) < 5 * np.sqrt(w * (1 - w) / draws.size))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_batch_is_seeded_and_poisons_padding(seed):
+    a, b = workloads.random_batch(seed), workloads.random_batch(seed)
+    for name in ("target", "draft", "tokens", "num_draft", "uniforms"):
+        np.testing.assert_array_equal(getattr(a, name), getattr(b, name))
+    np.testing.assert_array_equal(a.temperature.view(np.int32), b.temperature.view(np.int32))  # NaN-safe
+    assert a.target.shape == (a.B, a.gmax + 1, a.V) and a.draft.shape == (a.B, a.gmax, a.V)
+    assert 1 <= a.B <= 48 and 0 <= a.gmax <= 9 and a.V >= 2
+    t = workloads.logits_as_f64(a.target, a.dtype)
+    d = workloads.logits_as_f64(a.draft, a.dtype)
+    for i in range(a.B):
+        g = int(a.num_draft[i])
+        if g > a.gmax:  # a planted bad count: nothing else is promised for the row
+            continue
+        assert np.all(np.isposinf(t[i, g + 1:])) and np.all(np.isposinf(d[i, g:]))
+        assert np.all(a.tokens[i, g:] == -1)
+        assert np.all(np.isfinite(t[i, : g + 1])) and np.all(np.isfinite(d[i, :g]))
+    assert np.all((a.uniforms >= 0) & (a.uniforms < 1))
+
+
+def test_random_batches_cover_the_sweep():
+    batches = [workloads.random_batch(s) for s in range(48)]
+    assert {b.dtype for b in batches} == {"bf16", "f32"}
+    assert any(b.gmax == 0 for b in batches) and any(b.gmax >= 8 for b in batches)
+    assert any(b.V < 64 for b in batches) and any(b.V > 5000 for b in batches)
+    assert any(b.V % 8 for b in batches) and any(b.V % 8 == 0 for b in batches)
+    temps = np.concatenate([b.temperature for b in batches])
+    assert np.any(temps == 0) and np.any(temps > 0) and (np.any(np.isnan(temps)) or np.any(temps < 0))
