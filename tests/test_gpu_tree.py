@@ -40,12 +40,35 @@ def run_tree(sv, tb, **kw):
     ("medusa", 24, 64, 32000, "bf16"), ("random", 24, 40, 4099, "bf16"), ("star", 16, 33, 1024, "f32"),
     ("chain", 24, 17, 5000, "f32"), ("medusa", 8, 64, 128256, "bf16"), ("random", 8, 96, 151936, "bf16")])
 def test_tree_parity(sv, oracle_mod, shape, B, N, V, dtype):
-    tb = workloads.tree_batch(B, N, V, dtype=dtype, seed=hash((shape, N, V)) % 1000, shape=shape)
+    seed = (sum(map(ord, shape)) * 7919 + N * 31 + V) % 1000  # fixed per case (str hashes vary by process)
+    tb = workloads.tree_batch(B, N, V, dtype=dtype, seed=seed, shape=shape)
     ref = oracle_mod.tree_verify_batch(tb)
     toks, num, path, st = run_tree(sv, tb)
     rep = parity.compare_tree(tb, toks, num, path, ref)
     assert rep.mismatches_far == 0, (str(rep), rep.far_detail[:3])
     assert st == 0
+
+
+@gpu
+@pytest.mark.parametrize("seed", range(24))
+def test_tree_random_sweep(sv, oracle_mod, seed):
+    """Trees of random shape, size, vocabulary, dtype and temperature mix, at a
+    cluster size from 1 to 16 (or the automatic one), against the oracle."""
+    rng = np.random.default_rng(5000 + seed)
+    shape = ("chain", "star", "random", "medusa")[seed % 4]
+    B = int(rng.integers(1, 25))
+    N = int(rng.integers(1, 97))
+    V = int(rng.choice([int(rng.integers(2, 200)), int(rng.integers(200, 9000)), 32000, 4099]))
+    dtype = "bf16" if rng.random() < 0.6 else "f32"
+    temps = tuple(float(t) for t in rng.choice([0.0, 0.3, 0.7, 1.0, 2.0], size=int(rng.integers(1, 4))))
+    C = (0, 1, 2, 3, 4, 8, 16)[seed % 7]
+    tb = workloads.tree_batch(B, N, V, dtype=dtype, seed=6000 + seed, shape=shape, temps=temps,
+                              ragged=bool(rng.random() < 0.7), zipf=bool(rng.random() < 0.5))
+    ref = oracle_mod.tree_verify_batch(tb)
+    toks, num, path, st = run_tree(sv, tb, cluster_size=C)
+    rep = parity.compare_tree(tb, toks, num, path, ref)
+    assert rep.mismatches_far == 0, (shape, B, N, V, dtype, temps, C, str(rep), rep.far_detail[:3])
+    assert st == int(np.bitwise_or.reduce(ref.seq_status))
 
 
 @gpu
