@@ -320,7 +320,7 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
     if context.dim() != 2 or context.dtype != torch.int32:
         raise ValueError("context must be an int32 [B, S] tensor")
     dev = _device_of(context, context_len, out_tokens, out_num)
-    B, S = context.shape
+    B = context.shape[0]
     if context.stride(1) != 1:
         raise ValueError("context rows must be contiguous")
     if context.device.type == "cpu" and not context.is_pinned():
