@@ -78,7 +78,7 @@ def _check_input(t, name, dtype, shape, device):
     host tensor that the kernels read over the host link (zero copy)."""
     if t.device.type == "cpu":
         _check(t, name, dtype, shape, t.device)
-        if not t.is_pinned():
+        if t.numel() and not t.is_pinned():  # an empty tensor is never read
             raise ValueError(f"{name}: a host tensor must be page-locked (pin_memory()) for the GPU to read it")
     else:
         _check(t, name, dtype, shape, device)

@@ -39,3 +39,8 @@ def test_target_logits_must_be_three_dimensional():
 def test_counter_tensors_are_checked():
     with pytest.raises(ValueError, match="64-bit"):
         sv._counter_ptr(torch.zeros(3, dtype=torch.int32), 3, "counters")
+
+
+def test_empty_host_input_needs_no_page_locking():
+    # gamma_max = 0 gives [B, 0, V] draft logits: nothing to read, nothing to pin
+    sv._check_input(torch.zeros(3, 0, 5), "draft_logits", torch.float32, (3, 0, 5), CUDA0)

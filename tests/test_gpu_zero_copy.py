@@ -255,3 +255,27 @@ def test_spec_device_pointer(sv):
     rc = lib.spec_device_pointer(ctypes.c_void_p(pageable.ctypes.data), ctypes.byref(out))
     assert rc == sv.SPEC_ERR_INVALID_ARG and out.value == 7
     assert lib.spec_device_pointer(None, ctypes.byref(out)) == sv.SPEC_ERR_INVALID_ARG
+
+
+@gpu
+@pytest.mark.parametrize("seed", range(100, 116))
+def test_host_inputs_random_batches(sv, oracle_mod, seed):
+    """Random shapes, dtypes, temperatures and planted data problems
+    (workloads.random_batch) with every input on the host: the device-resident
+    bits at the same launch shape, and the oracle's answer."""
+    import torch
+
+    batch = workloads.random_batch(seed)
+    kernel = (0, 3)[seed % 2]
+    cluster = (0, 2, 4, 8)[(seed // 2) % 4]
+    dev = sv.to_device(batch)
+    st_d = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st_h = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = sv.verify(**dev, kernel=kernel, cluster_size=cluster, status=st_d)
+    got = sv.verify(**_pinned(dev), kernel=kernel, cluster_size=cluster, status=st_h)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
+    np.testing.assert_array_equal(got[1].cpu().numpy(), ref[1].cpu().numpy())
+    assert int(st_h.item()) == int(st_d.item())
+    rep = parity.compare(batch, got[0].cpu().numpy(), got[1].cpu().numpy(), oracle_mod.verify_batch(batch))
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
