@@ -96,3 +96,28 @@ def test_sample_greedy_ties_and_invalid(sv):
     batch = _as_round(rows, np.full(4, 0.5, np.float32), temps, "f32")
     got = _run(sv, batch)
     assert list(got) == [1, 0, 1, -1]
+
+
+@gpu
+@pytest.mark.parametrize("seed", range(200, 212))
+def test_sample_random_rows(sv, oracle_mod, seed):
+    """spec_sample on the first rows of random batches (workloads.random_batch:
+    tiny to 70000 ids, bf16 or float32, mixed and invalid temperatures) at a
+    cluster size from 1 to 16 or the automatic one, against the oracle."""
+    import torch
+
+    src = workloads.random_batch(seed)
+    rng = np.random.default_rng(seed)
+    temps = src.temperature.copy()
+    batch = _as_round(src.target[:, 0], rng.random(src.B).astype(np.float32), temps, src.dtype)
+    ref = oracle_mod.verify_batch(batch)
+    dev = sv.to_device(batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = sv.sample(dev["target_logits"][:, 0].contiguous(), dev["uniforms"][:, 0].contiguous(),
+                    dev["temperature"], status=status, cluster_size=(0, 1, 2, 4, 8, 16)[seed % 6])
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    out = np.stack([got, np.zeros_like(got)], 1)[:, :1]
+    rep = parity.compare(batch, out, np.zeros(batch.B, np.int32), ref)
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
+    assert int(status.item()) == int(np.bitwise_or.reduce(ref.seq_status))
