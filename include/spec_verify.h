@@ -61,7 +61,9 @@
  * spec_device_pointer returns for it.  The kernels then read those bytes over
  * the host link while they run ("zero copy"): no staging copy is made, and the
  * early-exit kernel (options.kernel 3) moves only the rows it needs across
- * the link.  The caller keeps such memory unchanged until the stream has
+ * the link, each once where two row slices fit in shared memory (it keeps the
+ * decided rows there for the final sample; host memory is not cached in L2).
+ * The caller keeps such memory unchanged until the stream has
  * passed the call.  Everything the kernels write (outputs, status, counters,
  * diagnostics) must be device memory.  The bulk-copy ring (options.kernel 1)
  * takes device-memory logits only (else SPEC_ERR_UNSUPPORTED).
