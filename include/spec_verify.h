@@ -26,7 +26,13 @@
  *           One more token y is drawn by inverse CDF with u = uniforms[b, gamma_max]
  *           from max(0, p_n - q_n) (n < g) or from p_g (n == g): y is the
  *           smallest id j with u * S < C_j, C_j the running sum of the weights
- *           in id order and S their total.
+ *           in id order and S their total.  The weights are integers on a
+ *           2^-60 grid, each within about 2^-36 of its exact value where it
+ *           matters (ids whose weight is within a factor 2^20 of the row's
+ *           largest; float32 for the rest), so every sum is exact and y
+ *           differs from the float64 definition only when u lies within
+ *           ~1e-10 of a boundary C_j / S (rows whose |logit| * log2(e) / T
+ *           passes 2^21 keep float32 weights throughout).
  *   T == 0: greedy; a_i = argmax of the raw target logits of row i (lowest id
  *           on ties); position i accepts iff x_i == a_i; y = a_n.  No draft row
  *           and no uniform is read.
@@ -63,10 +69,11 @@
  * early-exit kernel (options.kernel 3) moves only the rows it needs across
  * the link, each once where two row slices fit in shared memory (it keeps the
  * decided rows there for the final sample; host memory is not cached in L2).
- * The caller keeps such memory unchanged until the stream has
- * passed the call.  Everything the kernels write (outputs, status, counters,
- * diagnostics) must be device memory.  The bulk-copy ring (options.kernel 1)
- * takes device-memory logits only (else SPEC_ERR_UNSUPPORTED).
+ * The kernels read such memory after the call has returned, so the caller
+ * keeps it allocated and unchanged until the stream has passed the call (for
+ * example until an event recorded after the call completes).  Everything the
+ * kernels write (outputs, status, counters, diagnostics) must be device
+ * memory.
  *
  * Ownership and execution.  The caller owns every buffer.  The call enqueues
  * one kernel on 'stream' (a cudaStream_t; NULL = legacy default stream) and
@@ -80,10 +87,9 @@
  * position it uses, or a sampled row it uses whose logits have no finite
  * softmax normaliser (all -inf, any +inf or NaN) gets out_tokens[b, :] = -1
  * and out_num_accepted[b] = 0, and its SPEC_STATUS_* bit is OR-ed into
- * *status when status is not NULL (the caller zeroes it).  Every wait inside
- * the kernel is bounded; one that runs out sets SPEC_STATUS_TIMEOUT instead of
- * hanging.  NaN logits in
- * greedy rows give unspecified (in-range) tokens.
+ * *status when status is not NULL (the caller zeroes it).  The kernels wait only
+ * at hardware barriers that every thread of the CTA or cluster reaches.  NaN
+ * logits in greedy rows give unspecified (in-range) tokens.
  *
  * Limits: 0 <= B <= SPEC_MAX_BATCH (B == 0 is a no-op), 0 <= gamma_max <=
  * SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_VOCAB.
@@ -116,8 +122,9 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_TEMPERATURE 2u
 #define SPEC_STATUS_BAD_NUM_DRAFT 4u
 #define SPEC_STATUS_BAD_LOGITS 8u
-/* An internal wait of the kernel on its own asynchronous copies exceeded its
- * iteration limit (not expected on a healthy GPU): the sequence gets -1 tokens. */
+/* With a workspace (spec_verify_options.workspace): a CTA waiting for a
+ * pass-2 task to appear gave up after its wall-time limit (0.2 s; not
+ * expected on a healthy GPU).  Draws may then be missing. */
 #define SPEC_STATUS_TIMEOUT 16u
 /* spec_tree_verify: a node's parent is not an earlier node. */
 #define SPEC_STATUS_BAD_TREE 32u
@@ -131,17 +138,16 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
                         spec_dtype dtype, uint32_t *status, void *stream);
 
 /* Launch options (tuning, A/B measurement and the early-exit variant).  They
- * change no decision except one that lies within float32 rounding of its
- * boundary: the normalisers are merged from per-CTA partials, so the split of a
- * row (the cluster size) and the kernel variant move p-hat, q-hat and the CDF
- * by about 1e-7 relative, and an accept test or a sampled pick that close to
- * its boundary may come out differently.  Greedy (T == 0) results never
- * change. */
+ * change no decision except one that lies very close to its boundary: the
+ * normalisers are merged from per-CTA partials, so the split of a row (the
+ * cluster size) and the kernel variant move p-hat and q-hat by about 1e-7
+ * relative, and an accept test that close to its threshold (or a final draw
+ * within ~1e-10 of a CDF boundary) may come out differently.  Greedy (T == 0)
+ * results never change. */
 typedef struct spec_verify_options {
     int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1 to 16 */
     int kernel;       /* 0 = automatic (full sweep, register loads);
-                         1 = full sweep through a bulk-copy ring (16-byte aligned rows only,
-                             else SPEC_ERR_UNSUPPORTED);
+                         1 = not a kernel (SPEC_ERR_INVALID_ARG);
                          2 = full sweep, register loads;
                          3 = row-ordered early exit: position i's rows are read, reduced
                              and tested before position i+1's, and no row after the first
@@ -156,6 +162,15 @@ typedef struct spec_verify_options {
     uint64_t *accept_hist; /* optional device array [SPEC_MAX_GAMMA + 1] (8-byte aligned): += 1 at
                               index n (accepted count; min(n, SPEC_MAX_GAMMA) for trees) for each
                               verified sequence, the distribution behind the mean.  NULL: none. */
+    void *workspace;       /* optional device scratch, 256-byte aligned, of at least
+                              workspace_bytes >= spec_workspace_size(B, V, dtype, tree) bytes.
+                              With it the final draws run as a second kernel on the same stream
+                              that spreads every sequence's pass 2 over the whole GPU, instead of
+                              on each sequence's own CTAs after its pass 1 (results identical;
+                              faster when many sequences sample).  Its first bytes are zeroed
+                              on the stream before the first kernel; calls that share one
+                              workspace must be ordered on one stream.  NULL: one kernel. */
+    uint64_t workspace_bytes;
 } spec_verify_options;
 
 /* Same round, plus optional float32 diagnostics for tests (any may be NULL):
@@ -194,7 +209,7 @@ spec_status spec_verify_ex(const void *target_logits, const void *draft_logits, 
  *   logits [B, V] dtype; uniforms [B] float32 in [0, 1); temperature [B];
  *   out_tokens [B] int32 (-1 for a sequence with an invalid temperature or a
  *   sampled row without a finite normaliser; its bit goes to *status).
- * options: as for spec_verify_ex (kernel 1, the ring, is not available here).
+ * options: as for spec_verify_ex.
  * Same ownership, stream and error rules as spec_verify. */
 spec_status spec_sample(const void *logits, const float *uniforms, const float *temperature, int32_t *out_tokens,
                         int B, int V, spec_dtype dtype, uint32_t *status, void *stream,
@@ -277,6 +292,14 @@ spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, c
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
                                      int *num_ctas, int *threads_per_cta);
 
+/* Bytes of workspace (spec_verify_options.workspace) a call with B sequences
+ * (trees: tree = 1) and vocabulary V needs on the current device: per
+ * sequence one pass-2 record and its slice sums (about 2.5 KB at V = 128256;
+ * 1 KB more per tree for its rejected ids).  Touches the device (its SM count)
+ * but enqueues nothing.  SPEC_ERR_INVALID_ARG for a NULL bytes or sizes out of
+ * range. */
+spec_status spec_workspace_size(int B, int V, spec_dtype dtype, int tree, uint64_t *bytes);
+
 /* The address the kernels use for ptr: ptr itself for this device's memory,
  * the device alias for page-locked host memory mapped into the device's
  * address space (with unified addressing, the same value).  Returns
@@ -284,15 +307,6 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
  * unregistered host memory, another device's memory or a NULL argument, and
  * SPEC_ERR_CUDA if the runtime query fails.  Enqueues nothing. */
 spec_status spec_device_pointer(const void *ptr, const void **device_ptr);
-
-/* Self-test of the kernels' bounded waits (diagnostic).  Launches one small
- * kernel that waits on a shared-memory mbarrier which nothing completes, with
- * the limit every wait inside the kernels has (2^18 tries or 0.2 s of wall
- * time, whichever comes first); the wait gives up, SPEC_STATUS_TIMEOUT is
- * OR-ed into *status (a device word, 4-byte aligned, zeroed by the caller) and
- * the kernel returns, leaving the context usable.  Asynchronous on 'stream';
- * returns SPEC_ERR_INVALID_ARG for a NULL or misaligned status. */
-spec_status spec_selftest_bounded_wait(uint32_t *status, void *stream);
 
 /* Static description of a status code. */
 const char *spec_status_string(spec_status s);

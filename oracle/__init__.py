@@ -70,6 +70,9 @@ def _load():
             lib.oracle_tree_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int]
             lib.oracle_tree_verify.restype = ctypes.c_int
+            lib.oracle_pick_many.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                             ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
+            lib.oracle_pick_many.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -185,3 +188,31 @@ def tree_verify_batch(tb, nthreads=None) -> TreeResult:
     """Tree oracle on a workloads.TreeBatch-like object."""
     return tree_verify(tb.target, tb.dtype, tb.parent, tb.tokens, tb.num_nodes, tb.uniforms, tb.temperature,
                        nthreads=nthreads)
+
+
+PICK_P = 0          # p of the row (a bonus row, or the sampler's draw)
+PICK_RESIDUAL = 1   # max(0, p - q), q from a draft row
+PICK_POINT = 2      # p without the point-mass draft xn
+
+
+def pick_many(target_row, dtype, temperature, uniforms, mode=PICK_P, draft_row=None, xn=-1):
+    """The final draw of oracle_verify for many uniforms on one decided row.
+
+    target_row / draft_row: V logits (float32, or uint16 bfloat16 bits);
+    uniforms: float32 [n].  Returns (picks int32 [n], margins float64 [n], S):
+    the smallest j with u*S < C_j for each u, the distance of u to the nearer
+    CDF boundary of that pick, and the total weight S."""
+    lib = _load()
+    code = {"f32": F32, "bf16": BF16}[dtype]
+    elem = np.float32 if code == F32 else np.uint16
+    t = np.ascontiguousarray(target_row, dtype=elem).reshape(-1)
+    d = None if draft_row is None else np.ascontiguousarray(draft_row, dtype=elem).reshape(-1)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(-1)
+    picks = np.empty(u.size, np.int32)
+    margins = np.empty(u.size, np.float64)
+    mass = np.zeros(1, np.float64)
+    rc = lib.oracle_pick_many(_ptr(t), _ptr(d), code, t.size, float(temperature), int(mode), int(xn), _ptr(u),
+                              u.size, _ptr(picks), _ptr(margins), _ptr(mass))
+    if rc != 0:
+        raise ValueError("oracle_pick_many rejected its arguments")
+    return picks, margins, float(mass[0])

@@ -195,10 +195,88 @@ static void fill_diagnostics(const oracle_args *a, int b, int g, double T)
     }
 }
 
-/* Sample from the weights w_j of one decided row by inverse CDF with the
- * uniform u ([P1] ch.3 step 3, [P3] step 3).  'rejected' selects the residual
- * max(0, p - q) of row n, otherwise the target distribution of row n (the
- * bonus row when every draft was accepted). */
+/* Weights w_j of one decided row ([P1] ch.3 step 3, [P3] step 3): with
+ * 'rejected', the residual max(0, p - q) of the row (q from the draft row at
+ * doff, or the point mass at xn when there is no draft array); otherwise p of
+ * the target row (the bonus row when every draft was accepted).  A residual
+ * whose total is not above 1e-300 (unreachable in exact arithmetic) falls back
+ * to p of the same row.  Returns the total S, summed in index order. */
+static double decided_row_weights(const void *target, const void *draft, int dtype, size_t toff, size_t doff, int V,
+                                  double T, softmax_norm st, softmax_norm sd, int rejected, int xn, double *w)
+{
+    double S = 0.0;
+    for (int j = 0; j < V; ++j) {
+        double pj = row_prob(target, dtype, toff, j, T, st);
+        double wj = pj;
+        if (rejected) {
+            double qj = draft ? row_prob(draft, dtype, doff, j, T, sd) : (j == xn ? 1.0 : 0.0);
+            wj = pj - qj > 0.0 ? pj - qj : 0.0;
+        }
+        w[j] = wj;
+        S += wj;
+    }
+    if (!(S > 1e-300)) {
+        S = 0.0;
+        for (int j = 0; j < V; ++j) {
+            w[j] = row_prob(target, dtype, toff, j, T, st);
+            S += w[j];
+        }
+    }
+    return S;
+}
+
+/* Inverse CDF with uniform u: the smallest j with u*S < C_j, C_j the running
+ * sum of w in index order (C[j] when the caller has them, else summed here);
+ * if rounding leaves no such j, the last j with w_j > 0.  margin: the distance
+ * of u to the nearer boundary C_{j-1}/S, C_j/S of the pick (0 in the fallback). */
+static int pick_by_cdf(const double *w, const double *C, int V, double S, double u, double *margin)
+{
+    double thr = u * S;
+    int pick = -1;
+    double lo_c = 0.0, hi_c = 0.0;
+    if (C) {
+        /* C is nondecreasing: bisect for the smallest j with thr < C[j] */
+        int lo = 0, hi = V;
+        while (lo < hi) {
+            int mid = lo + (hi - lo) / 2;
+            if (thr < C[mid])
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        if (lo < V) {
+            pick = lo;
+            lo_c = lo > 0 ? C[lo - 1] : 0.0;
+            hi_c = C[lo];
+        }
+    } else {
+        double acc = 0.0;
+        for (int j = 0; j < V; ++j) {
+            double prev = acc;
+            acc += w[j];
+            if (thr < acc) {
+                pick = j;
+                lo_c = prev;
+                hi_c = acc;
+                break;
+            }
+        }
+    }
+    if (pick < 0) {
+        for (int j = V - 1; j >= 0; --j)
+            if (w[j] > 0.0) {
+                pick = j;
+                break;
+            }
+        *margin = 0.0;
+        return pick;
+    }
+    double m0 = u - lo_c / S, m1 = hi_c / S - u;
+    *margin = m0 < m1 ? m0 : m1;
+    return pick;
+}
+
+/* Sample one decided row of sequence b: its weights, then the inverse CDF. */
 static int sample_decided_row(const oracle_args *a, int b, int n, int rejected, double T, double u,
                               softmax_norm st, softmax_norm sd, int xn, double *mass_out, double *margin_out)
 {
@@ -208,48 +286,9 @@ static int sample_decided_row(const oracle_args *a, int b, int n, int rejected, 
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
     if (!w)
         return -1;
-    double S = 0.0;
-    for (int j = 0; j < V; ++j) {
-        double pj = row_prob(a->target, a->dtype, toff, j, T, st);
-        double wj = pj;
-        if (rejected) {
-            double qj = a->draft ? row_prob(a->draft, a->dtype, doff, j, T, sd) : (j == xn ? 1.0 : 0.0);
-            wj = pj - qj > 0.0 ? pj - qj : 0.0;
-        }
-        w[j] = wj;
-        S += wj;
-    }
-    if (!(S > 1e-300)) {
-        /* degenerate residual: fall back to p of the same row */
-        S = 0.0;
-        for (int j = 0; j < V; ++j) {
-            w[j] = row_prob(a->target, a->dtype, toff, j, T, st);
-            S += w[j];
-        }
-    }
+    double S = decided_row_weights(a->target, a->draft, a->dtype, toff, doff, V, T, st, sd, rejected, xn, w);
     *mass_out = S;
-    double thr = u * S;
-    double C = 0.0, Cprev = 0.0;
-    int pick = -1;
-    for (int j = 0; j < V; ++j) {
-        Cprev = C;
-        C += w[j];
-        if (thr < C) {
-            pick = j;
-            break;
-        }
-    }
-    if (pick < 0) {
-        for (int j = V - 1; j >= 0; --j)
-            if (w[j] > 0.0) {
-                pick = j;
-                break;
-            }
-        *margin_out = 0.0;
-    } else {
-        double lo = u - Cprev / S, hi = C / S - u;
-        *margin_out = lo < hi ? lo : hi;
-    }
+    int pick = pick_by_cdf(w, NULL, V, S, u, margin_out);
     free(w);
     return pick;
 }
@@ -705,5 +744,57 @@ int oracle_tree_verify(const void *target, int dtype, const int32_t *parent, con
         pthread_join(th[t], NULL);
     free(th);
     free(sl);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Many draws from one decided row (test support): the same weights and
+ * inverse CDF as the final sample of oracle_verify, for n uniforms at once.
+ *   target_row, draft_row: V logits each (draft_row may be NULL)
+ *   mode 0: p of the target row (a bonus row; the sampler's draw)
+ *   mode 1: residual max(0, p - q), q = softmax(draft_row / T)
+ *   mode 2: residual for a point-mass proposal at xn (p without xn)
+ *   us[n]: uniforms in [0, 1); picks[n], margins[n] (margins may be NULL)
+ *   mass (may be NULL): the total S of the weights
+ * Returns 0, or -1 on a bad argument or a row with no finite normaliser.
+ * ---------------------------------------------------------------------- */
+int oracle_pick_many(const void *target_row, const void *draft_row, int dtype, int V, float temperature, int mode,
+                     int xn, const float *us, int n, int32_t *picks, double *margins, double *mass)
+{
+    if (!target_row || V < 1 || n < 0 || (n > 0 && (!us || !picks)) || mode < 0 || mode > 2 ||
+        (mode == 1 && !draft_row) || (dtype != ORACLE_F32 && dtype != ORACLE_BF16) ||
+        !(temperature > 0.0f) || !temperature_is_valid(temperature))
+        return -1;
+    const double T = (double)temperature;
+    softmax_norm st = row_softmax_norm(target_row, dtype, 0, V, T);
+    softmax_norm sd = {0.0, 1.0};
+    if (mode == 1)
+        sd = row_softmax_norm(draft_row, dtype, 0, V, T);
+    if (!norm_is_valid(st) || !norm_is_valid(sd))
+        return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    double *C = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!w || !C) {
+        free(w);
+        free(C);
+        return -1;
+    }
+    double S = decided_row_weights(target_row, mode == 1 ? draft_row : NULL, dtype, 0, 0, V, T, st, sd, mode != 0,
+                                   mode == 2 ? xn : -1, w);
+    double acc = 0.0;
+    for (int j = 0; j < V; ++j) {
+        acc += w[j];
+        C[j] = acc;
+    }
+    if (mass)
+        *mass = S;
+    for (int i = 0; i < n; ++i) {
+        double mg = 0.0;
+        picks[i] = pick_by_cdf(w, C, V, S, (double)us[i], &mg);
+        if (margins)
+            margins[i] = mg;
+    }
+    free(w);
+    free(C);
     return 0;
 }

@@ -10,7 +10,12 @@ CPU fallback: if the library is missing, every call raises.
 
 Inputs are CUDA tensors, or page-locked host tensors (``pin_memory()``) that
 the kernels read over the host link without a staging copy; outputs are CUDA
-tensors.  See include/spec_verify.h for the operation, layouts and error behaviour.
+tensors.  A page-locked input is read while the kernel runs, after the call has
+returned: the binding keeps a reference to it until the launch stream has
+passed the call (an event recorded after the launch), so that torch's pinned
+memory cache cannot hand the block to another tensor earlier.  The caller must
+not change its contents before then.  See include/spec_verify.h for the
+operation, layouts and error behaviour.
 """
 from __future__ import annotations
 
@@ -30,7 +35,6 @@ STATUS_BAD_TOKEN = 1
 STATUS_BAD_TEMPERATURE = 2
 STATUS_BAD_NUM_DRAFT = 4
 STATUS_BAD_LOGITS = 8
-STATUS_TIMEOUT = 16
 STATUS_BAD_TREE = 32
 
 MAX_GAMMA = 16
@@ -131,6 +135,86 @@ def _prepare(target, draft, tokens, num_draft, uniforms, temperature, out_tokens
     return B, gmax, V, code, out_tokens, out_num
 
 
+def _status_ptr(t, device):
+    """Device pointer of the optional status word: an int32 CUDA tensor on
+    ``device`` with at least one element (the kernels OR bits into element 0)."""
+    import torch
+
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or t.device != device or t.numel() < 1 or not t.is_contiguous():
+        raise ValueError(f"status must be a contiguous int32 tensor on {device} with at least one element")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# Page-locked host inputs of launches the stream may not have passed yet:
+# (event recorded after the launch, the tensors).  A reference is dropped once
+# its event has completed, so torch's pinned-memory cache cannot reuse a block
+# that a running kernel still reads.
+_held = []
+
+
+def _hold_host_inputs(tensors, stream, device):
+    import torch
+
+    global _held
+    host = [t for t in tensors if t is not None and not t.is_cuda and t.numel()]
+    if not host and not _held:
+        return
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    with torch.cuda.stream(s):
+        if torch.cuda.is_current_stream_capturing():
+            # a captured launch reads its inputs at every replay: the caller
+            # keeps them for as long as the graph is replayed
+            return
+    _held = [(ev, ts) for ev, ts in _held if not ev.query()]
+    if not host:
+        return
+    ev = torch.cuda.Event()
+    ev.record(s)
+    _held.append((ev, host))
+
+
+_ws_sizes = {}
+
+
+def workspace_size(B: int, V: int, dtype_code: int, tree: bool = False) -> int:
+    """Bytes of the optional pass-2 workspace (spec_workspace_size) on the current device."""
+    import torch
+
+    key = (torch.cuda.current_device(), B, V, dtype_code, bool(tree))
+    n = _ws_sizes.get(key)
+    if n is None:
+        out = ctypes.c_uint64()
+        rc = _native.load().spec_workspace_size(B, V, dtype_code, int(bool(tree)), ctypes.byref(out))
+        if rc != SPEC_OK:
+            raise SpecVerifyError(rc, "spec_workspace_size")
+        n = _ws_sizes[key] = int(out.value)
+    return n
+
+
+def _workspace(workspace, B, V, code, tree, stream, device):
+    """(pointer, bytes, tensor) of the pass-2 workspace: a caller's uint8 CUDA
+    tensor, a fresh one from torch's allocator on the launch stream (True), or
+    none (False/None: pass 2 inside the verification kernel)."""
+    import torch
+
+    if workspace is None or workspace is False or B == 0:
+        return None, 0, None
+    need = workspace_size(B, V, code, tree)
+    if workspace is True:
+        s = torch.cuda.current_stream(device) if stream is None else stream
+        with torch.cuda.stream(s):
+            workspace = torch.empty(need + 256, dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or workspace.device != device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
+    ptr = workspace.data_ptr()
+    off = (-ptr) % 256
+    if workspace.numel() * workspace.element_size() - off < need:
+        raise ValueError(f"workspace needs {need} bytes (256-byte aligned)")
+    return ctypes.c_void_p(ptr + off), need, workspace
+
+
 def _counter_ptr(t, n, name):
     """Device pointer of an optional int64 CUDA tensor of at least n elements."""
     if t is None:
@@ -148,48 +232,57 @@ def _stream_handle(stream, device):
 
 
 KERNEL_AUTO = 0
-KERNEL_RING = 1      # full sweep through a bulk-copy ring (16-byte aligned rows)
 KERNEL_REGISTER = 2  # full sweep, register loads
 KERNEL_EARLY = 3     # row-ordered early exit: no row after the first rejection is read
 
 
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
            out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO,
-           counters=None, accept_hist=None):
+           counters=None, accept_hist=None, workspace=False):
     """One verification round on the GPU (asynchronous on ``stream``).
 
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
     ``status``: optional int32 CUDA tensor of one element receiving the
     per-sequence data-problem bits (STATUS_*), OR-ed; zero it first.
     ``cluster_size``: 0 = automatic, else 1 to 16 CTAs per sequence.
-    ``kernel``: KERNEL_AUTO, KERNEL_RING, KERNEL_REGISTER or KERNEL_EARLY.
+    ``kernel``: KERNEL_AUTO, KERNEL_REGISTER or KERNEL_EARLY.
     ``draft_logits=None``: point-mass proposals (a deterministic proposer such
     as ngram_propose): accept iff u < p(x), a rejection samples p without x.
     Inputs may be page-locked host tensors (zero copy; with KERNEL_EARLY only
-    the rows up to the first rejection cross the host link).
+    the rows up to the first rejection cross the host link); they must stay
+    unchanged until the stream has passed the call (the binding keeps them
+    alive that long).
     ``counters``: optional uint64 (int64) CUDA tensor [3], += drafted ids,
     accepted ids, verified sequences.  ``accept_hist``: optional int64 CUDA
     tensor [MAX_GAMMA + 1], += 1 at each verified sequence's accepted count.
+    ``workspace``: False (default) samples each sequence's final token on its
+    own CTAs; True takes a workspace from torch's allocator on the launch
+    stream (or pass a uint8 CUDA tensor of at least workspace_size() + 256
+    bytes), with which every CTA that has finished its own sequence runs
+    slices of the others' final draws (same results).
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
     lib = _native.load()
     args = [_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens), _in_ptr(num_draft),
             _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code,
-            _ptr(status), _stream_handle(stream, out_tokens.device)]
-    if cluster_size or kernel or counters is not None or accept_hist is not None:
+            _status_ptr(status, out_tokens.device), _stream_handle(stream, out_tokens.device)]
+    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, out_tokens.device)
+    if cluster_size or kernel or counters is not None or accept_hist is not None or ws is not None:
         opts = _native.Options(int(cluster_size), int(kernel), _counter_ptr(counters, 3, "counters"),
-                               _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
+                               _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"), ws_ptr, ws_bytes)
         rc = lib.spec_verify_ex(*args, ctypes.byref(opts))
     else:
         rc = lib.spec_verify(*args)
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify")
+    _hold_host_inputs((target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature), stream,
+                      out_tokens.device)
     return out_tokens, out_num_accepted
 
 
 def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, stream=None,
-                 cluster_size: int = 0, kernel: int = KERNEL_AUTO):
+                 cluster_size: int = 0, kernel: int = KERNEL_AUTO, workspace=False):
     """verify() plus the float32 diagnostics of spec_verify_debug (a dict of tensors)."""
     import torch
 
@@ -207,15 +300,18 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
         "status": torch.zeros((1,), dtype=torch.int32, device=dev),
     }
     lib = _native.load()
+    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, dev)
     rc = lib.spec_verify_debug(_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens),
                                _in_ptr(num_draft), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens),
                                _ptr(out_num), B, gmax, V,
                                code, _ptr(d["status"]), _stream_handle(stream, dev), _ptr(d["p_hat"]),
                                _ptr(d["q_hat"]), _ptr(d["logz_t"]), _ptr(d["logz_d"]), _ptr(d["resid_mass"]),
                                _ptr(d["seq_status"]),
-                               ctypes.byref(_native.Options(int(cluster_size), int(kernel))))
+                               ctypes.byref(_native.Options(int(cluster_size), int(kernel), None, None, ws_ptr,
+                                                            ws_bytes)))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_debug")
+    _hold_host_inputs((target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature), stream, dev)
     d["out_tokens"] = out_tokens
     d["out_num_accepted"] = out_num
     return d
@@ -223,7 +319,7 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
 
 def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens=None,
                 out_num_accepted=None, out_path=None, status=None, stream=None, cluster_size: int = 0,
-                counters=None, accept_hist=None):
+                counters=None, accept_hist=None, workspace=False):
     """One candidate-tree round on the GPU (spec_tree_verify; asynchronous on ``stream``).
 
     target_logits [B, N, V] (row k: the target after the path to node k);
@@ -253,14 +349,16 @@ def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature,
     _check(out_tokens, "out_tokens", torch.int32, (B, N), dev)
     _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
     _check(out_path, "out_path", torch.int32, (B, N), dev)
+    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, True, stream, dev)
     opts = _native.Options(int(cluster_size), 0, _counter_ptr(counters, 3, "counters"),
-                           _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
+                           _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"), ws_ptr, ws_bytes)
     lib = _native.load()
     rc = lib.spec_tree_verify(_in_ptr(target_logits), _in_ptr(parent), _in_ptr(tokens), _in_ptr(num_nodes),
                               _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,
-                              code, _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
+                              code, _status_ptr(status, dev), _stream_handle(stream, dev), ctypes.byref(opts))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_tree_verify")
+    _hold_host_inputs((target_logits, parent, tokens, num_nodes, uniforms, temperature), stream, dev)
     return out_tokens, out_num_accepted, out_path
 
 
@@ -284,7 +382,7 @@ def tree_to_device(tb, device="cuda"):
 
 
 def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=None, cluster_size: int = 0,
-           kernel: int = KERNEL_AUTO):
+           kernel: int = KERNEL_AUTO, workspace=False):
     """One token per row: y_b ~ softmax(logits[b] / T_b) by inverse CDF with
     uniforms[b], or argmax when T_b == 0 (spec_sample).  Draft-side sampling of
     a proposer, or target-only decoding.  Returns out_tokens [B] int32."""
@@ -302,11 +400,13 @@ def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=N
         out_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
     _check(out_tokens, "out_tokens", torch.int32, (B,), dev)
     lib = _native.load()
-    opts = _native.Options(int(cluster_size), int(kernel))
+    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, dev)
+    opts = _native.Options(int(cluster_size), int(kernel), None, None, ws_ptr, ws_bytes)
     rc = lib.spec_sample(_in_ptr(logits), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), B, V, code,
-                         _ptr(status), _stream_handle(stream, dev), ctypes.byref(opts))
+                         _status_ptr(status, dev), _stream_handle(stream, dev), ctypes.byref(opts))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_sample")
+    _hold_host_inputs((logits, uniforms, temperature), stream, dev)
     return out_tokens
 
 
@@ -340,20 +440,8 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
                                 _stream_handle(stream, dev))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_ngram_propose")
+    _hold_host_inputs((context, context_len), stream, dev)
     return out_tokens, out_num
-
-
-def selftest_bounded_wait(stream=None) -> int:
-    """Run spec_selftest_bounded_wait and return the status bits it set
-    (STATUS_TIMEOUT when a wait that cannot finish gave up as it should)."""
-    import torch
-
-    dev = torch.device("cuda", torch.cuda.current_device())
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    rc = _native.load().spec_selftest_bounded_wait(_ptr(status), _stream_handle(stream, dev))
-    if rc != SPEC_OK:
-        raise SpecVerifyError(rc, "spec_selftest_bounded_wait")
-    return int(status.cpu().item())
 
 
 def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):

@@ -89,25 +89,10 @@ __global__ void __launch_bounds__(kNgramThreads)
     }
 }
 
-// Self-test of the bounded wait the bulk-copy ring kernel uses: one thread
-// waits on an mbarrier that nothing arrives at, so its first phase never
-// completes; the wait gives up after its limit and the status bit is set, and
-// the kernel returns like any other.
-__global__ void spec_wait_selftest_kernel(uint32_t *status)
-{
-    __shared__ __align__(8) unsigned long long bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (!mbar_wait(&bar, 0))
-            atomicOr(status, SPEC_STATUS_TIMEOUT);
-    }
-}
-
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// point: point-mass proposals (the ring kernel has no such variant).
+// point: point-mass proposals.
 const void *kernel_for(spec_dtype dt, int kind, bool point)
 {
     if (dt == SPEC_BF16)
@@ -115,16 +100,12 @@ const void *kernel_for(spec_dtype dt, int kind, bool point)
     return point ? specv::kernel_f32_point(kind) : specv::kernel_f32(kind);
 }
 
-int kernel_threads(int kind) { return kind == kKindRing ? kTmaThreads : kThreads; }
-// Dynamic shared memory of the staged early-exit kernel at most: its chunk sums
-// and its copies of the decided rows' slices (one CTA per SM).
+// Dynamic shared memory of the staged early-exit kernel at most: pass 2's
+// staging area and its copies of the decided rows' slices (one CTA per SM).
 constexpr int kStagedDynMax = 200 * 1024;
-// Largest dynamic shared memory a kernel kind is launched with: the ring, the
-// staged early exit, or the register kernels' chunk sums.
-int kernel_dyn_smem(int kind)
-{
-    return kind == kKindRing ? kRingBytes : kind == kKindEarlyStaged ? kStagedDynMax : kMaxScanTiles * kThreads * 4;
-}
+// Largest dynamic shared memory a kernel kind is launched with: the staged
+// early exit, or pass 2's staging area and queue.
+int kernel_dyn_smem(int kind) { return kind == kKindEarlyStaged ? kStagedDynMax : kWorkerSmemBytes; }
 int variant_slot(spec_dtype dt, int kind, bool point)
 {
     return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
@@ -166,7 +147,7 @@ spec_status device_sm_count(int dev, int *out)
 }
 
 // Applies the kernel attributes once per device: dynamic shared memory above
-// the 48 KB default (ring kernel) and clusters of 16 CTAs.
+// the 48 KB default (staged early exit) and clusters of 16 CTAs.
 bool prepare_kernel(int dev, spec_dtype dt, int kind, bool point)
 {
     const int slot = variant_slot(dt, kind, point);
@@ -185,12 +166,12 @@ bool prepare_kernel(int dev, spec_dtype dt, int kind, bool point)
     return st == 1;
 }
 
-cudaLaunchConfig_t launch_config(int kind, unsigned grid, int C, size_t dyn_smem, cudaStream_t stream,
+cudaLaunchConfig_t launch_config(unsigned grid, int C, size_t dyn_smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3((unsigned)kernel_threads(kind));
+    cfg.blockDim = dim3((unsigned)kThreads);
     cfg.dynamicSmemBytes = dyn_smem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -211,7 +192,7 @@ bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
         state = 2;
         if (prepare_kernel(dev, dt, kind, point)) {
             cudaLaunchAttribute attr[1];
-            cudaLaunchConfig_t cfg = launch_config(kind, (unsigned)C * 4u, C, (size_t)kernel_dyn_smem(kind), 0, attr);
+            cudaLaunchConfig_t cfg = launch_config((unsigned)C * 4u, C, (size_t)kernel_dyn_smem(kind), 0, attr);
             int clusters = 0;
             const cudaError_t e =
                 cudaOccupancyMaxActiveClusters(&clusters, kernel_for(dt, kind, point), &cfg);
@@ -258,21 +239,16 @@ int auto_cluster(int B, int num_chunks, int sms)
 // Automatic cluster size for one row per sequence (gamma_max = 0: the
 // sampler).  Every cluster then does the same work, and a few long CTAs that
 // are all resident at once beat a grid of several waves: the largest power of
-// two with B*C <= 2 * SMs (at most 8; 16 for one or two rows), but no smaller
-// than the size at which a slice's chunk sums fit in shared memory (pass 1
-// keeps them, so pass 2 reads no row again).  Measured on GB300, 20-call graphs:
-// B=128, V=128256 bf16: 20.2 us at 8 -> 15.9 at 2; B=1024: 111 -> 65 us;
-// B=256, V=32000: 17.8 -> 10.7 us.
-int sampler_cluster(int B, int num_chunks, int sms)
+// two with B*C <= 2 * SMs (at most 8; 16 for one or two rows).  Measured on
+// GB300, 20-call graphs: B=128, V=128256 bf16: 20.2 us at 8 -> 15.9 at 2;
+// B=1024: 111 -> 65 us; B=256, V=32000: 17.8 -> 10.7 us.
+int sampler_cluster(int B, int sms)
 {
-    int keep = 1;
-    while (keep < kMaxCluster && per_thread_chunks(num_chunks, keep) > kMaxScanTiles)
-        ++keep;
     const int cap = B <= 2 ? 16 : 8;
     int C = 1;
     while (C < cap && (long long)B * C * 2 <= 2LL * sms)
         C *= 2;
-    return C > keep ? C : keep;
+    return C;
 }
 
 // Automatic cluster size of a candidate-tree walk.  Each level of the walk is
@@ -298,7 +274,7 @@ struct Shape {
 
 
 // Picks the kernel and cluster size.  want_kind: -1 automatic, else a KernelKind.
-// point: point-mass proposals, which the ring kernel does not handle.
+// point: point-mass proposals.
 spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_kind, int want_C, Shape *out,
                           bool point = false, bool one_row = false)
 {
@@ -309,22 +285,14 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
     st = device_sm_count(dev, &sms);
     if (st != SPEC_OK)
         return st;
-    int kinds[2];
+    int kinds[1];
     int nk = 0;
     if (want_kind >= 0) {
-        if (!aligned && (want_kind == kKindRing || want_kind == kKindScalarAligned || want_kind == kKindEarlyAligned))
-            return SPEC_ERR_UNSUPPORTED;
-        if (point && want_kind == kKindRing)
+        if (!aligned && (want_kind == kKindScalarAligned || want_kind == kKindEarlyAligned))
             return SPEC_ERR_UNSUPPORTED;
         kinds[nk++] = want_kind;
-    } else if (aligned) {
-        // Register loads: on GB300 its 32 resident reducing warps per SM beat the
-        // ring kernel's 16 (the reduction is issue-bound, not load-bound).
-        kinds[nk++] = kKindScalarAligned;
-        if (!point)
-            kinds[nk++] = kKindRing;
     } else {
-        kinds[nk++] = kKindScalar;
+        kinds[nk++] = aligned ? kKindScalarAligned : kKindScalar;
     }
     const int W = chunk_width(dt);
     const int num_chunks = (V + W - 1) / W;
@@ -332,7 +300,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
         const bool walk = kinds[i] == kKindTreeAligned || kinds[i] == kKindTree;
         int C = want_C > 0 ? want_C
                 : walk     ? tree_cluster(B, num_chunks, sms)
-                : one_row  ? sampler_cluster(B, num_chunks, sms)
+                : one_row  ? sampler_cluster(B, sms)
                            : auto_cluster(B, num_chunks, sms);
         for (;;) {
             if (cluster_launchable(dev, dt, kinds[i], C, point)) {
@@ -362,9 +330,35 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// True when p lies in device (or managed) memory.  The bulk-copy ring reads
-// its rows with cp.async.bulk, which is given device memory only; the other
-// kernels read with ordinary loads and also take page-locked host memory.
+// Slices per decided row for the pass-2 tasks: the smallest power of two (at
+// most 32) with B * S2 >= 8 * SMs tasks, keeping at least 256 chunks per slice.
+int pass2_slices(int B, int num_chunks, int sms)
+{
+    int S2 = 1;
+    while (S2 < 32 && (long long)B * S2 < 8LL * sms && num_chunks / (S2 * 2) >= kThreads)
+        S2 *= 2;
+    return S2;
+}
+
+// Checks a caller's workspace for B sequences and zeroes its counters on the
+// stream; on success *S2 is the slices per row of the second launch.
+spec_status prepare_workspace(const spec_verify_options *opt, int B, int num_chunks, bool tree, int sms,
+                              cudaStream_t stream, int *S2)
+{
+    *S2 = pass2_slices(B, num_chunks, sms);
+    const WsLayout L = ws_layout(B, *S2, tree);
+    if (((uintptr_t)opt->workspace & 255u) || opt->workspace_bytes < (uint64_t)L.total)
+        return SPEC_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(opt->workspace, 0, ws_zeroed(B), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    return SPEC_OK;
+}
+
+// True when p lies in device (or managed) memory; the kernels also read
+// page-locked host memory mapped into the device's address space, with
+// ordinary loads.
 bool device_memory(const void *p)
 {
     cudaPointerAttributes a;
@@ -390,12 +384,9 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         want_C = opt->cluster_size;
         if (want_C < 0 || want_C > kMaxCluster)
             return SPEC_ERR_INVALID_ARG;
-        if (opt->kernel < 0 || opt->kernel > 3)
+        if (opt->kernel < 0 || opt->kernel > 3 || opt->kernel == 1)
             return SPEC_ERR_INVALID_ARG;
-        want_kind = opt->kernel == 1   ? kKindRing
-                    : opt->kernel == 2 ? kKindScalarAligned
-                    : opt->kernel == 3 ? kKindEarlyAligned
-                                       : -1;
+        want_kind = opt->kernel == 2 ? kKindScalarAligned : opt->kernel == 3 ? kKindEarlyAligned : -1;
     }
     if (B == 0)
         return SPEC_OK;
@@ -417,10 +408,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
     const bool point = gmax > 0 && !draft;
-    const bool host_rows = (want_kind == kKindRing || (want_kind == kKindEarlyAligned && aligned)) &&
+    const bool host_rows = want_kind == kKindEarlyAligned && aligned &&
                            (!device_memory(target) || (draft && !device_memory(draft)));
-    if (want_kind == kKindRing && host_rows)
-        return SPEC_ERR_UNSUPPORTED;
     if (!aligned && want_kind == kKindScalarAligned)
         want_kind = kKindScalar;  // register loads work at any alignment
     if (!aligned && want_kind == kKindEarlyAligned)
@@ -442,8 +431,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
                 if (want_C > 0 && C != want_C)
                     break;
                 const long long cap = (chunks + C - 1) / C;
-                const long long tiles = (cap + kThreads - 1) / kThreads;
-                const long long need = (tiles <= kMaxScanTiles ? tiles * kThreads * 4 : 0) + nslot * cap * 16;
+                const long long need = kP2SmemBytes + nslot * cap * 16;
                 if (need <= kStagedDynMax && cluster_launchable(dev, dtype, kKindEarlyStaged, C, point)) {
                     shp.kind = kKindEarlyStaged;
                     shp.C = C;
@@ -452,15 +440,6 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             }
         }
     }
-    if (gmax == 0 && !point && shp.kind == kKindScalarAligned) {  // the sampler: pass 1 keeps the chunk sums
-        const int chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
-        const int slice_tiles = ((chunks + shp.C - 1) / shp.C + kThreads - 1) / kThreads;
-        int dev = 0;
-        if (slice_tiles <= kMaxScanTiles && current_device(&dev) == SPEC_OK &&
-            cluster_launchable(dev, dtype, kKindSample, shp.C, false))
-            shp.kind = kKindSample;
-    }
-
     Params prm;
     prm.target = target;
     prm.draft = draft;
@@ -482,27 +461,35 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     prm.V = V;
     prm.num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
     const int slice = (prm.num_chunks + shp.C - 1) / shp.C;
-    const int tiles = (slice + kThreads - 1) / kThreads;
-    prm.scan_tiles = (shp.kind != kKindRing && tiles <= kMaxScanTiles) ? tiles : 0;
     // Longest-first order matters only when clusters wait for a free slot: a
-    // grid that is resident at once (at most 4 CTAs per SM; 2 for the ring
-    // kernel) skips it and its prologue.
-    const long long slots = (long long)shp.sms * (shp.kind == kKindEarlyStaged                          ? 1
-                                                  : (shp.kind == kKindRing || shp.kind == kKindWide8) ? 2
-                                                                                                      : 4);
+    // grid that is resident at once (at most 4 CTAs per SM; 2 for the
+    // two-rows-per-trip variant, 1 for the staged early exit) skips it and its
+    // prologue.
+    const long long slots = (long long)shp.sms * (shp.kind == kKindEarlyStaged ? 1 : shp.kind == kKindWide8 ? 2 : 4);
     // (one row per sequence: every cost is equal, so the order is the identity)
     prm.ordered = (gmax > 0 && B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
     prm.out_path = nullptr;
-    size_t dyn = shp.kind == kKindRing ? (size_t)kRingBytes : (size_t)prm.scan_tiles * kThreads * 4;
+    prm.ws = nullptr;
+    prm.ws_s2 = 0;
+    // A workspace moves pass 2 to a second launch (not for the staged early
+    // exit, which keeps the decided rows in shared memory).
+    const bool two = opt && opt->workspace && shp.kind != kKindEarlyStaged;
+    if (two) {
+        st = prepare_workspace(opt, B, prm.num_chunks, false, shp.sms, (cudaStream_t)stream, &prm.ws_s2);
+        if (st != SPEC_OK)
+            return st;
+        prm.ws = reinterpret_cast<unsigned char *>(opt->workspace);
+    }
+    size_t dyn = two ? (size_t)kWorkerSmemBytes : (size_t)kP2SmemBytes;
     if (shp.kind == kKindEarlyStaged)
         dyn += (size_t)nslot * (size_t)slice * 16;
 
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg =
-        launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
+        launch_config((unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_for(dtype, shp.kind, point), args);
     if (e != cudaSuccess) {
@@ -561,18 +548,24 @@ spec_status run_tree(const void *target, const int32_t *parent, const int32_t *t
     prm.gmax = N - 1;
     prm.V = V;
     prm.num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
-    const int slice = (prm.num_chunks + shp.C - 1) / shp.C;
-    const int tiles = (slice + kThreads - 1) / kThreads;
-    prm.scan_tiles = tiles <= kMaxScanTiles ? tiles : 0;
     prm.ordered = 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = parent;
     prm.out_path = out_path;
-    const size_t dyn = (size_t)prm.scan_tiles * kThreads * 4;
+    prm.ws = nullptr;
+    prm.ws_s2 = 0;
+    const bool two = opt && opt->workspace;
+    if (two) {
+        st = prepare_workspace(opt, B, prm.num_chunks, true, shp.sms, (cudaStream_t)stream, &prm.ws_s2);
+        if (st != SPEC_OK)
+            return st;
+        prm.ws = reinterpret_cast<unsigned char *>(opt->workspace);
+    }
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg =
-        launch_config(shp.kind, (unsigned)B * (unsigned)shp.C, shp.C, dyn, (cudaStream_t)stream, attr);
+    cudaLaunchConfig_t cfg = launch_config((unsigned)B * (unsigned)shp.C, shp.C,
+                                           two ? (size_t)kWorkerSmemBytes : (size_t)kP2SmemBytes,
+                                           (cudaStream_t)stream, attr);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_for(dtype, shp.kind, false), args);
     if (e != cudaSuccess) {
@@ -641,8 +634,6 @@ spec_status spec_sample(const void *logits, const float *uniforms, const float *
                         const spec_verify_options *options)
 {
     NvtxScope nvtx("spec_sample");
-    if (options && options->kernel == 1)
-        return SPEC_ERR_UNSUPPORTED;  // the ring kernel is a full-sweep A/B variant only
     return run(logits, nullptr, nullptr, nullptr, uniforms, temperature, out_tokens, nullptr, B, 0, V, dtype, status,
                stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, options);
 }
@@ -699,7 +690,25 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
     if (num_ctas)
         *num_ctas = B * shp.C;
     if (threads_per_cta)
-        *threads_per_cta = kernel_threads(shp.kind);
+        *threads_per_cta = kThreads;
+    return SPEC_OK;
+}
+
+spec_status spec_workspace_size(int B, int V, spec_dtype dtype, int tree, uint64_t *bytes)
+{
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16)
+        return SPEC_ERR_UNSUPPORTED;
+    if (!bytes || B < 0 || B > SPEC_MAX_BATCH || V < 1 || V > SPEC_MAX_VOCAB)
+        return SPEC_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    spec_status st = current_device(&dev);
+    if (st != SPEC_OK)
+        return st;
+    st = device_sm_count(dev, &sms);
+    if (st != SPEC_OK)
+        return st;
+    const int num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
+    *bytes = (uint64_t)ws_layout(B, pass2_slices(B, num_chunks, sms), tree != 0).total;
     return SPEC_OK;
 }
 
@@ -723,17 +732,6 @@ spec_status spec_device_pointer(const void *ptr, const void **device_ptr)
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged && a.type != cudaMemoryTypeHost)
         return SPEC_ERR_INVALID_ARG;
     *device_ptr = a.devicePointer;
-    return SPEC_OK;
-}
-
-spec_status spec_selftest_bounded_wait(uint32_t *status, void *stream)
-{
-    NvtxScope nvtx("spec_selftest_bounded_wait");
-    if (!status || ((uintptr_t)status & 3u))
-        return SPEC_ERR_INVALID_ARG;
-    spec_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status);
-    if (cudaGetLastError() != cudaSuccess)
-        return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 

@@ -33,11 +33,14 @@
 //     rank order (identical bits in every CTA) and takes the accept decision
 //     itself: one lane per draft position, a warp ballot gives the first
 //     rejection.  No second barrier is needed to broadcast it.
-//   * Pass 2 (sampled sequences only) touches the one decided row (target,
-//     plus draft when a draft was rejected): weights max(0, p - q), p, or p
-//     without some ids, as unsigned 64-bit fixed point (2^-60 units), so every
-//     sum is exact and order-free.  Slice sums are exchanged over DSMEM; the
-//     CTA whose slice holds floor(u*S) scans its chunks and writes the id.
+//   * Pass 2 (sampled sequences only) sweeps the one decided row (target, plus
+//     draft when a draft was rejected) and puts every sampling weight on an
+//     exact 2^-60 integer grid: ids near the top of the row get an extended-
+//     precision exp2 (about 2^-36 relative), the rest their float32 value, so
+//     that the draw agrees with the float64 definition except within ~1e-10
+//     of a boundary (see "pass 2" below).  Per-warp and per-CTA sums cross the
+//     cluster over DSMEM; the CTA whose slice holds floor(u*S) recomputes one
+//     warp range of it and writes the id.
 //
 // Kernels sharing that protocol:
 //   spec_verify_stream_kernel (default) 128-bit loads straight into registers,
@@ -50,17 +53,9 @@
 //                             cache) keeps each position's slices in shared
 //                             memory so pass 2 reads nothing over the link.
 //   spec_tree_kernel          a walk down a tree of candidates, one row per level.
-//   spec_verify_ring_kernel   16-byte-aligned rows only.  A producer warp streams
-//                             the CTA's slices through an 8-stage shared-memory
-//                             ring with cp.async.bulk (the bulk-copy engine)
-//                             and mbarriers; eight reducing warps read shared
-//                             memory.  On GB300 it is slower here: the ring's
-//                             78 KB of shared memory leaves only 16 reducing
-//                             warps per SM.  Kept for A/B runs.
 // No kernel uses global scratch memory, atomics on the data path (only the
-// optional status word and counters) or unbounded waits: mbarrier waits give up
-// after a fixed number of tries or 0.2 s and report SPEC_STATUS_TIMEOUT, and
-// the only other waits are hardware barriers that every thread reaches.
+// optional status word and counters) or waits other than hardware barriers
+// that every thread of the CTA or of the cluster reaches.
 
 #pragma once
 
@@ -79,26 +74,14 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int kWarps = 8;  // warps that reduce (both kernels)
+constexpr int kWarps = 8;  // warps that reduce
 constexpr int kThreads = kWarps * 32;
-constexpr int kTmaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMaxRows = 2 * SPEC_MAX_GAMMA + 1;
 constexpr int kMaxCluster = 16;
-constexpr int kUnroll = 8;       // scalar kernel: 16-byte loads in flight per thread
-constexpr int kSegChunks = 512;  // ring kernel: 16-byte chunks per ring stage (8 KB)
-constexpr int kChunksPerThread = kSegChunks / kThreads;
-constexpr int kStages = 8;  // ring depth: 64 KB
-constexpr int kRingBytes = kStages * kSegChunks * 16;
-constexpr int kMaxSpin = 1 << 18;  // tries of one mbarrier wait before giving up
-constexpr unsigned long long kMaxWaitNs = 200000000ull;  // ... or this much wall time (0.2 s)
-constexpr int kMaxScanTiles = 48;  // register kernel: at most 48 * kThreads chunk sums (48 KB) in shared memory
+constexpr int kUnroll = 8;         // pass 1: 16-byte loads in flight per thread
 constexpr int kMaxOrdered = 1024;  // longest-first scheduling for B up to this
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kFixedUnit = 8.6736173798840355e-19f;    // 2^-60: pass-2 weight unit (to_fixed60)
-constexpr unsigned long long kTimeoutFlag = 1ull << 63;  // carried in exchanged slice sums
-
-static_assert(kSegChunks % kThreads == 0, "a segment must split evenly over the reducing threads");
 
 struct Params {
     const void *target;
@@ -118,12 +101,13 @@ struct Params {
     int32_t *seq_status;
     int B, gmax, V;
     int num_chunks;  // 16-byte chunks per row; the last is partial on the scalar path
-    int scan_tiles;  // register kernel: tiles of kThreads chunk sums kept in shared memory (0 = none)
     int ordered;     // map clusters to sequences longest-first (small B only)
     unsigned long long *counters;  // optional: += drafted, accepted, verified sequences
     unsigned long long *hist;      // optional: [SPEC_MAX_GAMMA + 1] += 1 at the accepted count
     const int32_t *parent;         // tree kernel: [B, gmax+1] parent of each node (num_draft = node count)
     int32_t *out_path;             // tree kernel: [B, gmax+1] accepted node indices, or NULL
+    unsigned char *ws;             // workspace: pass 2 as tasks for any CTA (NULL: each cluster samples its own)
+    int ws_s2;                     // pass-2 slices per row
 };
 
 // ---------------------------------------------------------------------------
@@ -377,46 +361,6 @@ struct RowAcc {
             t = __fadd2_rn(t, acc[q]);
         compensated_add(hi, lo, t.x + t.y);
     }
-    // add_soft that also leaves each chunk's sum of 2^(a - m) in cs[j * kThreads]
-    // (j = j0 + u: the chunk's tile in the slice, for j < tiles), rescaling the
-    // entries stored earlier when m rises.  Used for a row that pass 2 samples
-    // from as p itself (the sampler), so that its owner needs no second sweep.
-    template <typename T, int N>
-    __device__ __forceinline__ void add_soft_store(const uint4 (&v)[N], float k, float *cs, int j0, int tiles)
-    {
-        const float amax = chunks_max<T, N>(v) * k;
-        if (amax > m) {
-            const float mn = ceilf(amax);
-            const float sc = pow2_int(m - mn);
-            hi *= sc;
-            lo *= sc;
-            for (int j = 0; j < j0 && j < tiles; ++j)
-                cs[j * kThreads] *= sc;
-            m = mn;
-        }
-        if (m == -INFINITY) {
-#pragma unroll
-            for (int u = 0; u < N; ++u)
-                if (j0 + u < tiles)
-                    cs[(j0 + u) * kThreads] = 0.0f;
-            return;
-        }
-        constexpr int P = Elem<T>::W / 2;
-        const float2 k2 = make_float2(k, k), nm2 = make_float2(-m, -m);
-        float t = 0.0f;
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            float2 a = ex2_pair(__ffma2_rn(pair<T>(v[u], 0), k2, nm2));
-#pragma unroll
-            for (int q = 1; q < P; ++q)
-                a = __fadd2_rn(a, ex2_pair(__ffma2_rn(pair<T>(v[u], q), k2, nm2)));
-            const float cu = a.x + a.y;
-            if (j0 + u < tiles)
-                cs[(j0 + u) * kThreads] = cu;
-            t += cu;
-        }
-        compensated_add(hi, lo, t);
-    }
     // Adds chunks v[0..N) of a greedy row; chunk u starts at element index
     // base + u * stride.  Chunks arrive in increasing index order, so a strict
     // improvement keeps the lowest index of the maximum.
@@ -464,117 +408,355 @@ __device__ __forceinline__ unsigned long long to_fixed60(float w)
     return mant >> (-sh);
 }
 
-// Pass-2 weights of one chunk of the decided row: max(0, p - q) (residual) or
-// p, in float32.  tv/dv: the target and draft chunk.
-struct WeightParams {
-    float k, negmt, invzt, negmd, invzd;
-    bool residual;  // max(0, p - q) with q from the draft row
-    int zero_at;    // point-mass residual: p with this id removed (-1: none)
-    int zero_chunk; // the chunk holding zero_at (-1: none)
-    const int *zset;  // ZSET weights: p with these nz ids removed (a tree node's rejected candidates)
+
+// ---------------------------------------------------------------------------
+// pass 2: sampling weights on an exact integer grid
+// ---------------------------------------------------------------------------
+// The final draw is the smallest id j with u*S < C_j, so the boundary C_j/S of
+// an id depends on every weight before it.  Float32 weights (about 1e-7
+// relative error each, plus the float32 rounding of log2(e)/T, which tilts a
+// whole row) move the boundaries of a 128k-id row by ~1e-8 each, enough to
+// change about one full-row draw in a thousand against the float64
+// definition; a residual max(0, p - q) of small total amplifies that by
+// 1/total.  Pass 2 therefore puts every weight on a 2^-60 integer grid:
+//   * a "heavy" id, whose float32 weight is within a factor 2^kHeavySpan of the
+//     row's largest, gets 2^(l*K - mref) to about 2^-36 relative (exact_weight:
+//     K = log2(e)/T as a float-float pair, a float-float table of 2^(i/32) and
+//     a degree-4 polynomial for the rest -- the table-driven exponential of
+//     P. T. P. Tang, ACM TOMS 15(2), 1989 -- with Dekker's exact product and
+//     Knuth's exact sum splits);
+//   * every other id keeps ex2.approx(l*K - mref) in float32, summed in float32
+//     per chunk in id order and rounded to the grid once per chunk.  These ids
+//     hold at most ~V * 2^-kHeavySpan of the top weight, and their errors are
+//     unbiased.
+// Sums of grid integers are exact and order-free, so every CTA and every pass
+// sees the same boundaries.  A residual max(0, p - q) = max(0, a/A - b/B) (a, b
+// the target and draft weights, A, B their row totals) is sampled as the
+// integer weight a*B - b*A over the set J of ids where the float32 values say
+// p > q; a sum over J is then A_J*B - B_J*A, so a single sweep that keeps A_J
+// and B_J per warp range and A, B per row is enough.  (An id that float32
+// misplaces in J has |p - q| ~ 1e-7 p, so its contribution is negligible.)
+constexpr float kHeavySpan = 18.0f;  // log2 of the heavy window below the top weight
+constexpr int kP2Unroll = 4;         // pass-2 sweep: chunks in flight per thread (one row; half each for two)
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic rounds x to an integer for |x| < 2^22
+constexpr float kLn2Lo = -1.9046542121259336e-09f;  // ln 2 - (float)ln 2
+constexpr float kC2 = 0.24022650718688965f;    // (ln 2)^2 / 2
+constexpr float kC3 = 0.05550410971045494f;    // (ln 2)^3 / 6
+constexpr float kC4 = 0.009618128649890423f;   // (ln 2)^4 / 24
+
+// 2^(i/32) for i = -16..16 as float-float pairs (hi + lo), from the
+// exponential series summed in double precision at compile time.
+constexpr double series_exp(double x)
+{
+    double term = 1.0, sum = 1.0;
+    for (int n = 1; n < 40; ++n) {
+        term *= x / n;
+        sum += term;
+    }
+    return sum;
+}
+struct Exp2Table {
+    float hi[33];
+    float lo[33];
+};
+constexpr Exp2Table make_exp2_table()
+{
+    Exp2Table t{};
+    for (int i = 0; i < 33; ++i) {
+        const double v = series_exp((i - 16) / 32.0 * 0.6931471805599453094);
+        t.hi[i] = (float)v;
+        t.lo[i] = (float)(v - (double)t.hi[i]);
+    }
+    return t;
+}
+__device__ const Exp2Table kExp2Table = make_exp2_table();
+
+// One row's weight scale: weight_j = 2^(l_j * K - mref), K = khi + klo.
+struct ExactRow {
+    float khi, klo;  // log2(e)/T as a float-float pair
+    float nmref;     // -mref (integer-valued)
+    int e60;         // 60 - mref: weight * 2^60 = 2^(n + e60) * 2^f
+    float heavy;     // fast argument above this: exact weight (+inf: none)
+    bool wide;       // |l * K| may pass 2^12: fold the product's low part in first
+    float c;         // 2^ez / Z: float32 probability = fast weight * c (the set J)
+};
+
+// floor((s + lo) * 2^E) for a normalised float-float pair (s in [1/2, 2),
+// |lo| <= ulp(s)/2), by integer operations; E <= 62.
+__device__ __forceinline__ unsigned long long fixed_pair(float s, float lo, int E)
+{
+    const uint32_t sb = __float_as_uint(s);
+    const int es = (int)(sb >> 23) - 127;              // -1 or 0
+    const uint32_t ms = (sb & 0x7FFFFFu) | 0x800000u;  // s = ms * 2^(es - 23)
+    // lo * 2^(45 - es): |.| <= 2^21, rounded to an integer
+    const float L = __fmaf_rn(lo, es < 0 ? 70368744177664.0f : 35184372088832.0f, kMagic);
+    const long long M = ((long long)ms << 22) + (long long)(__float_as_int(L) - __float_as_int(kMagic));
+    const int sh = E + es - 45;  // (s + lo) * 2^E = M * 2^sh
+    if (sh >= 0)
+        return (unsigned long long)M << sh;
+    if (sh <= -63)
+        return 0ull;
+    return (unsigned long long)M >> (-sh);
+}
+
+// round(v * 2^60) for a float v with |v| < 8, signed, by integer operations.
+__device__ __forceinline__ long long fixed60_signed(float v)
+{
+    const uint32_t b = __float_as_uint(v);
+    const int ex = (int)((b >> 23) & 0xFFu);
+    if (ex == 0)
+        return 0;  // zero or below 2^-126
+    const unsigned long long mant = (b & 0x7FFFFFu) | 0x800000u;
+    const int sh = ex - 90;  // |v| * 2^60 = mant * 2^(ex - 90)
+    const unsigned long long mag = sh >= 0 ? mant << sh : (sh <= -24 ? 0ull : mant >> (-sh));
+    return (b >> 31) ? -(long long)mag : (long long)mag;
+}
+
+// 2^(l * K - mref) on the 2^-60 grid, to about 2^-36 relative, by float32
+// operations only (each rounding explicit, so that every call site computes
+// the same bits).  Needs |l * K| < 2^21 (the caller's 'exact' rows).
+__device__ __forceinline__ unsigned long long exact_weight(float l, const ExactRow &er)
+{
+    const float ph = __fmul_rn(l, er.khi);
+    float pl = __fmaf_rn(l, er.khi, -ph);  // l*khi = ph + pl exactly (Dekker)
+    pl = __fmaf_rn(l, er.klo, pl);         // + l*klo
+    const float t = __fadd_rn(ph, kMagic);
+    float f = __fsub_rn(ph, __fsub_rn(t, kMagic));  // ph - rint(ph): exact, |f| <= 1/2
+    int n = __float_as_int(t) - __float_as_int(kMagic);
+    if (er.wide) {  // |pl| up to 2^-2: two-sum f + pl (Knuth) and split again
+        const float s = __fadd_rn(f, pl);
+        const float bb = __fsub_rn(s, f);
+        const float e = __fadd_rn(__fsub_rn(f, __fsub_rn(s, bb)), __fsub_rn(pl, bb));
+        const float t1 = __fadd_rn(s, kMagic);
+        f = __fsub_rn(s, __fsub_rn(t1, kMagic));
+        n += __float_as_int(t1) - __float_as_int(kMagic);
+        pl = e;
+    }
+    // f = i/32 + r with |r| <= 1/64, r exact
+    const float t2 = __fmaf_rn(f, 32.0f, kMagic);
+    const int i = min(max(__float_as_int(t2) - __float_as_int(kMagic) + 16, 0), 32);  // [0, 32] already
+    const float r = __fmaf_rn(__fsub_rn(t2, kMagic), -0.03125f, f);
+    // 2^(r + pl) - 1 = hh + Q: first-order part as an exact pair, the rest small
+    const float h = __fmul_rn(r, kLn2);
+    const float he = __fmaf_rn(r, kLn2, -h);
+    const float g = __fmul_rn(pl, kLn2);
+    const float hh = __fadd_rn(h, g);
+    const float gb = __fsub_rn(hh, h);
+    const float eg = __fadd_rn(__fsub_rn(h, __fsub_rn(hh, gb)), __fsub_rn(g, gb));
+    const float rs = __fadd_rn(r, pl);
+    const float r2 = __fmul_rn(rs, rs);
+    float q = __fmaf_rn(rs, kC4, kC3);
+    q = __fmaf_rn(rs, q, kC2);
+    float Q = __fmaf_rn(r2, q, he);
+    Q = __fadd_rn(Q, eg);
+    Q = __fmaf_rn(rs, kLn2Lo, Q);
+    // 2^(i/32) * (1 + hh + Q) as a normalised float-float pair
+    const float th = __ldg(&kExp2Table.hi[i]), tl = __ldg(&kExp2Table.lo[i]);
+    const float u = __fmul_rn(th, hh);
+    const float ue = __fmaf_rn(th, hh, -u);
+    const float s0 = __fadd_rn(th, u);  // |u| < th: fast two-sum
+    const float se = __fsub_rn(u, __fsub_rn(s0, th));
+    float lo = __fmaf_rn(th, Q, tl);
+    lo = __fmaf_rn(tl, hh, lo);
+    lo = __fadd_rn(lo, ue);
+    lo = __fadd_rn(lo, se);
+    const float s = __fadd_rn(s0, lo);
+    lo = __fsub_rn(lo, __fsub_rn(s, s0));
+    return fixed_pair(s, lo, n + er.e60);
+}
+
+// Pass-2 weights of one decided row (or of a target/draft pair).
+enum P2Mode {
+    kP2Full = 0,      // p (the bonus row, or a degenerate residual)
+    kP2Residual = 1,  // max(0, p - q) from a target and a draft row
+    kP2Zero = 2       // p without some ids (point-mass residual; a tree node's rejected candidates)
+};
+
+// Per-sequence constants of pass 2, identical in every CTA of the cluster.
+struct P2Seq {
+    ExactRow rt, rd;  // target row; draft row (residual)
+    int mode;
+    int zero_at, zero_chunk;  // kP2Zero: one removed id (-1: none) and its chunk
+    const int *zset;          // kP2Zero: nz more removed ids (shared memory)
     int nz;
 };
 
-template <typename T, bool ZSET = false>
-__device__ __forceinline__ void chunk_weights(const uint4 &tv, const uint4 &dv, const WeightParams &wp,
-                                              float (&w)[Elem<T>::W], int chunk = -2)
+// ExactRow of a row with merged pass-1 statistics st at temperature temp:
+// mref = st.m + e, 2^e >= the row's float32 normaliser, so that each weight is
+// at most ~1 and a row total at most ~1 on the 2^-60 grid.
+__device__ __forceinline__ ExactRow exact_row(const RowStat &st, float temp)
 {
-    constexpr int P = Elem<T>::W / 2;
-    const float2 k2 = make_float2(wp.k, wp.k);
-    const float2 nmt = make_float2(wp.negmt, wp.negmt), izt = make_float2(wp.invzt, wp.invzt);
-    const float2 nmd = make_float2(wp.negmd, wp.negmd), nizd = make_float2(-wp.invzd, -wp.invzd);
+    ExactRow er;
+    const double K = 1.4426950408889634 / (double)temp;
+    er.khi = __double2float_rd(K);  // so that klo > 0: l = -inf gives -inf, not NaN
+    er.klo = (float)(K - (double)er.khi);
+    const float z = st.hi + st.lo;  // >= 1/2
+    const int ez = (int)((__float_as_uint(z) >> 23) & 0xFFu) - 126;  // z < 2^ez
+    const float mref = st.m + (float)ez;
+    er.nmref = -mref;
+    er.e60 = 60 - (int)mref;
+    const float am = fabsf(st.m) + 48.0f;  // bound on |l * K| over heavy ids
+    er.wide = am >= 4096.0f;
+    // heavy: fast weight above 2^-kHeavySpan of the largest (which is >= 2^(-ez-1))
+    er.heavy = am < 2097152.0f ? -(kHeavySpan + 1.0f + (float)ez) : INFINITY;
+    er.c = (float)(ldexp(1.0, ez) / (double)z);
+    return er;
+}
+
+// Fast pass over one chunk: the float32 weights of the non-heavy ids summed in
+// id order (J only and all), which ids are heavy and which are in J.  runt /
+// rund receive the running J sums after each id (the owner's final search).
+struct ChunkP2 {
+    float jt, at, jd, ad;  // non-heavy weights: in J, all (target, draft)
+    uint32_t heavy;        // bit e: target id e heavy; bit 8 + e: draft id e heavy
+    uint32_t inj;          // bit e: id e in J
+};
+
+template <typename T, bool RESID>
+__device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, int c, const P2Seq &ps,
+                                            float (&runt)[Elem<T>::W], float (&rund)[Elem<T>::W])
+{
+    constexpr int W = Elem<T>::W, P = W / 2;
+    const float2 kh = make_float2(ps.rt.khi, ps.rt.khi), kl = make_float2(ps.rt.klo, ps.rt.klo);
+    const float2 nmt = make_float2(ps.rt.nmref, ps.rt.nmref), nmd = make_float2(ps.rd.nmref, ps.rd.nmref);
+    uint32_t inj = (1u << W) - 1u;
+    if (!RESID && ps.mode == kP2Zero) {
+        if (c == ps.zero_chunk)
+            inj &= ~(1u << (ps.zero_at - c * W));
+        for (int z = 0; z < ps.nz; ++z) {
+            const int d = ps.zset[z] - c * W;
+            if (d >= 0 && d < W)
+                inj &= ~(1u << d);
+        }
+    }
+    ChunkP2 o{0.0f, 0.0f, 0.0f, 0.0f, 0u, 0u};
+    // one id at a time, in id order (the running sums are sequential)
+    auto step = [&](int e, float yt, float wt, float yd, float wd) {
+        const bool ht = yt > ps.rt.heavy;
+        const float a = ht ? 0.0f : wt;
+        bool j = (inj >> e) & 1u;
+        if (RESID) {
+            const bool hd = yd > ps.rd.heavy;
+            const float b = hd ? 0.0f : wd;
+            j = __fmul_rn(wt, ps.rt.c) > __fmul_rn(wd, ps.rd.c);
+            o.heavy |= (uint32_t)hd << (8 + e);
+            o.ad = __fadd_rn(o.ad, b);
+            o.jd = __fadd_rn(o.jd, j ? b : 0.0f);
+        }
+        o.heavy |= (uint32_t)ht << e;
+        o.inj |= (uint32_t)j << e;
+        o.at = __fadd_rn(o.at, a);
+        o.jt = __fadd_rn(o.jt, j ? a : 0.0f);
+        runt[e] = o.jt;
+        rund[e] = o.jd;
+    };
 #pragma unroll
     for (int q = 0; q < P; ++q) {
-        float2 pq = __fmul2_rn(ex2_pair(__ffma2_rn(pair<T>(tv, q), k2, nmt)), izt);
-        if (wp.residual) {
-            pq = __ffma2_rn(ex2_pair(__ffma2_rn(pair<T>(dv, q), k2, nmd)), nizd, pq);  // p - q
-            pq.x = fmaxf(pq.x, 0.0f);
-            pq.y = fmaxf(pq.y, 0.0f);
+        const float2 l = pair<T>(tv, q);
+        float2 y = __ffma2_rn(l, kh, nmt);
+        y = __ffma2_rn(l, kl, y);
+        const float2 w = ex2_pair(y);
+        float2 x = make_float2(0.0f, 0.0f), v = make_float2(0.0f, 0.0f);
+        if (RESID) {
+            const float2 ld = pair<T>(dv, q);
+            x = __ffma2_rn(ld, kh, nmd);
+            x = __ffma2_rn(ld, kl, x);
+            v = ex2_pair(x);
         }
-        w[2 * q] = pq.x;
-        w[2 * q + 1] = pq.y;
+        step(2 * q, y.x, w.x, x.x, v.x);
+        step(2 * q + 1, y.y, w.y, x.y, v.y);
     }
-    if (chunk == wp.zero_chunk) {  // point-mass residual: the rejected id has no weight
-#pragma unroll
-        for (int e = 0; e < Elem<T>::W; ++e)
-            if (chunk * Elem<T>::W + e == wp.zero_at)
-                w[e] = 0.0f;
-    }
-    if constexpr (ZSET) {  // several rejected ids (short list in shared memory)
-        const int lo = chunk * Elem<T>::W;
-        for (int z = 0; z < wp.nz; ++z) {
-            const int id = wp.zset[z];
-            if (id >= lo && id < lo + Elem<T>::W) {
-#pragma unroll
-                for (int e = 0; e < Elem<T>::W; ++e)
-                    if (lo + e == id)
-                        w[e] = 0.0f;
-            }
-        }
-    }
+    return o;
 }
 
-// A chunk's weight: the float32 sum of its elements in a fixed tree order ...
-template <typename T> __device__ __forceinline__ float chunk_sum(const float (&w)[Elem<T>::W])
+// Element e of a staged 16-byte chunk.
+template <typename T> __device__ __forceinline__ float staged_elem(const uint4 *chunk, int e)
 {
-    if (Elem<T>::W == 8)
-        return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-    return (w[0] + w[1]) + (w[2] + w[3]);
+    if (sizeof(T) == 2)
+        return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short *>(chunk)[e] << 16);
+    return reinterpret_cast<const float *>(chunk)[e];
 }
 
-// ... on the exact 2^-60 grid, converted once.  Prefix sums of these are exact,
-// so every CTA and every pass sees the same cumulative boundaries.
-template <typename T> __device__ __forceinline__ unsigned long long chunk_fixed(const float (&w)[Elem<T>::W])
+// Dynamic shared memory of pass 2: the chunks of one warp batch (kP2Slots
+// slots: kP2Unroll chunks of one row, or half as many of two) and the queue of
+// their heavy ids.
+constexpr int kP2Slots = kP2Unroll;
+static_assert(kP2Slots <= 8, "queue entries keep the slot in 3 bits");
+struct P2Smem {
+    uint4 stage[kWarps][kP2Slots][32];
+    unsigned short queue[kWarps][kP2Slots * 32 * 8];
+};
+constexpr int kP2SmemBytes = (int)sizeof(P2Smem);
+
+typedef __int128 i128;
+typedef unsigned __int128 u128;
+
+// Residual weight of a sum: JT*B - JD*A; the weights themselves otherwise (B = 1, JD = 0).
+__device__ __forceinline__ i128 p2_value(unsigned long long jt, unsigned long long jd, unsigned long long A,
+                                         unsigned long long B)
 {
-    return to_fixed60(chunk_sum<T>(w));
+    return (i128)((u128)jt * B) - (i128)((u128)jd * A);
 }
 
-template <typename T>
-__device__ __forceinline__ unsigned long long chunk_weight_fixed(const uint4 &tv, const uint4 &dv,
-                                                                 const WeightParams &wp)
-{
-    float w[Elem<T>::W];
-    chunk_weights<T>(tv, dv, wp, w);
-    return chunk_fixed<T>(w);
-}
-
-// Inside the chunk whose cumulative interval holds theta (rel = theta - chunk
-// start, 0 <= rel < chunk weight): the first element whose running float sum,
-// on the 2^-60 grid, passes rel; the last element with weight > 0 if rounding
-// leaves none.  An element of weight 0 is never picked.
-template <typename T>
-__device__ __forceinline__ int pick_in_chunk(const float (&w)[Elem<T>::W], unsigned long long rel)
-{
-    float run = 0.0f;
-    int last = 0;
-#pragma unroll
-    for (int e = 0; e < Elem<T>::W; ++e) {
-        run += w[e];
-        if (w[e] > 0.0f) {
-            if (rel < to_fixed60(run))
-                return e;
-            last = e;
-        }
-    }
-    return last;
-}
-
-// floor(u * S) exactly, u a float in [0, 1), S a 64-bit integer.
-__device__ __forceinline__ unsigned long long scaled_floor(float u, unsigned long long S)
+// floor(u * R) exactly, u a float in [0, 1), 0 <= R < 2^124.
+__device__ __forceinline__ i128 scaled_floor128(float u, i128 R)
 {
     const uint32_t bits = __float_as_uint(u);
     const uint32_t ex = (bits >> 23) & 0xFFu;
-    if (ex == 0 && (bits & 0x7FFFFFu) == 0)
-        return 0ull;
+    if (R <= 0 || (ex == 0 && (bits & 0x7FFFFFu) == 0))
+        return 0;
     const unsigned long long mant = (bits & 0x7FFFFFu) | (ex ? 0x800000u : 0u);
     const int sh = 150 - (int)(ex ? ex : 1u);  // u = mant * 2^-sh, sh >= 24
-    const unsigned long long lo = mant * S;
-    const unsigned long long hi = __umul64hi(mant, S);
-    if (sh >= 128)
-        return 0ull;
-    if (sh >= 64)
-        return hi >> (sh - 64);
-    return (lo >> sh) | (hi << (64 - sh));
+    const u128 ur = (u128)R;
+    const u128 hi = (u128)mant * (unsigned long long)(ur >> 64);  // mant * R = hi * 2^64 + lo
+    const u128 lo = (u128)mant * (unsigned long long)ur;
+    if (sh >= 192)
+        return 0;
+    if (sh <= 64)
+        return (i128)((hi << (64 - sh)) + (lo >> sh));
+    return (i128)((hi + (lo >> 64)) >> (sh - 64));
+}
+
+// Inclusive block scan of a signed 128-bit value over the CTA; also the total.
+__device__ __forceinline__ i128 block_scan_i128(i128 v, i128 &total, i128 *warp_tot)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long lo = __shfl_up_sync(0xffffffffu, (unsigned long long)v, d);
+        const long long hi = __shfl_up_sync(0xffffffffu, (long long)(v >> 64), d);
+        if (lane >= d)
+            v += (i128)(((u128)(unsigned long long)hi << 64) | lo);
+    }
+    __syncthreads();
+    if (lane == 31)
+        warp_tot[wid] = v;
+    __syncthreads();
+    i128 before = 0, t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < wid)
+            before += warp_tot[w];
+        t += warp_tot[w];
+    }
+    total = t;
+    return v + before;
+}
+
+// Lowest thread of the CTA with flag set (kThreads if none); all threads call it.
+__device__ __forceinline__ int block_first(bool flag, int *wmin)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const unsigned b = __ballot_sync(0xffffffffu, flag);
+    __syncthreads();
+    if (lane == 0)
+        wmin[wid] = b ? wid * 32 + __ffs(b) - 1 : kThreads;
+    __syncthreads();
+    int m = kThreads;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        m = min(m, wmin[w]);
+    return m;
 }
 
 // ---------------------------------------------------------------------------
@@ -593,69 +775,6 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Barrier of the kThreads reducing threads only (named barrier 1).
-__device__ __forceinline__ void reducers_sync()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long *bar)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ unsigned long long global_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Waits for the phase of the given parity to complete; false after kMaxSpin
-// tries or kMaxWaitNs of wall time, whichever comes first (one try may suspend
-// the thread for a hardware-defined time, so the tries alone bound the count,
-// not the duration).
-__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity)
-{
-    const uint32_t a = smem_addr(bar);
-    const unsigned long long t0 = global_ns();
-    for (int i = 0; i < kMaxSpin; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done)
-            return true;
-        if ((i & 63) == 63 && global_ns() - t0 > kMaxWaitNs)
-            break;
-    }
-    return false;
-}
-// Bulk copy (bulk-copy engine, no registers involved) of 'bytes' from global
-// memory into this CTA's shared memory; completion is signalled on 'bar'.
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // shared state and the per-sequence protocol common to both kernels
@@ -664,9 +783,9 @@ struct SharedState {
     RowStat warp_part[kMaxRows][kWarps];
     RowStat recv[kMaxCluster][kMaxRows];  // written remotely by every CTA of the cluster
     RowStat row[kMaxRows];                // merged statistics, identical in every CTA
-    unsigned long long recv_sum[2][kMaxCluster];
-    unsigned long long warp_sum[kWarps + 1];
-    unsigned long long tile_tot[kMaxScanTiles];
+    unsigned long long p2w[kWarps][4];    // pass 2: sums of each warp range (J target, J draft, all target, all draft)
+    unsigned long long p2recv[2][kMaxCluster][4];  // pass 2: each CTA's sums, written remotely [attempt][rank]
+    i128 p2scan[kWarps];                  // pass 2: block-scan partials
     int hist[kMaxRows + 1];
     int cnt[kWarps];
     int seq;
@@ -674,11 +793,9 @@ struct SharedState {
     float seq_temp;
     int bin;
     int rank_in_bin;
-    int recv_flag[kMaxCluster];
     RowStat recv_pos[2][kMaxCluster][2];  // early-exit kernel: [position parity][source rank][t / d]
     int n;
     int bits;
-    int timeout;
     int stop;
     int drafted[SPEC_MAX_GAMMA];  // the sequence's drafted ids (full-sweep decision)
 };
@@ -702,7 +819,8 @@ struct Seq {
     bool sampled;
     bool point;   // deterministic proposals: no draft rows, q_i(x_i) = 1
     bool drafts;  // sampled with draft rows to read
-    float k;  // log2(e) / T for sampled sequences
+    float k;      // log2(e) / T for sampled sequences (pass 1)
+    float temp;   // T
     size_t rowlen;
 };
 
@@ -800,8 +918,6 @@ __device__ __forceinline__ void exchange_rows(SharedState &sh, const Seq &s, int
         for (int dst = 0; dst < s.C; ++dst)
             *cluster.map_shared_rank(&sh.recv[s.rank][tid], dst) = v;
     }
-    if (tid < s.C)
-        *cluster.map_shared_rank(&sh.recv_flag[s.rank], tid) = sh.timeout;
     cluster_sync_all();
     if (tid < nrows) {
         RowStat v = sh.recv[0][tid];
@@ -916,11 +1032,6 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
             bits = SPEC_STATUS_BAD_TOKEN;
         else if (s.sampled && (n < g ? !((fine >> n) & 1u) : !soft_row_ok(sh.row[g])))
             bits = SPEC_STATUS_BAD_LOGITS;
-        int flag = 0;
-        for (int c = 0; c < s.C; ++c)
-            flag |= sh.recv_flag[c];
-        if (flag)
-            bits = SPEC_STATUS_TIMEOUT;
         if (lane == 0) {
             sh.n = n;
             sh.bits = (int)bits;
@@ -973,51 +1084,6 @@ __device__ __forceinline__ bool decide_and_write(const Params &p, SharedState &s
     return s.sampled && !bits;
 }
 
-// Pass-2 weight parameters of decided row n.  residual: the row of a
-// rejection, whose weights are max(0, p - q); with point-mass proposals that
-// is p with the rejected id xn removed.  Otherwise the weights are p.
-__device__ __forceinline__ WeightParams weight_params(const SharedState &sh, const Seq &s, int n, bool residual,
-                                                     int xn, int chunk_width)
-{
-    const RowStat st = sh.row[n];
-    const bool rows = residual && s.drafts;
-    const RowStat sd = rows ? sh.row[s.g + 1 + n] : st;
-    WeightParams wp;
-    wp.k = s.k;
-    wp.negmt = -st.m;
-    wp.invzt = 1.0f / (st.hi + st.lo);
-    wp.negmd = -sd.m;
-    wp.invzd = 1.0f / (sd.hi + sd.lo);
-    wp.residual = rows;
-    wp.zero_at = (residual && !s.drafts) ? xn : -1;
-    wp.zero_chunk = wp.zero_at >= 0 ? wp.zero_at / chunk_width : -1;
-    wp.zset = nullptr;
-    wp.nz = 0;
-    return wp;
-}
-
-// Sends this CTA's slice sum to every CTA of the cluster, then sums what
-// arrives: S (total) and P (sum over the lower ranks).  All threads call it.
-__device__ __forceinline__ void exchange_slice_sum(SharedState &sh, const Seq &s, int attempt,
-                                                   unsigned long long mine, unsigned long long &S,
-                                                   unsigned long long &P, bool &timed_out)
-{
-    cg::cluster_group cluster = cg::this_cluster();
-    const int tid = threadIdx.x;
-    if (tid < s.C)
-        *cluster.map_shared_rank(&sh.recv_sum[attempt][s.rank], tid) = mine;
-    cluster_sync_all();
-    S = 0;
-    P = 0;
-    timed_out = false;
-    for (int src = 0; src < s.C; ++src) {
-        const unsigned long long v = sh.recv_sum[attempt][src];
-        timed_out |= (v & kTimeoutFlag) != 0;
-        if (src < s.rank)
-            P += v & ~kTimeoutFlag;
-        S += v & ~kTimeoutFlag;
-    }
-}
 
 // The final uniform, clamped into [0, 1).
 __device__ __forceinline__ float final_uniform(const Params &p, const Seq &s)
@@ -1030,59 +1096,6 @@ __device__ __forceinline__ float final_uniform(const Params &p, const Seq &s)
     return u;
 }
 
-// Block-wide sum of a 64-bit value over all NW warps of the CTA (exact); every
-// thread gets the total.
-template <int NW>
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, SharedState &sh)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0)
-        sh.warp_sum[threadIdx.x >> 5] = v;
-    __syncthreads();
-    unsigned long long t = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-        t += sh.warp_sum[w];
-    return t;
-}
-
-// Inclusive scan of a 64-bit value over the kThreads reducing threads (exact);
-// also returns their total.  NAMED: the reducing threads are not the whole CTA
-// (ring kernel), so they meet at named barrier 1 instead of __syncthreads.
-template <bool NAMED>
-__device__ __forceinline__ unsigned long long reducers_scan_u64(unsigned long long v, unsigned long long &total,
-                                                                SharedState &sh)
-{
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o)
-            v += y;
-    }
-    if (NAMED)
-        reducers_sync();
-    else
-        __syncthreads();
-    if (lane == 31)
-        sh.warp_sum[wid] = v;
-    if (NAMED)
-        reducers_sync();
-    else
-        __syncthreads();
-    unsigned long long before = 0, t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        if (w < wid)
-            before += sh.warp_sum[w];
-        t += sh.warp_sum[w];
-    }
-    total = t;
-    return v + before;
-}
 
 // Number of rows sequence i reads: g + 1 target rows, plus g draft rows when
 // sampled; 0 for an invalid draft count.
@@ -1210,6 +1223,7 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
     s.point = POINT;
     s.drafts = s.sampled && !s.point;
     s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
+    s.temp = temp;
     s.rowlen = (size_t)p.V;
     return s;
 }
@@ -1222,21 +1236,17 @@ __device__ __forceinline__ Seq make_seq(const Params &p, int C, int rank, int b,
 // bytes are in flight while a batch is reduced (B=256, V=128256: 86.2 us
 // against 89.7 us without; prefetching across rows or two batches ahead was
 // slower).
-// STORE (sampled rows): each chunk's sum also goes to cs[tile * kThreads + tid],
-// relative to the warp's merged maximum once the row is done.
 // STAGE: every chunk of the slice is also kept in shared memory, stage[c - c0],
 // for a pass 2 that must not read the row again (rows in host memory).
-template <typename T, bool ALIGNED, bool STORE = false, bool STAGE = false>
-__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *cs = nullptr,
-                                             uint4 *stage = nullptr)
+template <typename T, bool ALIGNED, bool STAGE = false>
+__device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, uint4 *stage = nullptr)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
     RowAcc acc;
     acc.reset(s.c0 + tid < s.c1 ? (s.c0 + tid) * W : INT_MAX);
     const bool multi = ALIGNED && s.c1 - s.c0 > kUnroll * kThreads;
-    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
-    for (int ch = s.c0 + tid, j0 = 0; ch < s.c1; ch += kUnroll * kThreads, j0 += kUnroll) {
+    for (int ch = s.c0 + tid; ch < s.c1; ch += kUnroll * kThreads) {
         if (multi) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
@@ -1259,20 +1269,12 @@ __device__ __forceinline__ RowStat sweep_row(const Seq &s, const T *row, float *
                     stage[c - s.c0] = v[u];
             }
         }
-        if (STORE && s.sampled)
-            acc.add_soft_store<T, kUnroll>(v, s.k, cs + tid, j0, tiles);
-        else if (s.sampled)
+        if (s.sampled)
             acc.add_soft<T, kUnroll>(v, s.k);
         else
             acc.add_arg<T, kUnroll>(v, ch * W, kThreads * W);
     }
-    const RowStat w = warp_reduce(acc.stat(), s.sampled);
-    if (STORE && s.sampled) {  // this thread's entries, relative to the warp's maximum
-        const float sc = pow2_int(acc.m - w.m);
-        for (int j = 0; j < tiles; ++j)
-            cs[j * kThreads + tid] *= sc;
-    }
-    return w;
+    return warp_reduce(acc.stat(), s.sampled);
 }
 
 // Chunk c of a decided row's slice for pass 2: loaded from the row, or (STAGED)
@@ -1286,112 +1288,6 @@ __device__ __forceinline__ uint4 slice_chunk(const T *row, const uint4 *stage, i
         return load_chunk<T, ALIGNED>(row, c, s.V);
 }
 
-// The owner CTA's search for theta inside its slice (rel = theta - P, the
-// offset from the slice's start on the exact grid).  With 'keep', chunk_sums
-// holds the slice's chunk sums ([tile][lane]); otherwise the slice is scanned
-// tile by tile with reloads.  When rounding leaves rel at or beyond the slice's
-// own total (only on the bonus path, where the slice mass comes from the pass-1
-// partials), the last id of the slice with weight > 0 is taken.  All threads of
-// the CTA call it.
-template <typename T, bool ALIGNED, bool ZSET = false, bool STAGED = false>
-__device__ __forceinline__ void owner_search(const Params &p, SharedState &sh, const Seq &s, const T *trow, const T *drow,
-                             const WeightParams &wp, bool keep, const float *chunk_sums, unsigned long long rel,
-                             int32_t *outn, const uint4 *tst = nullptr, const uint4 *dst = nullptr)
-{
-    constexpr int W = Elem<T>::W;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
-    auto pick_at = [&](int c, unsigned long long r) {
-        const uint4 tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
-        const uint4 dv = wp.residual ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s) : tv;
-        float w[W];
-        chunk_weights<T, ZSET>(tv, dv, wp, w, c);
-        *outn = c * W + pick_in_chunk<T>(w, r);
-    };
-    if (keep) {
-        for (int j = wid; j < tiles; j += kWarps) {
-            unsigned long long t = 0;
-            for (int i = lane; i < kThreads; i += 32)
-                t += to_fixed60(chunk_sums[j * kThreads + i]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (lane == 0)
-                sh.tile_tot[j] = t;
-        }
-        __syncthreads();
-        unsigned long long before = 0;
-        int jt = -1;
-        for (int j = 0; j < tiles; ++j) {
-            if (rel < before + sh.tile_tot[j]) {
-                jt = j;
-                break;
-            }
-            before += sh.tile_tot[j];
-        }
-        if (jt >= 0) {
-            const unsigned long long f = to_fixed60(chunk_sums[jt * kThreads + tid]);
-            unsigned long long total;
-            const unsigned long long start = before + reducers_scan_u64<false>(f, total, sh) - f;
-            if (start <= rel && rel < start + f)
-                pick_at(s.c0 + jt * kThreads + tid, rel - start);
-            return;
-        }
-        // rel beyond the slice's chunk total: the last chunk with weight > 0
-        int last = -1;
-        for (int i = tid; i < tiles * kThreads; i += kThreads)
-            if (chunk_sums[i] > 0.0f)
-                last = i;
-        const int c_last = __reduce_max_sync(0xffffffffu, last);
-        if (lane == 0)
-            sh.cnt[wid] = c_last;
-        __syncthreads();
-        if (tid == 0) {
-            int m = -1;
-            for (int w = 0; w < kWarps; ++w)
-                m = max(m, sh.cnt[w]);
-            if (m >= 0)
-                pick_at(s.c0 + m, ~0ull);  // pick_in_chunk returns the last positive element
-        }
-        return;
-    }
-    // slice too large for shared memory: tiles in order, reloaded
-    unsigned long long carry = 0;
-    int last = -1;
-    for (int base = s.c0; base < s.c1; base += kThreads) {
-        const int c = base + tid;
-        float w[W];
-        unsigned long long sigma = 0;
-        if (c < s.c1) {
-            const uint4 tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
-            const uint4 dv = wp.residual ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s) : tv;
-            chunk_weights<T, ZSET>(tv, dv, wp, w, c);
-            sigma = chunk_fixed<T>(w);
-            if (chunk_sum<T>(w) > 0.0f)
-                last = c;
-        }
-        unsigned long long total;
-        const unsigned long long incl = reducers_scan_u64<false>(sigma, total, sh);
-        const unsigned long long start = carry + incl - sigma;
-        if (c < s.c1 && start <= rel && rel < start + sigma)
-            *outn = c * W + pick_in_chunk<T>(w, rel - start);
-        carry += total;
-        if (rel < carry)
-            return;
-    }
-    const int c_last = __reduce_max_sync(0xffffffffu, last);
-    __syncthreads();
-    if (lane == 0)
-        sh.cnt[wid] = c_last;
-    __syncthreads();
-    if (tid == 0) {
-        int m = -1;
-        for (int w = 0; w < kWarps; ++w)
-            m = max(m, sh.cnt[w]);
-        if (m >= 0)
-            pick_at(m, ~0ull);
-    }
-}
 
 // Pass 1 when every thread holds at most K chunks of each row (small slices:
 // small vocabularies or large clusters): the loads of U/K rows are issued
@@ -1435,142 +1331,804 @@ __device__ __forceinline__ void sweep_rows_batched(const Params &p, SharedState 
     }
 }
 
-// Inverse-CDF sample of one decided row across the cluster (pass 2).  The
-// weights are wp's: max(0, p - q) with q from drow, p, or p without some ids.
-// bonus: the weights are p itself, so CTA c's slice mass is its pass-1 partial
-// parts[c * stride] over the row's merged statistics tot, already known to
-// every CTA; only the owner reads its slice again and nothing crosses the
-// cluster.  Otherwise every CTA sums its slice's weights (pass 2a, chunk sums
-// kept in shared memory), the slice sums cross the cluster, and the CTA whose
-// slice holds floor(u*S) searches it.  A zero total (unreachable in exact
-// arithmetic) samples p instead.  All threads of the CTA call it; the
-// cluster's CTAs call it together.  mass_out (rank 0, may be NULL) receives S.
-// STAGED: the slices of trow and drow are read from the shared-memory copies
-// tst and dst that pass 1 made (sweep_row with STAGE), never from the rows.
-template <typename T, bool ALIGNED, bool ZSET, bool STAGED = false>
-__device__ __forceinline__ void sample_row(const Params &p, SharedState &sh, const Seq &s, const T *trow,
-                                           const T *drow, WeightParams wp, bool bonus, const RowStat &tot,
-                                           const RowStat *parts, int stride, float u, int32_t *outn,
-                                           float *mass_out, const RowStat *stored = nullptr,
-                                           const uint4 *tst = nullptr, const uint4 *dst = nullptr)
+
+// Warp w's contiguous range [r0, r1) of this CTA's slice.
+__device__ __forceinline__ void warp_range(const Seq &s, int w, int &r0, int &r1)
+{
+    const long long n = s.c1 - s.c0;
+    r0 = s.c0 + (int)(n * w / kWarps);
+    r1 = s.c0 + (int)(n * (w + 1) / kWarps);
+}
+
+// Sums of one warp range (every lane gets them): JT = sum over J of the target
+// weights, JD = of the draft weights, AT, AD = over all ids.
+struct RangeSums {
+    unsigned long long jt, jd, at, ad;
+};
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Pass-2 sweep of this warp's range: chunks base + u*32 + lane, kP2Unroll
+// chunks in flight per thread (U per row).  After the fast pass over a batch,
+// its heavy ids are queued (slot, lane, id, J) and spread over the lanes, 32
+// exact weights at a time, while the batch's chunks wait in shared memory.
+// All threads of the warp call it.
+template <typename T, bool ALIGNED, bool RESID, bool STAGED>
+__device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const T *drow, const uint4 *tst,
+                                              const uint4 *dst, const P2Seq &ps, P2Smem &sm)
+{
+    constexpr int U = RESID ? kP2Slots / 2 : kP2Slots;  // chunks per row in a batch
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int r0, r1;
+    warp_range(s, wid, r0, r1);
+    unsigned long long jt = 0, jd = 0, hat = 0, had = 0;
+    float ath = 0.0f, atl = 0.0f, adh = 0.0f, adl = 0.0f;
+    for (int base = r0; base < r1; base += 32 * U) {
+        int queued = 0;  // heavy ids of this batch (uniform over the warp)
+        {
+            uint4 tv[U], dv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = base + u * 32 + lane;
+                tv[u] = c < r1 ? slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s) : neg_inf_chunk<T>();
+                dv[u] = (RESID && c < r1) ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s) : neg_inf_chunk<T>();
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (base + u * 32 >= r1)
+                    break;  // uniform over the warp
+                const int c = base + u * 32 + lane;
+                float runt[Elem<T>::W], rund[Elem<T>::W];
+                const ChunkP2 o = p2_chunk<T, RESID>(tv[u], dv[u], c, ps, runt, rund);
+                jt += to_fixed60(o.jt);
+                compensated_add(ath, atl, o.at);
+                if (RESID) {
+                    jd += to_fixed60(o.jd);
+                    compensated_add(adh, adl, o.ad);
+                }
+                if (!__any_sync(0xffffffffu, o.heavy != 0))
+                    continue;
+                const int slot = RESID ? 2 * u : u;
+                sm.stage[wid][slot][lane] = tv[u];
+                if (RESID)
+                    sm.stage[wid][slot + 1][lane] = dv[u];
+                const int cnt = __popc(o.heavy);
+                int incl = cnt;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d)
+                        incl += y;
+                }
+                int off = queued + incl - cnt;
+                queued += __shfl_sync(0xffffffffu, incl, 31);
+                for (uint32_t hm = o.heavy; hm; hm &= hm - 1u) {
+                    const int bit = __ffs(hm) - 1, e = bit & 7;
+                    sm.queue[wid][off++] = (unsigned short)((slot + (bit >> 3)) | (lane << 3) | (e << 8) |
+                                                            (((o.inj >> e) & 1u) << 11));
+                }
+            }
+        }
+        if (!queued)
+            continue;
+        __syncwarp();
+        for (int k = lane; k < queued; k += 32) {
+            const unsigned ent = sm.queue[wid][k];
+            const int slot = ent & 7;
+            const bool row = RESID && (slot & 1);
+            const float l = staged_elem<T>(&sm.stage[wid][slot][(ent >> 3) & 31], (ent >> 8) & 7);
+            const unsigned long long w = exact_weight(l, row ? ps.rd : ps.rt);
+            const bool inj = (ent >> 11) & 1u;
+            if (row) {
+                had += w;
+                jd += inj ? w : 0ull;
+            } else {
+                hat += w;
+                jt += inj ? w : 0ull;
+            }
+        }
+        __syncwarp();
+    }
+    RangeSums r;
+    r.jt = warp_sum_u64(jt);
+    r.jd = warp_sum_u64(jd);
+    r.at = warp_sum_u64(hat + (unsigned long long)((long long)to_fixed60(ath) + fixed60_signed(atl)));
+    r.ad = warp_sum_u64(had + (unsigned long long)((long long)to_fixed60(adh) + fixed60_signed(adl)));
+    return r;
+}
+
+// Signed 128-bit value as a double (diagnostics only).
+__device__ __forceinline__ double i128_to_double(i128 v)
+{
+    const bool neg = v < 0;
+    const u128 m = neg ? (u128)(-v) : (u128)v;
+    const double d = (double)(unsigned long long)(m >> 64) * 18446744073709551616.0 + (double)(unsigned long long)m;
+    return neg ? -d : d;
+}
+
+// The owner CTA's search inside warp range [r0, r1) of its slice, which holds
+// the draw (rel = theta - start of the range, on the exact grid).  The range is
+// recomputed chunk by chunk with the sweep's arithmetic (identical bits), one
+// chunk per thread and pass; a block scan finds the chunk, its thread the id
+// from the running sums in id order.  All threads of the CTA call it.
+template <typename T, bool ALIGNED, bool RESID, bool STAGED>
+__device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, const T *trow, const T *drow,
+                                      const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0, int r1, i128 rel,
+                                      unsigned long long A, unsigned long long B, int32_t *outn)
 {
     constexpr int W = Elem<T>::W;
     const int tid = threadIdx.x;
-    const int rank = s.rank;
-    extern __shared__ float chunk_sums[];  // [scan_tiles][kThreads]
-    const int tiles = (s.c1 - s.c0 + kThreads - 1) / kThreads;
-    const bool keep = tiles <= p.scan_tiles;
-    constexpr int U2 = kUnroll / 2;
-    // chunk c = c0 + j*kThreads + tid is tile j, lane tid; returns the thread's fixed-point total
-    auto slice_sums = [&]() {
-        unsigned long long acc = 0;
-        for (int j0 = 0; j0 < tiles; j0 += U2) {
-            uint4 tv[U2], dv[U2];
-#pragma unroll
-            for (int u = 0; u < U2; ++u) {
-                const int c = s.c0 + (j0 + u) * kThreads + tid;
-                tv[u] = c < s.c1 ? slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s) : neg_inf_chunk<T>();
-                dv[u] = (wp.residual && c < s.c1) ? slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s)
-                                                  : neg_inf_chunk<T>();
+    i128 carry = 0;
+    for (int base = r0; base < r1; base += kThreads) {
+        const int c = base + tid;
+        uint4 tv = neg_inf_chunk<T>(), dv = neg_inf_chunk<T>();
+        float runt[W], rund[W];
+        ChunkP2 o{0.0f, 0.0f, 0.0f, 0.0f, 0u, 0u};
+        i128 v = 0;
+        if (c < r1) {
+            tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
+            if (RESID)
+                dv = slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s);
+            o = p2_chunk<T, RESID>(tv, dv, c, ps, runt, rund);
+            unsigned long long jt = to_fixed60(o.jt), jd = RESID ? to_fixed60(o.jd) : 0ull;
+            for (uint32_t hm = o.heavy; hm; hm &= hm - 1u) {
+                const int bit = __ffs(hm) - 1, e = bit & 7;
+                if (!((o.inj >> e) & 1u))
+                    continue;
+                if (bit >> 3)
+                    jd += exact_weight(elem<T>(dv, e), ps.rd);
+                else
+                    jt += exact_weight(elem<T>(tv, e), ps.rt);
             }
+            v = RESID ? p2_value(jt, jd, A, B) : (i128)jt;
+        }
+        i128 total;
+        const i128 incl = block_scan_i128(v, total, scan_tmp);
+        const int first = block_first(c < r1 && carry + incl > rel, wmin);
+        if (first < kThreads) {
+            // the warp holding that chunk finds the id: lane e (< W) holds id e's
+            // running sums, lanes e and W + e its exact weights (if heavy, in J)
+            if ((first >> 5) == (tid >> 5)) {
+                const int src = first & 31, lane = tid & 31, e = lane & (W - 1), row = lane / W;
+                const i128 off = rel - (carry + incl - v);  // 0 <= off < v in the source lane
+                const long long off_hi = __shfl_sync(0xffffffffu, (long long)(off >> 64), src);
+                const unsigned long long off_lo = __shfl_sync(0xffffffffu, (unsigned long long)off, src);
+                const i128 off_s = (i128)(((u128)(unsigned long long)off_hi << 64) | off_lo);
+                uint4 t2, d2;
+                t2.x = __shfl_sync(0xffffffffu, tv.x, src);
+                t2.y = __shfl_sync(0xffffffffu, tv.y, src);
+                t2.z = __shfl_sync(0xffffffffu, tv.z, src);
+                t2.w = __shfl_sync(0xffffffffu, tv.w, src);
+                d2.x = __shfl_sync(0xffffffffu, dv.x, src);
+                d2.y = __shfl_sync(0xffffffffu, dv.y, src);
+                d2.z = __shfl_sync(0xffffffffu, dv.z, src);
+                d2.w = __shfl_sync(0xffffffffu, dv.w, src);
+                const uint32_t heavy = __shfl_sync(0xffffffffu, o.heavy, src);
+                const uint32_t inj = __shfl_sync(0xffffffffu, o.inj, src);
+                float rt_e = 0.0f, rd_e = 0.0f;
 #pragma unroll
-            for (int u = 0; u < U2; ++u) {
-                const int c = s.c0 + (j0 + u) * kThreads + tid;
-                float sum = 0.0f;
-                if (c < s.c1) {
-                    float w[W];
-                    chunk_weights<T, ZSET>(tv[u], dv[u], wp, w, c);
-                    sum = chunk_sum<T>(w);
-                    acc += to_fixed60(sum);
+                for (int k = 0; k < W; ++k) {
+                    const float x = __shfl_sync(0xffffffffu, runt[k], src);
+                    const float y = __shfl_sync(0xffffffffu, rund[k], src);
+                    if (e == k) {
+                        rt_e = x;
+                        rd_e = y;
+                    }
                 }
-                if (keep && j0 + u < tiles)
-                    chunk_sums[(j0 + u) * kThreads + tid] = sum;
+                unsigned long long wv = 0;
+                if (row < 2 && ((inj >> e) & 1u) && ((heavy >> (row * 8 + e)) & 1u))
+                    wv = exact_weight(elem<T>(row ? d2 : t2, e), row ? ps.rd : ps.rt);
+                // running sums of the exact weights in id order, per row (groups of W lanes)
+#pragma unroll
+                for (int d = 1; d < W; d <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, wv, d, W);
+                    if (e >= d)
+                        wv += y;
+                }
+                const unsigned long long pd = __shfl_sync(0xffffffffu, wv, W + e);
+                const unsigned long long at = to_fixed60(rt_e) + wv;
+                const i128 cum = RESID ? p2_value(at, to_fixed60(rd_e) + pd, A, B) : (i128)at;
+                const unsigned hit = __ballot_sync(0xffffffffu, lane < W && off_s < cum);
+                if (lane == 0)
+                    *outn = (base + first) * W + (hit ? __ffs(hit) - 1 : W - 1);  // chunk base + first
             }
+            return;
         }
-        return acc;
-    };
-
-    if (bonus) {
-        const float z = tot.hi + tot.lo;
-        unsigned long long S = 0, P = 0, mine = 0;
-        for (int c = 0; c < s.C; ++c) {
-            const RowStat part = parts[c * stride];
-            const float share = (part.hi + part.lo) * pow2_int(part.m - tot.m) / z;
-            const unsigned long long f = to_fixed60(fminf(fmaxf(share, 0.0f), 8.0f));
-            if (c < rank)
-                P += f;
-            if (c == rank)
-                mine = f;
-            S += f;
-        }
-        if (rank == 0 && tid == 0 && mass_out)
-            *mass_out = (float)S * kFixedUnit;
-        const unsigned long long theta = scaled_floor(u, S);
-        if (S == 0 || !(P <= theta && theta < P + mine))
-            return;  // another CTA owns the sample
-        if (keep) {
-            if (stored) {  // pass 1 kept the chunk sums: scale them to p
-                const float f = pow2_int(stored[threadIdx.x >> 5].m - tot.m) / z;
-                for (int j = 0; j < tiles; ++j)
-                    chunk_sums[j * kThreads + tid] *= f;
-            } else {
-                slice_sums();
-            }
-            __syncthreads();
-        }
-        owner_search<T, ALIGNED, ZSET, STAGED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn, tst,
-                                                 dst);
-        return;
+        carry += total;
     }
-
-    unsigned long long S = 0, P = 0, mine = 0;
-    bool timed_out = false;
-    bool use_weights = true;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        mine = block_sum_u64<kWarps>(slice_sums(), sh);
-        exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
-        if (S > 0 || !use_weights)
-            break;
-        use_weights = false;  // degenerate residual (unreachable in exact arithmetic): sample p
-        wp.residual = false;
-        wp.zero_at = -1;
-        wp.zero_chunk = -1;
-        wp.nz = 0;
-    }
-    if (rank == 0 && tid == 0 && mass_out)
-        *mass_out = (float)S * kFixedUnit;
-    const unsigned long long theta = scaled_floor(u, S);  // pick: C_{j-1} <= theta < C_j
-    if (S == 0 || !(P <= theta && theta < P + mine))
-        return;  // another CTA owns the sample (S == 0 only for an all-zero row)
-    owner_search<T, ALIGNED, ZSET, STAGED>(p, sh, s, trow, drow, wp, keep, chunk_sums, theta - P, outn, tst,
-                                                 dst);
+    if (tid == 0)
+        *outn = -1;  // unreachable: the range's exact total exceeds rel
 }
 
-// Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n
-// (sh.row holds the merged statistics of rows t_n and, if n < g, d_n; parts
-// [c * stride] is CTA c's pass-1 partial of row t_n): the residual row after a
-// rejection (max(0, p - q), or p without x_n for point-mass drafts), the bonus
-// row t_g otherwise.
-// stored: the row's pass-1 warp partials when pass 1 kept its chunk sums (the sampler).
-// STAGED: tst and dst hold this CTA's slices of rows t_n and d_n (early exit
-// with rows in host memory), so pass 2 reads neither row again.
-template <typename T, bool ALIGNED, bool STAGED = false>
-__device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, const Seq &s, int n, const RowStat *parts,
-                             int stride, const RowStat *stored = nullptr, const uint4 *tst = nullptr,
-                             const uint4 *dst = nullptr)
+// Pass 2 of one sequence across its cluster: the inverse-CDF draw with uniform
+// u from the weights ps describes, into *outn.  Every CTA sweeps its slice
+// (p2_sweep), the CTA totals cross the cluster over DSMEM, and the CTA whose
+// slice holds floor(u * R) searches one warp range of it.  A total R of 0 (a
+// residual with no mass, unreachable in exact arithmetic, or p without ids
+// that hold all of it) samples p instead.  mass_out (rank 0; may be NULL):
+// the normalised total (residual mass, or 1 - p(removed ids)).  All threads
+// of every CTA of the cluster call it.
+template <typename T, bool ALIGNED, bool STAGED>
+__device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T *trow, const T *drow,
+                                          const uint4 *tst, const uint4 *dst, P2Seq ps, float u, int32_t *outn,
+                                          float *mass_out)
 {
-    constexpr int W = Elem<T>::W;
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
+    P2Smem &sm = *reinterpret_cast<P2Smem *>(dyn_smem);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    unsigned long long A = 0, B = 1;
+    i128 R = 0;
+    int att = 0;
+    bool resid = false;
+    for (;; ++att) {
+        resid = ps.mode == kP2Residual;
+        const RangeSums r = resid ? p2_sweep<T, ALIGNED, true, STAGED>(s, trow, drow, tst, dst, ps, sm)
+                                  : p2_sweep<T, ALIGNED, false, STAGED>(s, trow, drow, tst, dst, ps, sm);
+        if (lane == 0) {
+            sh.p2w[wid][0] = r.jt;
+            sh.p2w[wid][1] = r.jd;
+            sh.p2w[wid][2] = r.at;
+            sh.p2w[wid][3] = r.ad;
+        }
+        __syncthreads();
+        if (tid < 4) {
+            unsigned long long v = 0;
+            for (int w = 0; w < kWarps; ++w)
+                v += sh.p2w[w][tid];
+            for (int d = 0; d < s.C; ++d)
+                *cluster.map_shared_rank(&sh.p2recv[att][s.rank][tid], d) = v;
+        }
+        cluster_sync_all();
+        A = 0;
+        B = 0;
+        for (int src = 0; src < s.C; ++src) {
+            A += sh.p2recv[att][src][2];
+            B += sh.p2recv[att][src][3];
+        }
+        if (!resid)
+            B = 1;
+        R = 0;
+        for (int src = 0; src < s.C; ++src)
+            R += p2_value(sh.p2recv[att][src][0], resid ? sh.p2recv[att][src][1] : 0ull, A, B);
+        if (R > 0 || att == 1)
+            break;
+        ps.mode = kP2Full;  // no mass: sample p of the target row
+        ps.nz = 0;
+        ps.zero_at = -1;
+        ps.zero_chunk = -1;
+    }
+    if (mass_out && s.rank == 0 && tid == 0)
+        *mass_out = (float)(resid ? i128_to_double(R) / ((double)A * (double)B) : i128_to_double(R) / (double)A);
+    if (R <= 0)
+        return;  // nothing to draw from
+    const i128 theta = scaled_floor128(u, R);  // the draw: first weight whose running sum passes theta
+    // the rank whose slice holds it
+    i128 before = 0;
+    int owner = s.C - 1;
+    for (int src = 0; src < s.C; ++src) {
+        const i128 v = p2_value(sh.p2recv[att][src][0], resid ? sh.p2recv[att][src][1] : 0ull, A, B);
+        if (theta < before + v) {
+            owner = src;
+            break;
+        }
+        before += v;
+    }
+    if (owner != s.rank)
+        return;
+    // the warp range inside the slice
+    i128 rel = theta - before;
+    int w = kWarps - 1;
+    for (int k = 0; k < kWarps; ++k) {
+        const i128 v = p2_value(sh.p2w[k][0], resid ? sh.p2w[k][1] : 0ull, A, B);
+        if (rel < v) {
+            w = k;
+            break;
+        }
+        rel -= v;
+    }
+    int r0, r1;
+    warp_range(s, w, r0, r1);
+    if (resid)
+        p2_owner<T, ALIGNED, true, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
+    else
+        p2_owner<T, ALIGNED, false, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
+}
+
+// Pass-2 weights of a chain sequence whose cut is n (sh.row holds the merged
+// statistics of rows t_n and, if n < g, d_n): the residual row after a
+// rejection (max(0, p - q), or p without x_n for point-mass drafts), the
+// bonus row t_g otherwise.
+template <typename T>
+__device__ __forceinline__ P2Seq chain_p2seq(const SharedState &sh, const Seq &s, int n)
+{
+    const int g = s.g;
+    const bool rejected = n < g;
+    const bool rows = rejected && s.drafts;
+    P2Seq ps;
+    ps.rt = exact_row(sh.row[n], s.temp);
+    ps.rd = rows ? exact_row(sh.row[g + 1 + n], s.temp) : ps.rt;
+    ps.mode = !rejected ? kP2Full : rows ? kP2Residual : kP2Zero;
+    ps.zero_at = (rejected && !s.drafts) ? sh.drafted[n] : -1;
+    ps.zero_chunk = ps.zero_at >= 0 ? ps.zero_at / Elem<T>::W : -1;
+    ps.zset = nullptr;
+    ps.nz = 0;
+    return ps;
+}
+
+// Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n.
+// With a workspace, rank 0 only appends the sequence's record for
+// any CTA's pass-2 tasks.  Otherwise the cluster samples here; STAGED: tst and dst
+// hold this CTA's slices of rows t_n and d_n (early exit with rows in host
+// memory), so pass 2 reads neither row again.
+template <typename T, bool ALIGNED, bool STAGED = false>
+__device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, const Seq &s, int n,
+                                            const uint4 *tst = nullptr, const uint4 *dst = nullptr)
+{
     const int g = s.g, b = s.b;
-    const bool residual = n < g;
+    const bool rows = n < g && s.drafts;
+    const P2Seq ps = chain_p2seq<T>(sh, s, n);
     const T *trow = row_ptr<T>(p, s, n);
-    const T *drow = (residual && s.drafts) ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    const int xn = (residual && !s.drafts) ? sh.drafted[n] : -1;  // point mode only
-    const WeightParams wp = weight_params(sh, s, n, residual, xn, W);
+    const T *drow = rows ? row_ptr<T>(p, s, g + 1 + n) : trow;
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
-    sample_row<T, ALIGNED, false, STAGED>(p, sh, s, trow, drow, wp, !residual, sh.row[n], parts, stride,
-                                          final_uniform(p, s), outn, p.resid_mass ? p.resid_mass + b : nullptr,
-                                          residual ? nullptr : stored, tst,
-                                          (residual && s.drafts) ? dst : tst);
+    float *mass = p.resid_mass ? p.resid_mass + b : nullptr;
+    if (!STAGED && p.ws) {
+        if (s.rank == 0 && threadIdx.x == 0)
+            p2_publish(p, p2_append(p, ps, trow, drow, outn, mass, final_uniform(p, s)));
+        return;
+    }
+    pass2_sample<T, ALIGNED, STAGED>(sh, s, trow, drow, tst, rows ? dst : tst, ps, final_uniform(p, s), outn, mass);
+}
+
+// ===========================================================================
+// Pass 2 as tasks for any CTA (when the caller gives a workspace)
+// ===========================================================================
+// Pass 2 of a sequence is a sweep of its decided row (two rows for a residual)
+// with the exact weights above: several times the ALU work of pass 1's
+// reduction of the same bytes.  Done by the sequence's own cluster after its
+// pass 1, the last clusters' pass 2 becomes the grid's tail while most SMs
+// idle.  With a workspace, rank 0 of each sampled, valid sequence instead
+// appends a P2Record (decided rows, weight scales, uniform, output slot) and
+// marks it ready; every CTA, once its own sequence is decided, becomes a
+// worker that takes slice tasks (record e, slice k) from the workspace.  A
+// task sweeps its slice as a cluster CTA would (p2_sweep), stores the
+// per-warp-range sums and counts itself done with an atomic; the task that
+// completes a record (the last arriver: no CTA waits for another's result)
+// adds the sums in slice and warp order, finds the slice and warp range that
+// hold floor(u*R), recomputes that range (p2_owner) and writes the token.  The
+// results are the one-kernel path's: the same integer weights, summed exactly.
+// A worker with no task to take waits for one only once every cluster of the
+// grid has started (so it holds no SM slot that an unscheduled cluster needs),
+// polling with a backoff and a wall-time limit (kWorkerWaitNs: it then gives
+// up and sets SPEC_STATUS_TIMEOUT); it leaves when every sequence is decided
+// and every task handed out.  Waits never form a cycle: tasks come from CTAs
+// that are streaming or deciding, which never wait.
+constexpr unsigned long long kWorkerWaitNs = 200000000ull;  // 0.2 s
+
+struct P2Record {
+    const void *trow;   // decided target row
+    const void *drow;   // its draft row (residual), else trow
+    int32_t *out;       // the token's slot in out_tokens
+    float *mass;        // resid_mass slot, or NULL
+    ExactRow rt, rd;
+    float u;            // the final uniform
+    int mode;           // P2Mode
+    int zero_at;        // kP2Zero: a removed id (-1: none)
+    int nz;             // kP2Zero: ids in the record's zero set (tree walks)
+};
+
+// Workspace layout: [count][counters[B]] (zeroed before each call), records,
+// per record, slice and warp range the four sums, and (tree walks) each
+// record's zero set.
+// Counters at the start of the workspace (zeroed before each call).
+struct WsHeader {
+    unsigned count;     // records appended
+    unsigned taken;     // slice tasks handed out
+    unsigned decided;   // sequences decided (every kind)
+    unsigned started;   // clusters started
+};
+
+struct WsLayout {
+    size_t counters, ready, records, sums, zsets, total;
+};
+__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
+__host__ __device__ inline WsLayout ws_layout(int B, int S2, bool tree)
+{
+    WsLayout L;
+    L.counters = 256;
+    L.ready = ws_align(L.counters + 4 * (size_t)B);
+    L.records = ws_align(L.ready + 4 * (size_t)B);
+    L.sums = ws_align(L.records + sizeof(P2Record) * (size_t)B);
+    L.zsets = ws_align(L.sums + 32 * (size_t)kWarps * (size_t)S2 * (size_t)B);
+    L.total = ws_align(L.zsets + (tree ? 4 * (size_t)kMaxTree * (size_t)B : 0));
+    return L;
+}
+// Bytes zeroed before each call: the header, the per-record counters and ready flags.
+__host__ __device__ inline size_t ws_zeroed(int B) { return ws_layout(B, 1, false).records; }
+
+// Rank 0, thread 0: appends sequence b's pass 2 as a record (index returned);
+// p2_publish marks it ready once the record (and a tree's zero set) is written.
+__device__ __forceinline__ int p2_append(const Params &p, const P2Seq &ps, const void *trow, const void *drow,
+                                         int32_t *outn, float *mass, float u)
+{
+    const WsLayout L = ws_layout(p.B, p.ws_s2, p.parent != nullptr);
+    const int e = (int)atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->count, 1u);
+    P2Record &r = reinterpret_cast<P2Record *>(p.ws + L.records)[e];
+    r.trow = trow;
+    r.drow = drow;
+    r.out = outn;
+    r.mass = mass;
+    r.rt = ps.rt;
+    r.rd = ps.rd;
+    r.u = u;
+    r.mode = ps.mode;
+    r.zero_at = ps.zero_at;
+    r.nz = ps.nz;
+    return e;
+}
+
+__device__ __forceinline__ void p2_publish(const Params &p, int e)
+{
+    const WsLayout L = ws_layout(p.B, p.ws_s2, p.parent != nullptr);
+    __threadfence();  // the record is visible before its flag
+    atomicExch(reinterpret_cast<unsigned *>(p.ws + L.ready) + e, 1u);
+}
+
+// One sequence decided (rank 0, thread 0, after publishing its record if any).
+__device__ __forceinline__ void p2_decided(const Params &p)
+{
+    __threadfence();
+    atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->decided, 1u);
+}
+
+struct P2Launch {
+    unsigned char *ws;
+    int B, S2, num_chunks, V;
+    int tree;  // records carry zero sets
+};
+
+struct P2Shared {
+    P2Record rec;
+    int zset[kMaxTree];
+    unsigned long long w[kWarps][4];
+    unsigned long long sl[kWarps][4];  // finisher: partial sums of slices, per warp
+    i128 scan[kWarps];
+    i128 rel;
+    int wmin[kWarps];
+    int owner, wr;
+    int last;
+    int task, state;
+};
+// Dynamic shared memory of a CTA that runs pass-2 tasks.
+constexpr int kWorkerSmemBytes = (int)(((sizeof(P2Smem) + 15) & ~(size_t)15) + sizeof(P2Shared));
+
+// Slice k of S2 over the row's chunks, as a Seq for p2_sweep / p2_owner.
+__device__ __forceinline__ Seq p2_slice(const P2Launch &q, int k)
+{
+    Seq s;
+    s.b = 0;
+    s.g = 0;
+    s.gmax = 0;
+    s.V = q.V;
+    s.rank = k;
+    s.C = q.S2;
+    s.c0 = (int)((long long)q.num_chunks * k / q.S2);
+    s.c1 = (int)((long long)q.num_chunks * (k + 1) / q.S2);
+    s.sampled = true;
+    s.point = false;
+    s.drafts = false;
+    s.k = 0.0f;
+    s.temp = 0.0f;
+    s.rowlen = (size_t)q.V;
+    return s;
+}
+
+template <typename T, bool ALIGNED>
+__device__ __forceinline__ RangeSums p2_task_sweep(const P2Launch &q, const P2Shared &sh, const P2Seq &ps, int k,
+                                                   P2Smem &sm)
+{
+    const Seq s = p2_slice(q, k);
+    const T *trow = reinterpret_cast<const T *>(sh.rec.trow);
+    const T *drow = reinterpret_cast<const T *>(sh.rec.drow);
+    return ps.mode == kP2Residual ? p2_sweep<T, ALIGNED, true, false>(s, trow, drow, nullptr, nullptr, ps, sm)
+                                  : p2_sweep<T, ALIGNED, false, false>(s, trow, drow, nullptr, nullptr, ps, sm);
+}
+
+// The task that completed record e: totals, the draw, the owner range, the id.
+// Thread t < S2 * kWarps loads the sums of (slice t / kWarps, warp range
+// t % kWarps), so every load is issued at once.
+template <typename T, bool ALIGNED>
+__device__ __noinline__ void p2_finish(const P2Launch &q, P2Shared &sh, P2Seq ps, const unsigned long long *sums,
+                                       P2Smem &sm)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int S2 = q.S2, G = S2 * kWarps;  // G <= kThreads (S2 <= 32)
+    bool resid = ps.mode == kP2Residual;
+    unsigned long long v[4] = {0ull, 0ull, 0ull, 0ull};
+    if (tid < G) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = __ldcg(sums + (size_t)tid * 4 + j);  // written by other CTAs: read past L1
+    }
+    // totals: exact, so the order of the additions does not matter
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const unsigned long long t = warp_sum_u64(v[j]);
+        if (lane == 0)
+            sh.sl[wid][j] = t;
+    }
+    __syncthreads();
+    unsigned long long tot[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        for (int w = 0; w < kWarps; ++w)
+            tot[j] += sh.sl[w][j];
+    unsigned long long A = tot[2], B = resid ? tot[3] : 1ull;
+    i128 R = p2_value(tot[0], resid ? tot[1] : 0ull, A, B);
+    const bool fallback = R <= 0;
+    int owner = S2 - 1, wr = kWarps - 1;
+    i128 rel = 0;
+    if (!fallback) {
+        // each group's value, then the slice and warp range holding theta, in order
+        const i128 gv = tid < G ? p2_value(v[0], resid ? v[1] : 0ull, A, B) : (i128)0;
+        __syncthreads();  // sh.sl is read above
+        const i128 theta = scaled_floor128(sh.rec.u, R);
+        i128 total;
+        const i128 incl = block_scan_i128(gv, total, sh.scan);
+        const int first = block_first(tid < G && incl > theta, sh.wmin);
+        if (tid == first) {
+            sh.rel = theta - (incl - gv);
+            sh.owner = tid / kWarps;
+            sh.wr = tid % kWarps;
+        }
+        __syncthreads();
+        if (first < kThreads) {
+            rel = sh.rel;
+            owner = sh.owner;
+            wr = sh.wr;
+        }
+        __syncthreads();
+    } else {
+        // no mass (unreachable in exact arithmetic for a residual): sample p,
+        // sweeping every slice again here with J = all ids
+        ps.mode = kP2Full;
+        ps.nz = 0;
+        ps.zero_at = -1;
+        ps.zero_chunk = -1;
+        resid = false;
+        B = 1;
+        unsigned long long total = 0;
+        for (int k = 0; k < S2; ++k) {
+            const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
+            if (lane == 0)
+                sh.w[wid][0] = r.jt;
+            __syncthreads();
+            for (int w = 0; w < kWarps; ++w)
+                total += sh.w[w][0];
+            __syncthreads();
+        }
+        A = total;
+        R = (i128)A;
+        const i128 theta = scaled_floor128(sh.rec.u, R);
+        i128 before = 0;
+        for (int k = 0; k < S2; ++k) {  // the owner slice, then its warp range
+            const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
+            if (lane == 0)
+                sh.w[wid][0] = r.jt;
+            __syncthreads();
+            i128 sv = 0;
+            for (int w = 0; w < kWarps; ++w)
+                sv += (i128)sh.w[w][0];
+            if (theta < before + sv || k == S2 - 1) {
+                owner = k;
+                rel = theta - before;
+                for (int w = 0; w < kWarps; ++w) {
+                    wr = w;
+                    if (rel < (i128)sh.w[w][0])
+                        break;
+                    if (w < kWarps - 1)
+                        rel -= (i128)sh.w[w][0];
+                }
+                break;
+            }
+            before += sv;
+            __syncthreads();
+        }
+        __syncthreads();
+    }
+    if (sh.rec.mass && tid == 0)
+        *sh.rec.mass = (float)(resid ? i128_to_double(R) / ((double)A * (double)B) : i128_to_double(R) / (double)A);
+    if (R <= 0) {
+        if (tid == 0)
+            *sh.rec.out = -1;  // an all-zero row: nothing to draw from (not reachable for a valid row)
+        return;
+    }
+    const Seq s = p2_slice(q, owner);
+    int r0, r1;
+    warp_range(s, wr, r0, r1);
+    const T *trow = reinterpret_cast<const T *>(sh.rec.trow);
+    const T *drow = reinterpret_cast<const T *>(sh.rec.drow);
+    if (resid)
+        p2_owner<T, ALIGNED, true, false>(sh.scan, sh.wmin, s, trow, drow, nullptr, nullptr, ps, r0, r1, rel, A, B,
+                                          sh.rec.out);
+    else
+        p2_owner<T, ALIGNED, false, false>(sh.scan, sh.wmin, s, trow, drow, nullptr, nullptr, ps, r0, r1, rel, A, B,
+                                           sh.rec.out);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One slice task: record t / S2, slice t % S2.  The record's writer may still
+// be filling it: its ready flag is awaited first (bounded).  False when that
+// wait ran out.  All threads of the CTA call it.
+template <typename T, bool ALIGNED>
+__device__ __forceinline__ bool p2_run_task(const P2Launch &q, P2Shared &sh, P2Smem &sm, int t)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int e = t / q.S2, k = t % q.S2;
+    const WsLayout L = ws_layout(q.B, q.S2, q.tree != 0);
+    if (tid == 0) {
+        const volatile unsigned *ready = reinterpret_cast<const volatile unsigned *>(q.ws + L.ready) + e;
+        const unsigned long long t0 = globaltimer_ns();
+        int ok = 1;
+        while (!*ready) {
+            if (globaltimer_ns() - t0 > kWorkerWaitNs) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
+        }
+        __threadfence();  // the record's fields, written before its flag
+        if (ok)
+            sh.rec = reinterpret_cast<const P2Record *>(q.ws + L.records)[e];
+        sh.last = ok;
+    }
+    __syncthreads();
+    if (!sh.last)
+        return false;
+    const int nz = q.tree ? sh.rec.nz : 0;
+    for (int i = tid; i < nz; i += kThreads)
+        sh.zset[i] = reinterpret_cast<const int *>(q.ws + L.zsets)[(size_t)e * kMaxTree + i];
+    __syncthreads();
+    P2Seq ps;
+    ps.rt = sh.rec.rt;
+    ps.rd = sh.rec.rd;
+    ps.mode = sh.rec.mode;
+    ps.zero_at = sh.rec.zero_at;
+    ps.zero_chunk = ps.zero_at >= 0 ? ps.zero_at / Elem<T>::W : -1;
+    ps.zset = sh.zset;
+    ps.nz = nz;
+    const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
+    unsigned long long *sums = reinterpret_cast<unsigned long long *>(q.ws + L.sums);
+    unsigned long long *mine = sums + ((size_t)e * q.S2 + k) * kWarps * 4;
+    if (lane == 0) {
+        mine[wid * 4 + 0] = r.jt;
+        mine[wid * 4 + 1] = r.jd;
+        mine[wid * 4 + 2] = r.at;
+        mine[wid * 4 + 3] = r.ad;
+    }
+    __threadfence();  // the sums are visible before the count says so
+    __syncthreads();
+    if (tid == 0)
+        sh.last = atomicAdd(reinterpret_cast<unsigned *>(q.ws + L.counters) + e, 1u) == (unsigned)(q.S2 - 1);
+    __syncthreads();
+    if (sh.last) {
+        __threadfence();  // every other task's sums, counted before ours
+        p2_finish<T, ALIGNED>(q, sh, ps, sums + (size_t)e * q.S2 * kWarps * 4, sm);
+    }
+    __syncthreads();  // sh is reused by the next task
+    return true;
+}
+
+// A CTA whose own sequence is decided runs pass-2 tasks until every sequence
+// is decided and every task handed out (see the notes above).  While clusters
+// are still to start, it takes only a task whose record is already appended
+// (one compare-and-swap on the number handed out) and otherwise leaves, so
+// that it holds no SM slot an unscheduled cluster needs.  Once every cluster
+// has started it claims the next task number with one fetch-and-add (a claim
+// may run ahead of the records: the CTA then waits, bounded, for that record
+// to be published, or leaves once every sequence is decided and the number is
+// past the last task).  All threads of the CTA call it.
+template <typename T, bool ALIGNED>
+__device__ __noinline__ void p2_worker(const Params &p)
+{
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
+    P2Smem &sm = *reinterpret_cast<P2Smem *>(dyn_smem);
+    P2Shared &sh = *reinterpret_cast<P2Shared *>(dyn_smem + ((sizeof(P2Smem) + 15) & ~(size_t)15));
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
+    volatile WsHeader *vh = hdr;
+    P2Launch q;
+    q.ws = p.ws;
+    q.B = p.B;
+    q.S2 = p.ws_s2;
+    q.num_chunks = p.num_chunks;
+    q.V = p.V;
+    q.tree = p.parent != nullptr;
+    const WsLayout L = ws_layout(q.B, q.S2, q.tree != 0);
+    const volatile unsigned *ready = reinterpret_cast<const volatile unsigned *>(p.ws + L.ready);
+    const unsigned S2 = (unsigned)q.S2;
+    long long held = -1;  // thread 0: a claimed task number not yet run
+    unsigned long long idle_since = 0;
+    unsigned nap = 32;
+    for (;;) {
+        if (threadIdx.x == 0) {
+            int task = -1, state = 0;  // 0: wait, 1: run task, 2: leave
+            if (vh->started < (unsigned)p.B) {
+                const unsigned taken = vh->taken;
+                if (taken < vh->count * S2 && atomicCAS(&hdr->taken, taken, taken + 1u) == taken) {
+                    task = (int)taken;
+                    state = 1;
+                } else {
+                    state = 2;  // clusters still to start need this slot; they will run their own tasks
+                }
+            } else {
+                if (held < 0)
+                    held = (long long)atomicAdd(&hdr->taken, 1u);
+                const unsigned e = (unsigned)(held / S2);
+                if (e < vh->count && ready[e]) {
+                    task = (int)held;
+                    held = -1;
+                    state = 1;
+                } else if (vh->decided >= (unsigned)p.B && e >= vh->count) {
+                    state = 2;  // every sequence is decided and this number is past the last task
+                } else {
+                    const unsigned long long now = globaltimer_ns();
+                    if (!idle_since)
+                        idle_since = now;
+                    if (now - idle_since > kWorkerWaitNs) {
+                        state = 2;
+                        if (p.status)
+                            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
+                    }
+                }
+            }
+            sh.task = task;
+            sh.state = state;
+        }
+        __syncthreads();
+        const int state = sh.state, task = sh.task;
+        __syncthreads();
+        if (state == 2)
+            return;
+        if (state == 0) {
+            __nanosleep(nap);
+            nap = nap < 512 ? 2 * nap : nap;
+            continue;
+        }
+        nap = 32;
+        idle_since = 0;
+        if (!p2_run_task<T, ALIGNED>(q, sh, sm, task) && threadIdx.x == 0 && p.status)
+            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
+    }
+}
+
+// Cluster start and sequence end for the task scheme (no-ops without a workspace).
+__device__ __forceinline__ void p2_start(const Params &p, int rank)
+{
+    if (p.ws && rank == 0 && threadIdx.x == 0)
+        atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->started, 1u);
+}
+// After the sequence's decision (and its record, if any): counts it decided,
+// then runs pass-2 tasks.  All threads of the CTA call it, then return.
+template <typename T, bool ALIGNED>
+__device__ __forceinline__ void p2_leave(const Params &p, int rank)
+{
+    if (!p.ws)
+        return;
+    if (rank == 0 && threadIdx.x == 0)
+        p2_decided(p);
+    p2_worker<T, ALIGNED>(p);
 }
 
 // ===========================================================================
@@ -1579,9 +2137,7 @@ __device__ __forceinline__ void stream_pass2(const Params &p, SharedState &sh, c
 // KB = 1, 2, 4: the slice gives every thread at most KB chunks of a row, and
 // pass 1 reads 8/KB rows per round trip (sweep_rows_batched); KB = 8: at most
 // 8 chunks, two rows per round trip with 16 loads in flight per thread, for
-// grids that fit in two CTAs per SM (small batches); KB = 16: the sampler (one
-// row, gamma_max = 0), whose pass 1 keeps the chunk sums for pass 2; KB = 0:
-// one row at a time.
+// grids that fit in two CTAs per SM (small batches); KB = 0: one row at a time.
 template <typename T, bool ALIGNED, bool POINT, int KB>
 __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_kernel(const Params p)
 {
@@ -1596,12 +2152,12 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
 
     const uint32_t bad = check_inputs(p, b, g, temp);
     init_diagnostics(p, b, rank);
+    p2_start(p, rank);
     if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
         write_invalid(p, b, rank, bad);
+        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
-    if (tid == 0)
-        sh.timeout = 0;
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
 
     const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
@@ -1609,15 +2165,7 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     Gathered gt = wid == 0 ? gather_ids(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
 
     // ---- pass 1: one streaming sweep of this CTA's slice of every needed row
-    bool stored = false;
-    if constexpr (KB == 16) {
-        extern __shared__ float chunk_sums[];
-        stored = (s.c1 - s.c0 + kThreads - 1) / kThreads <= p.scan_tiles;  // room for every tile
-        const T *row = row_ptr<T>(p, s, 0);
-        const RowStat st = stored ? sweep_row<T, ALIGNED, true>(s, row, chunk_sums) : sweep_row<T, ALIGNED>(s, row);
-        if (lane == 0)
-            sh.warp_part[0][wid] = st;
-    } else if constexpr (KB == 8) {
+    if constexpr (KB == 8) {
         sweep_rows_batched<T, ALIGNED, 8, 2 * kUnroll>(p, sh, s, nrows);
     } else if constexpr (KB > 0) {
         sweep_rows_batched<T, ALIGNED, KB>(p, sh, s, nrows);
@@ -1632,9 +2180,10 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     if (wid == 0)
         gather_logits<T>(p, s, lane, gt);
     exchange_rows(sh, s, nrows);
-    if (!decide_and_write<T>(p, sh, s, gt))
-        return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED>(p, sh, s, sh.n, &sh.recv[0][sh.n], kMaxRows, stored ? sh.warp_part[0] : nullptr);
+    const bool go = decide_and_write<T>(p, sh, s, gt);  // uniform over the cluster; no DSMEM access follows
+    if (go)
+        chain_pass2<T, ALIGNED>(p, sh, s, sh.n);  // with a workspace: the record only
+    p2_leave<T, ALIGNED>(p, rank);
 }
 
 // ===========================================================================
@@ -1666,19 +2215,19 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
 
     const uint32_t bad = check_inputs(p, b, g, temp);
     init_diagnostics(p, b, rank);
+    p2_start(p, rank);
     if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
         write_invalid(p, b, rank, bad);
+        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
-    if (tid == 0) {
-        sh.timeout = 0;
+    if (tid == 0)
         sh.stop = 0;
-    }
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
     const Seq s = make_seq<POINT>(p, C, rank, b, g, temp);
     const int gmax = s.gmax;
     const int cap = (p.num_chunks + C - 1) / C;
-    uint4 *stage = STAGED ? reinterpret_cast<uint4 *>(early_dyn + (size_t)p.scan_tiles * kThreads * 4) : nullptr;
+    uint4 *stage = STAGED ? reinterpret_cast<uint4 *>(early_dyn + kP2SmemBytes) : nullptr;
     // every drafted id is checked, as in the full sweep (lane-parallel)
     if (wid == 0) {
         const bool tb = lane < g && !(p.tokens[(size_t)b * gmax + lane] >= 0 &&
@@ -1702,7 +2251,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
             const T *row = row_ptr<T>(p, s, slot ? g + 1 + i : i);
             // greedy rows need no pass 2: only sampled sequences keep a copy
             const RowStat st = (STAGED && s.sampled)
-                                   ? sweep_row<T, ALIGNED, false, true>(s, row, nullptr, stage + (size_t)slot * cap)
+                                   ? sweep_row<T, ALIGNED, true>(s, row, stage + (size_t)slot * cap)
                                    : sweep_row<T, ALIGNED>(s, row);
             if (lane == 0)
                 sh.warp_part[slot][wid] = st;
@@ -1801,10 +2350,9 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 count_round(p.counters, p.hist, g, n);
         }
     }
-    if (!s.sampled || bits)
-        return;  // uniform over the cluster; no DSMEM access follows
-    stream_pass2<T, ALIGNED, STAGED>(p, sh, s, n, &sh.recv_pos[n & 1][0][0], 2, nullptr, stage,
-                                     STAGED ? stage + cap : nullptr);
+    if (s.sampled && !bits)  // uniform over the cluster
+        chain_pass2<T, ALIGNED, STAGED>(p, sh, s, n, stage, STAGED ? stage + cap : nullptr);
+    p2_leave<T, ALIGNED>(p, rank);
 }
 
 // ===========================================================================
@@ -1822,7 +2370,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
 // ids already rejected there (R): child c passes iff u_c * (1 - p(R)) < p(x_c)
 // ("Speculative Decoding", ch.3).  The first child to pass becomes the next
 // node; when none passes, one token is sampled from p without R by the same
-// exact inverse CDF as the chain kernels (sample_row, with R as a zero set),
+// exact inverse CDF as the chain kernels (pass2_sample, with R as a zero set),
 // using uniforms[b][0] (the root is never tested).  T = 0 follows the child
 // whose id is the argmax, and emits the argmax where none is.  Only the rows
 // on the accepted path are read.
@@ -1856,10 +2404,12 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
         bad |= SPEC_STATUS_BAD_TREE;
     if (__syncthreads_or(bad_token))
         bad |= SPEC_STATUS_BAD_TOKEN;
+    p2_start(p, rank);
     if (bad) {
         write_invalid(p, b, rank, bad);
         if (rank == 0 && p.out_path && tid < N)
             p.out_path[base + tid] = -1;
+        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
     if (tid < kMaxTree) {
@@ -1881,6 +2431,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
     s.point = true;
     s.drafts = false;
     s.k = s.sampled ? __fdiv_rn(kLog2e, temp) : 0.0f;
+    s.temp = temp;
     s.rowlen = (size_t)p.V;
     __syncthreads();
 
@@ -1995,6 +2546,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
         write_invalid(p, b, rank, bits);
         if (rank == 0 && p.out_path && tid < N)
             p.out_path[base + tid] = -1;
+        p2_leave<T, ALIGNED>(p, rank);
         return;  // uniform over the cluster; no DSMEM access follows
     }
     if (rank == 0) {
@@ -2010,327 +2562,68 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
                 count_round(p.counters, p.hist, nn - 1, n);
         }
     }
-    if (!s.sampled)
+    if (!s.sampled) {
+        p2_leave<T, ALIGNED>(p, rank);
         return;
-    const RowStat rs = sh.row[0];
-    WeightParams wp;
-    wp.k = s.k;
-    wp.negmt = -rs.m;
-    wp.invzt = 1.0f / (rs.hi + rs.lo);
-    wp.negmd = 0.0f;
-    wp.invzd = 0.0f;
-    wp.residual = false;
-    wp.zero_at = -1;
-    wp.zero_chunk = -1;
-    wp.zset = tr.rej;
-    wp.nz = tr.nrej;
+    }
+    P2Seq ps;
+    ps.rt = exact_row(sh.row[0], temp);
+    ps.rd = ps.rt;
+    ps.mode = tr.nrej ? kP2Zero : kP2Full;
+    ps.zero_at = -1;
+    ps.zero_chunk = -1;
+    ps.zset = tr.rej;
+    ps.nz = tr.nrej;
     float u = p.uniforms[base];
     if (!(u >= 0.0f))
         u = 0.0f;
     if (u >= 1.0f)
         u = __uint_as_float(0x3F7FFFFFu);
     const T *row = row_ptr<T>(p, s, node);
-    sample_row<T, ALIGNED, true>(p, sh, s, row, row, wp, tr.nrej == 0, rs, &sh.recv_pos[step & 1][0][0], 2, u,
-                                 p.out_tokens + base + n, nullptr);
-}
-
-// ===========================================================================
-// Kernel 2: bulk-copy ring (16-byte aligned rows; A/B alternative)
-// ===========================================================================
-// Segment k of a CTA's copy stream lands in ring stage k % kStages; both the
-// producer lane and the reducing warps walk the same sequence of segments.
-struct RingState {
-    uint4 *ring;
-    unsigned long long *full;
-    unsigned long long *empty;
-};
-
-// A CTA that saw one wait run out waits no more (its results are void anyway),
-// so a fault costs at most one wait's bound per CTA.
-__device__ __forceinline__ bool timed_out_before(const SharedState &sh)
-{
-    return *reinterpret_cast<const volatile int *>(&sh.timeout) != 0;
-}
-
-// Producer: waits until stage k % kStages is free, then starts the copy of
-// segment k into it.  Returns false (copy not started) if the wait ran out or
-// an earlier one did.
-__device__ __forceinline__ bool ring_produce(const RingState &rs, const SharedState &sh, uint32_t k,
-                                             const void *src, uint32_t bytes)
-{
-    const uint32_t st = k % kStages, use = k / kStages;
-    if (timed_out_before(sh))
-        return false;
-    if (use > 0 && !mbar_wait(&rs.empty[st], (use - 1) & 1u))
-        return false;
-    mbar_arrive_expect_tx(&rs.full[st], bytes);
-    bulk_copy_g2s(rs.ring + (size_t)st * kSegChunks, src, bytes, &rs.full[st]);
-    return true;
-}
-
-// Reducers: wait for segment k, then read this thread's chunks of it.
-// 'contiguous' picks chunks tid*N .. tid*N+N-1 (prefix order, pass 2b) instead of
-// tid, tid+kThreads, ... (conflict-free, passes 1 and 2a).
-template <typename T>
-__device__ __forceinline__ void ring_consume(const RingState &rs, SharedState &sh, uint32_t k, int count,
-                                             bool contiguous, uint4 (&v)[kChunksPerThread])
-{
-    const uint32_t st = k % kStages;
-    if (!timed_out_before(sh) && !mbar_wait(&rs.full[st], (k / kStages) & 1u))
-        sh.timeout = 1;
-    const uint4 *seg = rs.ring + (size_t)st * kSegChunks;
-    const int tid = threadIdx.x;
-#pragma unroll
-    for (int u = 0; u < kChunksPerThread; ++u) {
-        const int i = contiguous ? tid * kChunksPerThread + u : tid + u * kThreads;
-        v[u] = i < count ? seg[i] : neg_inf_chunk<T>();
-    }
-    __syncwarp();
-    if ((tid & 31) == 0)
-        mbar_arrive(&rs.empty[st]);
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kTmaThreads, 2) spec_verify_ring_kernel(const Params p)
-{
-    extern __shared__ __align__(128) uint4 ring_mem[];
-    __shared__ SharedState sh;
-    __shared__ __align__(8) unsigned long long full_bar[kStages];
-    __shared__ __align__(8) unsigned long long empty_bar[kStages];
-    cg::cluster_group cluster = cg::this_cluster();
-    constexpr int W = Elem<T>::W;
-    const int C = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
-    const int b = pick.b, g = pick.g;
-    const float temp = pick.temp;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const bool producer = wid == kWarps;
-
-    const uint32_t bad = check_inputs(p, b, g, temp);
-    init_diagnostics(p, b, rank);
-    if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
-        write_invalid(p, b, rank, bad);
-        return;
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kWarps);
-        }
-        sh.timeout = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
-
-    const Seq s = make_seq<false>(p, C, rank, b, g, temp);
-    const int nrows = s.sampled ? 2 * g + 1 : g + 1;
-    const int slice = s.c1 - s.c0;
-    const int nseg = (slice + kSegChunks - 1) / kSegChunks;  // segments per row slice
-    const RingState rs{ring_mem, full_bar, empty_bar};
-    uint32_t k = 0;  // segment counter, identical on both sides
-    const Gathered gt = wid == 0 ? gather_position<T>(p, s, lane) : Gathered{-1, 0.0f, 0.0f, 0.0f};
-
-    // ---- pass 1: every needed row slice in one continuous copy stream
-    if (producer) {
-        if (lane == 0) {
-            for (int step = 0; step < nrows; ++step) {
-                const T *row = row_ptr<T>(p, s, row_at_step(step, g, s.sampled));
-                for (int j = 0; j < nseg; ++j) {
-                    const int start = s.c0 + j * kSegChunks;
-                    const int cnt = min(kSegChunks, s.c1 - start);
-                    if (!ring_produce(rs, sh, k + (uint32_t)(step * nseg + j), row + (size_t)start * W,
-                                      (uint32_t)cnt * 16u))
-                        sh.timeout = 1;
-                }
-            }
-        }
-        __syncwarp();
-        k = (uint32_t)(nrows * nseg);
-    } else {
-        for (int step = 0; step < nrows; ++step) {
-            const int r = row_at_step(step, g, s.sampled);
-            RowAcc acc;
-            acc.reset(tid < min(kSegChunks, slice) ? (s.c0 + tid) * W : INT_MAX);
-            for (int j = 0; j < nseg; ++j) {
-                const int start = s.c0 + j * kSegChunks;
-                const int cnt = min(kSegChunks, s.c1 - start);
-                uint4 v[kChunksPerThread];
-                ring_consume<T>(rs, sh, k++, cnt, false, v);
-                if (s.sampled) {
-                    acc.add_soft<T, kChunksPerThread>(v, s.k);
-                } else {
-                    acc.add_arg<T, kChunksPerThread>(v, (start + tid) * W, kThreads * W);
-                }
-            }
-            const RowStat st = warp_reduce(acc.stat(), s.sampled);
-            if (lane == 0)
-                sh.warp_part[r][wid] = st;
-        }
-    }
-    exchange_rows(sh, s, nrows);
-    if (!decide_and_write<T>(p, sh, s, gt))
-        return;  // uniform over the cluster; every copy issued so far has been consumed
-
-    // ---- pass 2a: slice sums of the decided row's weights (streamed again)
-    const int n = sh.n;
-    bool use_residual = n < g;
-    const T *trow = row_ptr<T>(p, s, n);
-    const T *drow = n < g ? row_ptr<T>(p, s, g + 1 + n) : trow;
-    WeightParams wp = weight_params(sh, s, n, use_residual, -1, W);
-    unsigned long long S = 0, P = 0, mine = 0;
-    bool timed_out = false;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const uint32_t per = use_residual ? 2u : 1u;
-        unsigned long long acc = 0;
-        if (producer) {
-            if (lane == 0) {
-                for (int j = 0; j < nseg; ++j) {
-                    const int start = s.c0 + j * kSegChunks;
-                    const uint32_t bytes = (uint32_t)min(kSegChunks, s.c1 - start) * 16u;
-                    if (!ring_produce(rs, sh, k + per * j, trow + (size_t)start * W, bytes))
-                        sh.timeout = 1;
-                    if (use_residual && !ring_produce(rs, sh, k + per * j + 1, drow + (size_t)start * W, bytes))
-                        sh.timeout = 1;
-                }
-            }
-            __syncwarp();
-        } else {
-            for (int j = 0; j < nseg; ++j) {
-                const int start = s.c0 + j * kSegChunks;
-                const int cnt = min(kSegChunks, s.c1 - start);
-                uint4 tv[kChunksPerThread], dv[kChunksPerThread];
-                ring_consume<T>(rs, sh, k + per * j, cnt, false, tv);
-                if (use_residual)
-                    ring_consume<T>(rs, sh, k + per * j + 1, cnt, false, dv);
-#pragma unroll
-                for (int u = 0; u < kChunksPerThread; ++u)
-                    if (tid + u * kThreads < cnt)
-                        acc += chunk_weight_fixed<T>(tv[u], use_residual ? dv[u] : tv[u], wp);
-            }
-        }
-        k += per * (uint32_t)nseg;
-        mine = block_sum_u64<kWarps + 1>(acc, sh);
-        if (sh.timeout)
-            mine |= kTimeoutFlag;
-        exchange_slice_sum(sh, s, attempt, mine, S, P, timed_out);
-        mine &= ~kTimeoutFlag;
-        if (timed_out || S > 0 || !use_residual)
-            break;
-        use_residual = false;  // degenerate residual (unreachable in exact arithmetic): sample p_n
-        wp = weight_params(sh, s, n, false, -1, W);
-    }
-    if (rank == 0 && tid == 0 && p.resid_mass)
-        p.resid_mass[b] = (float)S * kFixedUnit;
-    if (timed_out) {
+    if (p.ws) {  // pass 2 as a record (with its zero set) for any CTA's tasks
         if (rank == 0) {
-            if (tid <= s.gmax)
-                p.out_tokens[(size_t)b * (s.gmax + 1) + tid] = -1;
-            if (tid == 0) {
-                if (p.out_num)
-                    p.out_num[b] = 0;
-                if (p.seq_status)
-                    p.seq_status[b] = SPEC_STATUS_TIMEOUT;
-                if (p.status)
-                    atomicOr(p.status, SPEC_STATUS_TIMEOUT);
-            }
+            if (tid == 0)
+                sh.n = p2_append(p, ps, row, row, p.out_tokens + base + n, nullptr, u);
+            __syncthreads();
+            const WsLayout L = ws_layout(p.B, p.ws_s2, true);
+            int *z = reinterpret_cast<int *>(p.ws + L.zsets) + (size_t)sh.n * kMaxTree;
+            for (int i = tid; i < tr.nrej; i += kThreads)
+                z[i] = tr.rej[i];
+            __threadfence();
+            __syncthreads();
+            if (tid == 0)
+                p2_publish(p, sh.n);
         }
+        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
-
-    // ---- pass 2b: the CTA whose slice holds floor(u*S) finds the id
-    const unsigned long long theta = scaled_floor(final_uniform(p, s), S);  // pick: C_{j-1} <= theta < C_j
-    if (S == 0 || !(P <= theta && theta < P + mine))
-        return;  // another CTA owns the sample (S == 0 only for an all-zero bonus row)
-    const uint32_t per = use_residual ? 2u : 1u;
-    if (producer) {
-        if (lane == 0) {
-            for (int j = 0; j < nseg; ++j) {
-                const int start = s.c0 + j * kSegChunks;
-                const uint32_t bytes = (uint32_t)min(kSegChunks, s.c1 - start) * 16u;
-                if (!ring_produce(rs, sh, k + per * j, trow + (size_t)start * W, bytes))
-                    sh.timeout = 1;
-                if (use_residual && !ring_produce(rs, sh, k + per * j + 1, drow + (size_t)start * W, bytes))
-                    sh.timeout = 1;
-            }
-        }
-        __syncwarp();
-        return;
-    }
-    unsigned long long carry = P;
-    for (int j = 0; j < nseg; ++j) {
-        const int start = s.c0 + j * kSegChunks;
-        const int cnt = min(kSegChunks, s.c1 - start);
-        uint4 tv[kChunksPerThread], dv[kChunksPerThread];
-        ring_consume<T>(rs, sh, k + per * j, cnt, true, tv);
-        if (use_residual)
-            ring_consume<T>(rs, sh, k + per * j + 1, cnt, true, dv);
-        if (theta < carry)
-            continue;  // found in an earlier segment: drain the stream only (uniform)
-        unsigned long long sig[kChunksPerThread];
-        unsigned long long L = 0;
-#pragma unroll
-        for (int u = 0; u < kChunksPerThread; ++u) {
-            const int i = tid * kChunksPerThread + u;
-            sig[u] = i < cnt ? chunk_weight_fixed<T>(tv[u], use_residual ? dv[u] : tv[u], wp) : 0ull;
-            L += sig[u];
-        }
-        unsigned long long total;
-        const unsigned long long incl = reducers_scan_u64<true>(L, total, sh);
-        unsigned long long start_u = carry + incl - L;
-        if (start_u <= theta && theta < start_u + L) {
-#pragma unroll
-            for (int u = 0; u < kChunksPerThread; ++u) {
-                if (start_u <= theta && theta < start_u + sig[u]) {
-                    float w[W];
-                    chunk_weights<T>(tv[u], use_residual ? dv[u] : tv[u], wp, w);
-                    const int c = start + tid * kChunksPerThread + u;
-                    p.out_tokens[(size_t)b * (s.gmax + 1) + n] = c * W + pick_in_chunk<T>(w, theta - start_u);
-                }
-                start_u += sig[u];
-            }
-        }
-        carry += total;
-    }
-    reducers_sync();
-    if (sh.timeout && tid == 0) {
-        p.out_tokens[(size_t)b * (s.gmax + 1) + n] = -1;
-        if (p.status)
-            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
-    }
+    pass2_sample<T, ALIGNED, false>(sh, s, row, row, nullptr, nullptr, ps, u, p.out_tokens + base + n, nullptr);
 }
+
 
 // ---------------------------------------------------------------------------
 // kernel variants
 // ---------------------------------------------------------------------------
 enum KernelKind {
-    kKindRing = 0,
-    kKindScalarAligned = 1,  // full sweep, register loads, 16-byte aligned rows
-    kKindScalar = 2,         // full sweep, register loads, any alignment
-    kKindEarlyAligned = 3,   // early exit, 16-byte aligned rows
-    kKindEarly = 4,          // early exit, any alignment
-    kKindSmall1 = 5,         // full sweep, aligned, at most 1/2/4 chunks per thread and row
-    kKindSmall2 = 6,
-    kKindSmall4 = 7,
-    kKindTreeAligned = 8,    // candidate-tree walk, 16-byte aligned rows
-    kKindTree = 9,           // candidate-tree walk, any alignment
-    kKindWide8 = 10,         // full sweep, aligned, at most 8 chunks per thread and row, 2 CTAs/SM
-    kKindSample = 11,        // the sampler (gamma_max = 0), aligned: pass 1 keeps the chunk sums
-    kKindEarlyStaged = 12,   // early exit, aligned, decided rows kept in shared memory (rows in host memory)
-    kKinds = 13
+    kKindScalarAligned = 0,  // full sweep, register loads, 16-byte aligned rows
+    kKindScalar = 1,         // full sweep, register loads, any alignment
+    kKindEarlyAligned = 2,   // early exit, 16-byte aligned rows
+    kKindEarly = 3,          // early exit, any alignment
+    kKindSmall1 = 4,         // full sweep, aligned, at most 1/2/4 chunks per thread and row
+    kKindSmall2 = 5,
+    kKindSmall4 = 6,
+    kKindTreeAligned = 7,    // candidate-tree walk, 16-byte aligned rows
+    kKindTree = 8,           // candidate-tree walk, any alignment
+    kKindWide8 = 9,          // full sweep, aligned, at most 8 chunks per thread and row, 2 CTAs/SM
+    kKindEarlyStaged = 10,   // early exit, aligned, decided rows kept in shared memory (rows in host memory)
+    kKinds = 11
 };
 
 // The kernel of one variant, as the pointer the launch API takes (nullptr: no
-// such variant; the ring kernel has no point-mass form).
+// such variant; the tree walk has no separate point-mass form).
 template <typename T, bool POINT> const void *kernel_for_t(int kind)
 {
     switch (kind) {
-    case kKindRing:
-        if constexpr (POINT)
-            return nullptr;
-        else
-            return (const void *)spec_verify_ring_kernel<T>;
     case kKindScalarAligned:
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 0>;
     case kKindScalar:
@@ -2343,11 +2636,6 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 4>;
     case kKindWide8:
         return (const void *)spec_verify_stream_kernel<T, true, POINT, 8>;
-    case kKindSample:
-        if constexpr (POINT)
-            return nullptr;
-        else
-            return (const void *)spec_verify_stream_kernel<T, true, false, 16>;
     case kKindTreeAligned:  // candidates are point masses already: one variant
         if constexpr (POINT)
             return nullptr;
@@ -2362,8 +2650,10 @@ template <typename T, bool POINT> const void *kernel_for_t(int kind)
         return (const void *)spec_verify_early_kernel<T, true, POINT>;
     case kKindEarlyStaged:
         return (const void *)spec_verify_early_kernel<T, true, POINT, true>;
-    default:
+    case kKindEarly:
         return (const void *)spec_verify_early_kernel<T, false, POINT>;
+    default:
+        return nullptr;
     }
 }
 

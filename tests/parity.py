@@ -83,14 +83,38 @@ def compare(batch, gpu_tokens, gpu_num, ref, gpu_status=None) -> ParityReport:
     return rep
 
 
-def softmax_close(gpu_vals, ref_vals, rtol=SOFTMAX_RTOL, atol=1e-30, subset=False):
+def read_masks(batch, num_accepted, ok=None):
+    """Entries of the diagnostics the early-exit kernel must report: for each
+    valid sampled sequence with cut n, the evaluated positions i <= min(n, g-1)
+    (p_hat, q_hat, logz_d) and the target rows i <= n (logz_t).  ok: optional
+    [B] mask of the sequences to include."""
+    B, gmax = batch.B, batch.gmax
+    g = np.clip(batch.num_draft.astype(np.int64), 0, gmax)
+    n = np.asarray(num_accepted, np.int64)
+    live = batch.temperature > 0
+    if ok is not None:
+        live = live & ok
+    i = np.arange(gmax)[None, :]
+    pos = live[:, None] & (i < g[:, None]) & (i <= n[:, None])
+    i1 = np.arange(gmax + 1)[None, :]
+    rows_t = live[:, None] & (i1 <= np.minimum(n, g)[:, None])
+    return {"p_hat": pos, "q_hat": pos, "logz_d": pos, "logz_t": rows_t}
+
+
+def softmax_close(gpu_vals, ref_vals, rtol=SOFTMAX_RTOL, atol=1e-30, need=None):
     """|gpu - ref| <= rtol * |ref| + atol where the oracle has a finite value; the
     finite-value pattern must agree.  Probabilities use rel 1e-5 (atol only
     absorbs float32 underflow); log-normalisers use atol 1e-5, since an absolute
-    error d in log Z is a relative error d in every probability."""
+    error d in log Z is a relative error d in every probability.
+    need: the early exit reports only the rows it read -- a boolean mask of the
+    entries that must be present (finite wherever the oracle is); the others may
+    be missing (NaN) but, where present, must match too."""
     g = np.asarray(gpu_vals, np.float64)
     r = np.asarray(ref_vals, np.float64)
-    if subset:  # the GPU reported only the rows it read (early exit): compare those
+    if need is not None:
+        need = np.asarray(need, bool)
+        missing = need & np.isfinite(r) & ~np.isfinite(g)
+        assert not missing.any(), f"{int(missing.sum())} entries the kernel read are missing"
         has = np.isfinite(g)
         assert np.all(np.isfinite(r[has])), "GPU value where the oracle has none"
     else:

@@ -37,7 +37,7 @@ def _eager_then_replay(fn, outs):
 
 
 @gpu
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3])
+@pytest.mark.parametrize("kernel", [0, 2, 3])
 @pytest.mark.parametrize("cfg,B", [(3, 16), (4, 24)])
 def test_verify_replays_from_a_graph(sv, cfg, B, kernel):
     import torch

@@ -230,15 +230,6 @@ def test_pageable_host_tensor_rejected(sv):
 
 
 @gpu
-def test_ring_kernel_takes_device_logits_only(sv):
-    batch = workloads.make_config(3, B=4)
-    dev = sv.to_device(batch)
-    with pytest.raises(sv.SpecVerifyError) as e:
-        sv.verify(**_pinned(dev), kernel=sv.KERNEL_RING)
-    assert e.value.code == sv.SPEC_ERR_UNSUPPORTED
-
-
-@gpu
 def test_spec_device_pointer(sv):
     import torch
 
