@@ -314,6 +314,8 @@ def config_table(args, sv, dev, stream, main_batch, backend):
                "input_sets": nsets, "set_bytes": set_bytes,
                "l2": "rotated sets cover >= 2x L2" if set_bytes * nsets >= 2 * l2 else "inputs fit in L2"}
         algo = batch.algorithmic_bytes()
+        _, _, _, auto_kind = sv.launch_shape(batch.B, batch.gmax, batch.V, batch.dtype)
+        row["auto_kernel"] = "early_exit" if auto_kind == sv.KERNEL_EARLY else "full_sweep"
         for label, kern in (("auto", sv.KERNEL_AUTO), ("full_sweep", sv.KERNEL_REGISTER),
                             ("early_exit", sv.KERNEL_EARLY)):
             def one(i, kern=kern):
@@ -331,6 +333,15 @@ def config_table(args, sv, dev, stream, main_batch, backend):
             ms = reduce_max(a.elapsed_time(z), backend) / k
             row[f"{label}_us"] = ms * 1e3
             if label == "auto":
+                if auto_kind == sv.KERNEL_EARLY:  # the rows up to each cut, from the outcome
+                    import numpy as np
+
+                    n_acc = on.cpu().numpy().astype(np.int64)
+                    g_np = np.clip(batch.num_draft.astype(np.int64), 0, batch.gmax)
+                    smp = (batch.temperature > 0).astype(np.int64)
+                    rows_full = int(((g_np + 1) + smp * g_np).sum())
+                    rows_early = int(((np.minimum(n_acc, g_np) + 1) + smp * np.minimum(n_acc + 1, g_np)).sum())
+                    algo = algo - (rows_full - rows_early) * batch.V * batch.elem_size
                 row.update({"sequences_per_s": batch.B / (ms / 1e3), "rounds_per_s": 1e3 / ms,
                             "algorithmic_bytes": algo, "hbm_gbs_algorithmic": algo / (ms / 1e3) / 1e9,
                             "frac_of_peak": algo / (ms / 1e3) / 1e9 / peak, "gpu_launches": k})
@@ -373,11 +384,12 @@ def run_ours(args):
     out_tokens = torch.empty((B, batch.gmax + 1), dtype=torch.int32, device=dev)
     out_num = torch.empty((B,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    algo_bytes = batch.algorithmic_bytes()
-    C, nctas, threads = sv.launch_shape(B, batch.gmax, batch.V, batch.dtype)
+    full_bytes = batch.algorithmic_bytes()  # every row the full sweep needs
+    C, nctas, threads, auto_kind = sv.launch_shape(B, batch.gmax, batch.V, batch.dtype)
     if args.cluster:
         C, nctas = args.cluster, B * args.cluster
     kernel = {"auto": sv.KERNEL_AUTO, "stream": sv.KERNEL_REGISTER, "early": sv.KERNEL_EARLY}[args.kernel]
+    ran = auto_kind if args.kernel == "auto" else kernel  # the kernel the steps run
 
     calls = [0]
 
@@ -434,6 +446,17 @@ def run_ours(args):
 
     value = aggregate_value(B, ws, args.steps, ms_max / 1e3)
     ms_step = ms_max / args.steps
+    # bytes one launch must read: every needed row for the full sweep; for the
+    # early exit, the rows up to each sequence's cut (n + 1 target rows, and
+    # min(n + 1, g) draft rows when sampled), from this batch's outcome
+    import numpy as np
+
+    n_acc = out_num.cpu().numpy().astype(np.int64)
+    g_np = batch.num_draft.astype(np.int64)
+    smp_np = (batch.temperature > 0).astype(np.int64)
+    small_bytes = full_bytes - int(((g_np + 1) + smp_np * g_np).sum()) * batch.V * batch.elem_size
+    early_rows = int(((n_acc + 1) + smp_np * np.minimum(n_acc + 1, g_np)).sum())
+    algo_bytes = early_rows * batch.V * batch.elem_size + small_bytes if ran == sv.KERNEL_EARLY else full_bytes
 
     # the distribution of single calls: each of 200 back-to-back calls between
     # its own CUDA events (median, p10 and p90 of the device time)
@@ -715,7 +738,7 @@ def run_ours(args):
 
         # three rounds of the three paths, interleaved, so that a slow stretch
         # of the shared host link falls on every path; the median round counts
-        full_kernel = kernel
+        full_kernel = sv.KERNEL_REGISTER
         rounds = {"zc": [], "full": [], "staged": []}
         for _ in range(3):
             rounds["zc"].append(timed(lambda: zero_copy_step(sv.KERNEL_EARLY)))
@@ -755,7 +778,8 @@ def run_ours(args):
 
     peak, peak_src = measured_peaks()
     achieved = algo_bytes / (ms_step / 1e3) / 1e9
-    workload_key = f"cfg{args.config}-B{B}-g{batch.gmax}-V{batch.V}-{batch.dtype}"
+    kernel_name = "spec_verify_early_kernel" if ran == sv.KERNEL_EARLY else "spec_verify_stream_kernel"
+    workload_key = f"cfg{args.config}-B{B}-g{batch.gmax}-V{batch.V}-{batch.dtype}-{kernel_name}"
     traffic = recorded_traffic(workload_key) if args.kernel == "auto" and not args.cluster else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -772,7 +796,11 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": algo_bytes},
+                     "algorithmic_bytes_per_launch": algo_bytes, "kernel": kernel_name,
+                     "bytes_rule": "rows the launch must read (x V x 2 B) + the 4-byte arrays; early exit: "
+                                   "n+1 target and min(n+1, g) draft rows per sampled sequence, n+1 target "
+                                   "rows per greedy one, from this batch's outcome"},
+        "full_sweep_bytes_per_s": full_bytes / (ms_step / 1e3) / 1e9,
         "gpu_launches": args.steps,
         "per_call_us": per_call,
         "graph_replay": graph,

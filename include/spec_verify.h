@@ -42,9 +42,10 @@
  * prompt lookup, "Speculative Decoding" ch.5): q_i is 1 at x_i, so position i
  * accepts iff uniforms[b, i] < p_i(x_i) and a rejection samples p_n with x_n
  * removed (max(0, p - q) for that q).  No draft row is read.
- * Rows after the cut are still read by this full-sweep variant; rows
- * i > g (target) and i >= g (draft), and every draft row of a greedy
- * sequence, are never read.
+ * The full sweep (options.kernel 2) also reads the rows after the cut; the
+ * early exit (kernel 3, the automatic choice for large batches and tiny rows)
+ * reads none.  Rows i > g (target) and i >= g (draft), and every draft row of
+ * a greedy sequence, are never read.
  *
  * Layout.  All arrays are dense, row-major, and readable by the device of the
  * calling thread's current CUDA context:
@@ -122,10 +123,6 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_TEMPERATURE 2u
 #define SPEC_STATUS_BAD_NUM_DRAFT 4u
 #define SPEC_STATUS_BAD_LOGITS 8u
-/* With a workspace (spec_verify_options.workspace): a CTA waiting for a
- * pass-2 task to appear gave up after its wall-time limit (0.2 s; not
- * expected on a healthy GPU).  Draws may then be missing. */
-#define SPEC_STATUS_TIMEOUT 16u
 /* spec_tree_verify: a node's parent is not an earlier node. */
 #define SPEC_STATUS_BAD_TREE 32u
 
@@ -146,7 +143,9 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
  * results never change. */
 typedef struct spec_verify_options {
     int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1 to 16 */
-    int kernel;       /* 0 = automatic (full sweep, register loads);
+    int kernel;       /* 0 = automatic: the early exit (3) when the full sweep's grid would
+                             fill more than half of the device's resident CTA slots or the
+                             rows are tiny (V * element size <= 8 KB), else the full sweep (2);
                          1 = not a kernel (SPEC_ERR_INVALID_ARG);
                          2 = full sweep, register loads;
                          3 = row-ordered early exit: position i's rows are read, reduced
@@ -162,15 +161,6 @@ typedef struct spec_verify_options {
     uint64_t *accept_hist; /* optional device array [SPEC_MAX_GAMMA + 1] (8-byte aligned): += 1 at
                               index n (accepted count; min(n, SPEC_MAX_GAMMA) for trees) for each
                               verified sequence, the distribution behind the mean.  NULL: none. */
-    void *workspace;       /* optional device scratch, 256-byte aligned, of at least
-                              workspace_bytes >= spec_workspace_size(B, V, dtype, tree) bytes.
-                              With it the final draws run as a second kernel on the same stream
-                              that spreads every sequence's pass 2 over the whole GPU, instead of
-                              on each sequence's own CTAs after its pass 1 (results identical;
-                              faster when many sequences sample).  Its first bytes are zeroed
-                              on the stream before the first kernel; calls that share one
-                              workspace must be ordered on one stream.  NULL: one kernel. */
-    uint64_t workspace_bytes;
 } spec_verify_options;
 
 /* Same round, plus optional float32 diagnostics for tests (any may be NULL):
@@ -183,7 +173,7 @@ typedef struct spec_verify_options {
  *                            sequence (residual mass, or ~1 for a bonus row)
  *   seq_status [B]           SPEC_STATUS_* bits of each sequence (0 = valid)
  * The diagnostic rows are computed for every i <= g, also after the cut (with
- * the full-sweep kernels).  A sequence with a data problem (seq_status != 0)
+ * the full-sweep kernels; options.kernel 0 takes the full sweep here).  A sequence with a data problem (seq_status != 0)
  * may carry partial diagnostics: the rows swept before the problem was found.
  * options: as for spec_verify_ex (NULL = automatic). */
 spec_status spec_verify_debug(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
@@ -285,20 +275,13 @@ spec_status spec_tree_verify(const void *target_logits, const int32_t *parent, c
                              int max_nodes, int V, spec_dtype dtype, uint32_t *status, void *stream,
                              const spec_verify_options *options);
 
-/* Launch shape spec_verify would use on the current device for these sizes:
- * cluster size (CTAs per sequence), total CTAs and threads per CTA.  Any
- * output pointer may be NULL.  Touches the device (attribute queries) but
- * enqueues nothing. */
+/* Launch shape spec_verify would use on the current device for these sizes
+ * (device-memory rows): cluster size (CTAs per sequence), total CTAs, threads
+ * per CTA and the kernel the automatic choice takes (2 = full sweep, 3 = early
+ * exit; see spec_verify_options.kernel).  Any output pointer may be NULL.
+ * Touches the device (attribute queries) but enqueues nothing. */
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
-                                     int *num_ctas, int *threads_per_cta);
-
-/* Bytes of workspace (spec_verify_options.workspace) a call with B sequences
- * (trees: tree = 1) and vocabulary V needs on the current device: per
- * sequence one pass-2 record and its slice sums (about 2.5 KB at V = 128256;
- * 1 KB more per tree for its rejected ids).  Touches the device (its SM count)
- * but enqueues nothing.  SPEC_ERR_INVALID_ARG for a NULL bytes or sizes out of
- * range. */
-spec_status spec_workspace_size(int B, int V, spec_dtype dtype, int tree, uint64_t *bytes);
+                                     int *num_ctas, int *threads_per_cta, int *kernel);
 
 /* The address the kernels use for ptr: ptr itself for this device's memory,
  * the device alias for page-locked host memory mapped into the device's

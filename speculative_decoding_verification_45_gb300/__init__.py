@@ -175,46 +175,6 @@ def _hold_host_inputs(tensors, stream, device):
     _held.append((ev, host))
 
 
-_ws_sizes = {}
-
-
-def workspace_size(B: int, V: int, dtype_code: int, tree: bool = False) -> int:
-    """Bytes of the optional pass-2 workspace (spec_workspace_size) on the current device."""
-    import torch
-
-    key = (torch.cuda.current_device(), B, V, dtype_code, bool(tree))
-    n = _ws_sizes.get(key)
-    if n is None:
-        out = ctypes.c_uint64()
-        rc = _native.load().spec_workspace_size(B, V, dtype_code, int(bool(tree)), ctypes.byref(out))
-        if rc != SPEC_OK:
-            raise SpecVerifyError(rc, "spec_workspace_size")
-        n = _ws_sizes[key] = int(out.value)
-    return n
-
-
-def _workspace(workspace, B, V, code, tree, stream, device):
-    """(pointer, bytes, tensor) of the pass-2 workspace: a caller's uint8 CUDA
-    tensor, a fresh one from torch's allocator on the launch stream (True), or
-    none (False/None: pass 2 inside the verification kernel)."""
-    import torch
-
-    if workspace is None or workspace is False or B == 0:
-        return None, 0, None
-    need = workspace_size(B, V, code, tree)
-    if workspace is True:
-        s = torch.cuda.current_stream(device) if stream is None else stream
-        with torch.cuda.stream(s):
-            workspace = torch.empty(need + 256, dtype=torch.uint8, device=device)
-    if not workspace.is_cuda or workspace.device != device or not workspace.is_contiguous():
-        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
-    ptr = workspace.data_ptr()
-    off = (-ptr) % 256
-    if workspace.numel() * workspace.element_size() - off < need:
-        raise ValueError(f"workspace needs {need} bytes (256-byte aligned)")
-    return ctypes.c_void_p(ptr + off), need, workspace
-
-
 def _counter_ptr(t, n, name):
     """Device pointer of an optional int64 CUDA tensor of at least n elements."""
     if t is None:
@@ -238,7 +198,7 @@ KERNEL_EARLY = 3     # row-ordered early exit: no row after the first rejection 
 
 def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens=None,
            out_num_accepted=None, status=None, stream=None, cluster_size: int = 0, kernel: int = KERNEL_AUTO,
-           counters=None, accept_hist=None, workspace=False):
+           counters=None, accept_hist=None):
     """One verification round on the GPU (asynchronous on ``stream``).
 
     Returns (out_tokens [B, gamma_max+1] int32, out_num_accepted [B] int32).
@@ -255,11 +215,6 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     ``counters``: optional uint64 (int64) CUDA tensor [3], += drafted ids,
     accepted ids, verified sequences.  ``accept_hist``: optional int64 CUDA
     tensor [MAX_GAMMA + 1], += 1 at each verified sequence's accepted count.
-    ``workspace``: False (default) samples each sequence's final token on its
-    own CTAs; True takes a workspace from torch's allocator on the launch
-    stream (or pass a uint8 CUDA tensor of at least workspace_size() + 256
-    bytes), with which every CTA that has finished its own sequence runs
-    slices of the others' final draws (same results).
     """
     B, gmax, V, code, out_tokens, out_num_accepted = _prepare(
         target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, out_tokens, out_num_accepted)
@@ -267,10 +222,9 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
     args = [_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens), _in_ptr(num_draft),
             _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), B, gmax, V, code,
             _status_ptr(status, out_tokens.device), _stream_handle(stream, out_tokens.device)]
-    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, out_tokens.device)
-    if cluster_size or kernel or counters is not None or accept_hist is not None or ws is not None:
+    if cluster_size or kernel or counters is not None or accept_hist is not None:
         opts = _native.Options(int(cluster_size), int(kernel), _counter_ptr(counters, 3, "counters"),
-                               _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"), ws_ptr, ws_bytes)
+                               _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
         rc = lib.spec_verify_ex(*args, ctypes.byref(opts))
     else:
         rc = lib.spec_verify(*args)
@@ -282,7 +236,7 @@ def verify(target_logits, draft_logits, draft_tokens, num_draft, uniforms, tempe
 
 
 def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature, stream=None,
-                 cluster_size: int = 0, kernel: int = KERNEL_AUTO, workspace=False):
+                 cluster_size: int = 0, kernel: int = KERNEL_AUTO):
     """verify() plus the float32 diagnostics of spec_verify_debug (a dict of tensors)."""
     import torch
 
@@ -300,15 +254,13 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
         "status": torch.zeros((1,), dtype=torch.int32, device=dev),
     }
     lib = _native.load()
-    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, dev)
     rc = lib.spec_verify_debug(_in_ptr(target_logits), _in_ptr(draft_logits), _in_ptr(draft_tokens),
                                _in_ptr(num_draft), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens),
                                _ptr(out_num), B, gmax, V,
                                code, _ptr(d["status"]), _stream_handle(stream, dev), _ptr(d["p_hat"]),
                                _ptr(d["q_hat"]), _ptr(d["logz_t"]), _ptr(d["logz_d"]), _ptr(d["resid_mass"]),
                                _ptr(d["seq_status"]),
-                               ctypes.byref(_native.Options(int(cluster_size), int(kernel), None, None, ws_ptr,
-                                                            ws_bytes)))
+                               ctypes.byref(_native.Options(int(cluster_size), int(kernel))))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_debug")
     _hold_host_inputs((target_logits, draft_logits, draft_tokens, num_draft, uniforms, temperature), stream, dev)
@@ -319,7 +271,7 @@ def verify_debug(target_logits, draft_logits, draft_tokens, num_draft, uniforms,
 
 def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature, out_tokens=None,
                 out_num_accepted=None, out_path=None, status=None, stream=None, cluster_size: int = 0,
-                counters=None, accept_hist=None, workspace=False):
+                counters=None, accept_hist=None):
     """One candidate-tree round on the GPU (spec_tree_verify; asynchronous on ``stream``).
 
     target_logits [B, N, V] (row k: the target after the path to node k);
@@ -349,9 +301,8 @@ def tree_verify(target_logits, parent, tokens, num_nodes, uniforms, temperature,
     _check(out_tokens, "out_tokens", torch.int32, (B, N), dev)
     _check(out_num_accepted, "out_num_accepted", torch.int32, (B,), dev)
     _check(out_path, "out_path", torch.int32, (B, N), dev)
-    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, True, stream, dev)
     opts = _native.Options(int(cluster_size), 0, _counter_ptr(counters, 3, "counters"),
-                           _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"), ws_ptr, ws_bytes)
+                           _counter_ptr(accept_hist, MAX_GAMMA + 1, "accept_hist"))
     lib = _native.load()
     rc = lib.spec_tree_verify(_in_ptr(target_logits), _in_ptr(parent), _in_ptr(tokens), _in_ptr(num_nodes),
                               _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_path), B, N, V,
@@ -382,7 +333,7 @@ def tree_to_device(tb, device="cuda"):
 
 
 def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=None, cluster_size: int = 0,
-           kernel: int = KERNEL_AUTO, workspace=False):
+           kernel: int = KERNEL_AUTO):
     """One token per row: y_b ~ softmax(logits[b] / T_b) by inverse CDF with
     uniforms[b], or argmax when T_b == 0 (spec_sample).  Draft-side sampling of
     a proposer, or target-only decoding.  Returns out_tokens [B] int32."""
@@ -400,8 +351,7 @@ def sample(logits, uniforms, temperature, out_tokens=None, status=None, stream=N
         out_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
     _check(out_tokens, "out_tokens", torch.int32, (B,), dev)
     lib = _native.load()
-    ws_ptr, ws_bytes, ws = _workspace(workspace, B, V, code, False, stream, dev)
-    opts = _native.Options(int(cluster_size), int(kernel), None, None, ws_ptr, ws_bytes)
+    opts = _native.Options(int(cluster_size), int(kernel))
     rc = lib.spec_sample(_in_ptr(logits), _in_ptr(uniforms), _in_ptr(temperature), _ptr(out_tokens), B, V, code,
                          _status_ptr(status, dev), _stream_handle(stream, dev), ctypes.byref(opts))
     if rc != SPEC_OK:
@@ -445,14 +395,15 @@ def ngram_propose(context, context_len, min_n: int, max_n: int, gamma_max: int, 
 
 
 def launch_shape(B: int, gamma_max: int, V: int, dtype: str = "bf16"):
-    """(cluster size, CTAs, threads per CTA) the library picks for these sizes on the current device."""
+    """(cluster size, CTAs, threads per CTA, kernel) the library picks for these
+    sizes on the current device; kernel is KERNEL_REGISTER or KERNEL_EARLY."""
     lib = _native.load()
-    c, n, t = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    c, n, t, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = lib.spec_verify_launch_shape(B, gamma_max, V, SPEC_BF16 if dtype == "bf16" else SPEC_F32,
-                                      ctypes.byref(c), ctypes.byref(n), ctypes.byref(t))
+                                      ctypes.byref(c), ctypes.byref(n), ctypes.byref(t), ctypes.byref(k))
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_launch_shape")
-    return c.value, n.value, t.value
+    return c.value, n.value, t.value, k.value
 
 
 def to_device(batch, device="cuda"):

@@ -28,7 +28,7 @@ class Options(ctypes.Structure):
     """spec_verify_options of include/spec_verify.h."""
 
     _fields_ = [("cluster_size", ctypes.c_int), ("kernel", ctypes.c_int), ("counters", ctypes.c_void_p),
-                ("accept_hist", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_uint64)]
+                ("accept_hist", ctypes.c_void_p)]
 
 
 def nvcc_path() -> str:
@@ -101,10 +101,8 @@ def load() -> ctypes.CDLL:
         lib.spec_sample.restype = i32
         lib.spec_tree_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
         lib.spec_tree_verify.restype = i32
-        lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_verify_launch_shape.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
         lib.spec_verify_launch_shape.restype = i32
-        lib.spec_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_uint64)]
-        lib.spec_workspace_size.restype = i32
         lib.spec_device_pointer.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
         lib.spec_device_pointer.restype = i32
         lib.spec_status_string.argtypes = [i32]

@@ -105,7 +105,7 @@ const void *kernel_for(spec_dtype dt, int kind, bool point)
 constexpr int kStagedDynMax = 200 * 1024;
 // Largest dynamic shared memory a kernel kind is launched with: the staged
 // early exit, or pass 2's staging area and queue.
-int kernel_dyn_smem(int kind) { return kind == kKindEarlyStaged ? kStagedDynMax : kWorkerSmemBytes; }
+int kernel_dyn_smem(int kind) { return kind == kKindEarlyStaged ? kStagedDynMax : kP2SmemBytes; }
 int variant_slot(spec_dtype dt, int kind, bool point)
 {
     return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
@@ -238,17 +238,37 @@ int auto_cluster(int B, int num_chunks, int sms)
 
 // Automatic cluster size for one row per sequence (gamma_max = 0: the
 // sampler).  Every cluster then does the same work, and a few long CTAs that
-// are all resident at once beat a grid of several waves: the largest power of
-// two with B*C <= 2 * SMs (at most 8; 16 for one or two rows).  Measured on
-// GB300, 20-call graphs: B=128, V=128256 bf16: 20.2 us at 8 -> 15.9 at 2;
-// B=1024: 111 -> 65 us; B=256, V=32000: 17.8 -> 10.7 us.
-int sampler_cluster(int B, int sms)
+// are all resident at once beat a grid of several waves for the streaming:
+// the largest power of two with B*C <= 2 * SMs (at most 8; 16 for one or two
+// rows).  But the final draw's exact weights (pass 2) cost several times the
+// streaming's ALU work per byte and run on the row's own CTAs, so a long row
+// (at least 4096 chunks) is split over at least 4 CTAs.  Measured on GB300,
+// 10-call graphs, V = 128256 bf16, half the rows at T = 1: B = 256 takes
+// 119 us at 1 CTA per row, 101 at 2, 69 at 4, 82 at 8; B = 64 and 32 are best
+// at the first rule's 4 and 8.
+int sampler_cluster(int B, int num_chunks, int sms)
 {
     const int cap = B <= 2 ? 16 : 8;
     int C = 1;
     while (C < cap && (long long)B * C * 2 <= 2LL * sms)
         C *= 2;
+    if (num_chunks >= 4096 && C < 4)
+        C = 4;
     return C;
+}
+
+// Whether the automatic choice is the row-ordered early exit: when the full
+// sweep's grid would fill more than half of the resident slots (many
+// sequences: reading only the rows up to each cut saves bandwidth and the
+// final draws start earlier), or for tiny rows (at most 512 chunks: one
+// round trip per position either way).  Measured on GB300, 10-call graphs:
+// B = 256, V = 128256 (half greedy): 122 us early exit against 150 us full
+// sweep; B = 64, V = 151936: 69 against 71; B = 32 (every sequence sampled):
+// 51 against 45; B = 1, V = 32000: 45 against 33; B = 1, V = 1024: 18
+// against 23.
+bool auto_early_exit(int B, int num_chunks, int sms)
+{
+    return num_chunks <= 512 || (long long)B * auto_cluster(B, num_chunks, sms) > 2LL * sms;
 }
 
 // Automatic cluster size of a candidate-tree walk.  Each level of the walk is
@@ -300,7 +320,7 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
         const bool walk = kinds[i] == kKindTreeAligned || kinds[i] == kKindTree;
         int C = want_C > 0 ? want_C
                 : walk     ? tree_cluster(B, num_chunks, sms)
-                : one_row  ? sampler_cluster(B, sms)
+                : one_row  ? sampler_cluster(B, num_chunks, sms)
                            : auto_cluster(B, num_chunks, sms);
         for (;;) {
             if (cluster_launchable(dev, dt, kinds[i], C, point)) {
@@ -329,32 +349,6 @@ spec_status resolve_shape(int B, int V, spec_dtype dt, bool aligned, int want_ki
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
-
-// Slices per decided row for the pass-2 tasks: the smallest power of two (at
-// most 32) with B * S2 >= 8 * SMs tasks, keeping at least 256 chunks per slice.
-int pass2_slices(int B, int num_chunks, int sms)
-{
-    int S2 = 1;
-    while (S2 < 32 && (long long)B * S2 < 8LL * sms && num_chunks / (S2 * 2) >= kThreads)
-        S2 *= 2;
-    return S2;
-}
-
-// Checks a caller's workspace for B sequences and zeroes its counters on the
-// stream; on success *S2 is the slices per row of the second launch.
-spec_status prepare_workspace(const spec_verify_options *opt, int B, int num_chunks, bool tree, int sms,
-                              cudaStream_t stream, int *S2)
-{
-    *S2 = pass2_slices(B, num_chunks, sms);
-    const WsLayout L = ws_layout(B, *S2, tree);
-    if (((uintptr_t)opt->workspace & 255u) || opt->workspace_bytes < (uint64_t)L.total)
-        return SPEC_ERR_INVALID_ARG;
-    if (cudaMemsetAsync(opt->workspace, 0, ws_zeroed(B), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return SPEC_ERR_CUDA;
-    }
-    return SPEC_OK;
-}
 
 // True when p lies in device (or managed) memory; the kernels also read
 // page-locked host memory mapped into the device's address space, with
@@ -408,6 +402,14 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
     const bool point = gmax > 0 && !draft;
+    // automatic: full sweep or early exit (the debug call's row diagnostics
+    // need the full sweep, which reads every row)
+    if (want_kind < 0 && gmax > 0 && !p_hat && !q_hat && !logz_t && !logz_d) {
+        int dev = 0, sms = 0;
+        if (current_device(&dev) == SPEC_OK && device_sm_count(dev, &sms) == SPEC_OK &&
+            auto_early_exit(B, (V + chunk_width(dtype) - 1) / chunk_width(dtype), sms))
+            want_kind = kKindEarlyAligned;
+    }
     const bool host_rows = want_kind == kKindEarlyAligned && aligned &&
                            (!device_memory(target) || (draft && !device_memory(draft)));
     if (!aligned && want_kind == kKindScalarAligned)
@@ -472,18 +474,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
     prm.out_path = nullptr;
-    prm.ws = nullptr;
-    prm.ws_s2 = 0;
-    // A workspace moves pass 2 to a second launch (not for the staged early
-    // exit, which keeps the decided rows in shared memory).
-    const bool two = opt && opt->workspace && shp.kind != kKindEarlyStaged;
-    if (two) {
-        st = prepare_workspace(opt, B, prm.num_chunks, false, shp.sms, (cudaStream_t)stream, &prm.ws_s2);
-        if (st != SPEC_OK)
-            return st;
-        prm.ws = reinterpret_cast<unsigned char *>(opt->workspace);
-    }
-    size_t dyn = two ? (size_t)kWorkerSmemBytes : (size_t)kP2SmemBytes;
+    size_t dyn = (size_t)kP2SmemBytes;
     if (shp.kind == kKindEarlyStaged)
         dyn += (size_t)nslot * (size_t)slice * 16;
 
@@ -553,19 +544,9 @@ spec_status run_tree(const void *target, const int32_t *parent, const int32_t *t
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = parent;
     prm.out_path = out_path;
-    prm.ws = nullptr;
-    prm.ws_s2 = 0;
-    const bool two = opt && opt->workspace;
-    if (two) {
-        st = prepare_workspace(opt, B, prm.num_chunks, true, shp.sms, (cudaStream_t)stream, &prm.ws_s2);
-        if (st != SPEC_OK)
-            return st;
-        prm.ws = reinterpret_cast<unsigned char *>(opt->workspace);
-    }
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config((unsigned)B * (unsigned)shp.C, shp.C,
-                                           two ? (size_t)kWorkerSmemBytes : (size_t)kP2SmemBytes,
-                                           (cudaStream_t)stream, attr);
+    cudaLaunchConfig_t cfg =
+        launch_config((unsigned)B * (unsigned)shp.C, shp.C, (size_t)kP2SmemBytes, (cudaStream_t)stream, attr);
     void *args[] = {&prm};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_for(dtype, shp.kind, false), args);
     if (e != cudaSuccess) {
@@ -673,7 +654,7 @@ spec_status spec_ngram_propose(const int32_t *context, int64_t context_stride, c
 }
 
 spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dtype, int *cluster_size,
-                                     int *num_ctas, int *threads_per_cta)
+                                     int *num_ctas, int *threads_per_cta, int *kernel)
 {
     if (dtype != SPEC_F32 && dtype != SPEC_BF16)
         return SPEC_ERR_UNSUPPORTED;
@@ -681,34 +662,29 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
         V > SPEC_MAX_VOCAB)
         return SPEC_ERR_INVALID_ARG;
     const bool aligned = ((size_t)V * (size_t)elem_size(dtype)) % 16 == 0;
+    int want = -1;
+    if (gamma_max > 0) {
+        int dev = 0, sms = 0;
+        spec_status st0 = current_device(&dev);
+        if (st0 == SPEC_OK)
+            st0 = device_sm_count(dev, &sms);
+        if (st0 != SPEC_OK)
+            return st0;
+        if (auto_early_exit(B > 0 ? B : 1, (V + chunk_width(dtype) - 1) / chunk_width(dtype), sms))
+            want = aligned ? kKindEarlyAligned : kKindEarly;
+    }
     Shape shp;
-    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, -1, 0, &shp, false, gamma_max == 0);
+    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, want, 0, &shp, false, gamma_max == 0);
     if (st != SPEC_OK)
         return st;
+    if (kernel)
+        *kernel = (shp.kind == kKindEarlyAligned || shp.kind == kKindEarly) ? 3 : 2;
     if (cluster_size)
         *cluster_size = shp.C;
     if (num_ctas)
         *num_ctas = B * shp.C;
     if (threads_per_cta)
         *threads_per_cta = kThreads;
-    return SPEC_OK;
-}
-
-spec_status spec_workspace_size(int B, int V, spec_dtype dtype, int tree, uint64_t *bytes)
-{
-    if (dtype != SPEC_F32 && dtype != SPEC_BF16)
-        return SPEC_ERR_UNSUPPORTED;
-    if (!bytes || B < 0 || B > SPEC_MAX_BATCH || V < 1 || V > SPEC_MAX_VOCAB)
-        return SPEC_ERR_INVALID_ARG;
-    int dev = 0, sms = 0;
-    spec_status st = current_device(&dev);
-    if (st != SPEC_OK)
-        return st;
-    st = device_sm_count(dev, &sms);
-    if (st != SPEC_OK)
-        return st;
-    const int num_chunks = (V + chunk_width(dtype) - 1) / chunk_width(dtype);
-    *bytes = (uint64_t)ws_layout(B, pass2_slices(B, num_chunks, sms), tree != 0).total;
     return SPEC_OK;
 }
 

@@ -106,8 +106,6 @@ struct Params {
     unsigned long long *hist;      // optional: [SPEC_MAX_GAMMA + 1] += 1 at the accepted count
     const int32_t *parent;         // tree kernel: [B, gmax+1] parent of each node (num_draft = node count)
     int32_t *out_path;             // tree kernel: [B, gmax+1] accepted node indices, or NULL
-    unsigned char *ws;             // workspace: pass 2 as tasks for any CTA (NULL: each cluster samples its own)
-    int ws_s2;                     // pass-2 slices per row
 };
 
 // ---------------------------------------------------------------------------
@@ -1662,11 +1660,10 @@ __device__ __forceinline__ P2Seq chain_p2seq(const SharedState &sh, const Seq &s
     return ps;
 }
 
-// Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n.
-// With a workspace, rank 0 only appends the sequence's record for
-// any CTA's pass-2 tasks.  Otherwise the cluster samples here; STAGED: tst and dst
-// hold this CTA's slices of rows t_n and d_n (early exit with rows in host
-// memory), so pass 2 reads neither row again.
+// Pass 2 of the chain kernels for a sampled, valid sequence whose cut is n,
+// across its cluster.  STAGED: tst and dst hold this CTA's slices of rows t_n
+// and d_n (early exit with rows in host memory), so pass 2 reads neither row
+// again.
 template <typename T, bool ALIGNED, bool STAGED = false>
 __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, const Seq &s, int n,
                                             const uint4 *tst = nullptr, const uint4 *dst = nullptr)
@@ -1678,457 +1675,7 @@ __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, co
     const T *drow = rows ? row_ptr<T>(p, s, g + 1 + n) : trow;
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
     float *mass = p.resid_mass ? p.resid_mass + b : nullptr;
-    if (!STAGED && p.ws) {
-        if (s.rank == 0 && threadIdx.x == 0)
-            p2_publish(p, p2_append(p, ps, trow, drow, outn, mass, final_uniform(p, s)));
-        return;
-    }
     pass2_sample<T, ALIGNED, STAGED>(sh, s, trow, drow, tst, rows ? dst : tst, ps, final_uniform(p, s), outn, mass);
-}
-
-// ===========================================================================
-// Pass 2 as tasks for any CTA (when the caller gives a workspace)
-// ===========================================================================
-// Pass 2 of a sequence is a sweep of its decided row (two rows for a residual)
-// with the exact weights above: several times the ALU work of pass 1's
-// reduction of the same bytes.  Done by the sequence's own cluster after its
-// pass 1, the last clusters' pass 2 becomes the grid's tail while most SMs
-// idle.  With a workspace, rank 0 of each sampled, valid sequence instead
-// appends a P2Record (decided rows, weight scales, uniform, output slot) and
-// marks it ready; every CTA, once its own sequence is decided, becomes a
-// worker that takes slice tasks (record e, slice k) from the workspace.  A
-// task sweeps its slice as a cluster CTA would (p2_sweep), stores the
-// per-warp-range sums and counts itself done with an atomic; the task that
-// completes a record (the last arriver: no CTA waits for another's result)
-// adds the sums in slice and warp order, finds the slice and warp range that
-// hold floor(u*R), recomputes that range (p2_owner) and writes the token.  The
-// results are the one-kernel path's: the same integer weights, summed exactly.
-// A worker with no task to take waits for one only once every cluster of the
-// grid has started (so it holds no SM slot that an unscheduled cluster needs),
-// polling with a backoff and a wall-time limit (kWorkerWaitNs: it then gives
-// up and sets SPEC_STATUS_TIMEOUT); it leaves when every sequence is decided
-// and every task handed out.  Waits never form a cycle: tasks come from CTAs
-// that are streaming or deciding, which never wait.
-constexpr unsigned long long kWorkerWaitNs = 200000000ull;  // 0.2 s
-
-struct P2Record {
-    const void *trow;   // decided target row
-    const void *drow;   // its draft row (residual), else trow
-    int32_t *out;       // the token's slot in out_tokens
-    float *mass;        // resid_mass slot, or NULL
-    ExactRow rt, rd;
-    float u;            // the final uniform
-    int mode;           // P2Mode
-    int zero_at;        // kP2Zero: a removed id (-1: none)
-    int nz;             // kP2Zero: ids in the record's zero set (tree walks)
-};
-
-// Workspace layout: [count][counters[B]] (zeroed before each call), records,
-// per record, slice and warp range the four sums, and (tree walks) each
-// record's zero set.
-// Counters at the start of the workspace (zeroed before each call).
-struct WsHeader {
-    unsigned count;     // records appended
-    unsigned taken;     // slice tasks handed out
-    unsigned decided;   // sequences decided (every kind)
-    unsigned started;   // clusters started
-};
-
-struct WsLayout {
-    size_t counters, ready, records, sums, zsets, total;
-};
-__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
-__host__ __device__ inline WsLayout ws_layout(int B, int S2, bool tree)
-{
-    WsLayout L;
-    L.counters = 256;
-    L.ready = ws_align(L.counters + 4 * (size_t)B);
-    L.records = ws_align(L.ready + 4 * (size_t)B);
-    L.sums = ws_align(L.records + sizeof(P2Record) * (size_t)B);
-    L.zsets = ws_align(L.sums + 32 * (size_t)kWarps * (size_t)S2 * (size_t)B);
-    L.total = ws_align(L.zsets + (tree ? 4 * (size_t)kMaxTree * (size_t)B : 0));
-    return L;
-}
-// Bytes zeroed before each call: the header, the per-record counters and ready flags.
-__host__ __device__ inline size_t ws_zeroed(int B) { return ws_layout(B, 1, false).records; }
-
-// Rank 0, thread 0: appends sequence b's pass 2 as a record (index returned);
-// p2_publish marks it ready once the record (and a tree's zero set) is written.
-__device__ __forceinline__ int p2_append(const Params &p, const P2Seq &ps, const void *trow, const void *drow,
-                                         int32_t *outn, float *mass, float u)
-{
-    const WsLayout L = ws_layout(p.B, p.ws_s2, p.parent != nullptr);
-    const int e = (int)atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->count, 1u);
-    P2Record &r = reinterpret_cast<P2Record *>(p.ws + L.records)[e];
-    r.trow = trow;
-    r.drow = drow;
-    r.out = outn;
-    r.mass = mass;
-    r.rt = ps.rt;
-    r.rd = ps.rd;
-    r.u = u;
-    r.mode = ps.mode;
-    r.zero_at = ps.zero_at;
-    r.nz = ps.nz;
-    return e;
-}
-
-__device__ __forceinline__ void p2_publish(const Params &p, int e)
-{
-    const WsLayout L = ws_layout(p.B, p.ws_s2, p.parent != nullptr);
-    __threadfence();  // the record is visible before its flag
-    atomicExch(reinterpret_cast<unsigned *>(p.ws + L.ready) + e, 1u);
-}
-
-// One sequence decided (rank 0, thread 0, after publishing its record if any).
-__device__ __forceinline__ void p2_decided(const Params &p)
-{
-    __threadfence();
-    atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->decided, 1u);
-}
-
-struct P2Launch {
-    unsigned char *ws;
-    int B, S2, num_chunks, V;
-    int tree;  // records carry zero sets
-};
-
-struct P2Shared {
-    P2Record rec;
-    int zset[kMaxTree];
-    unsigned long long w[kWarps][4];
-    unsigned long long sl[kWarps][4];  // finisher: partial sums of slices, per warp
-    i128 scan[kWarps];
-    i128 rel;
-    int wmin[kWarps];
-    int owner, wr;
-    int last;
-    int task, state;
-};
-// Dynamic shared memory of a CTA that runs pass-2 tasks.
-constexpr int kWorkerSmemBytes = (int)(((sizeof(P2Smem) + 15) & ~(size_t)15) + sizeof(P2Shared));
-
-// Slice k of S2 over the row's chunks, as a Seq for p2_sweep / p2_owner.
-__device__ __forceinline__ Seq p2_slice(const P2Launch &q, int k)
-{
-    Seq s;
-    s.b = 0;
-    s.g = 0;
-    s.gmax = 0;
-    s.V = q.V;
-    s.rank = k;
-    s.C = q.S2;
-    s.c0 = (int)((long long)q.num_chunks * k / q.S2);
-    s.c1 = (int)((long long)q.num_chunks * (k + 1) / q.S2);
-    s.sampled = true;
-    s.point = false;
-    s.drafts = false;
-    s.k = 0.0f;
-    s.temp = 0.0f;
-    s.rowlen = (size_t)q.V;
-    return s;
-}
-
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ RangeSums p2_task_sweep(const P2Launch &q, const P2Shared &sh, const P2Seq &ps, int k,
-                                                   P2Smem &sm)
-{
-    const Seq s = p2_slice(q, k);
-    const T *trow = reinterpret_cast<const T *>(sh.rec.trow);
-    const T *drow = reinterpret_cast<const T *>(sh.rec.drow);
-    return ps.mode == kP2Residual ? p2_sweep<T, ALIGNED, true, false>(s, trow, drow, nullptr, nullptr, ps, sm)
-                                  : p2_sweep<T, ALIGNED, false, false>(s, trow, drow, nullptr, nullptr, ps, sm);
-}
-
-// The task that completed record e: totals, the draw, the owner range, the id.
-// Thread t < S2 * kWarps loads the sums of (slice t / kWarps, warp range
-// t % kWarps), so every load is issued at once.
-template <typename T, bool ALIGNED>
-__device__ __noinline__ void p2_finish(const P2Launch &q, P2Shared &sh, P2Seq ps, const unsigned long long *sums,
-                                       P2Smem &sm)
-{
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int S2 = q.S2, G = S2 * kWarps;  // G <= kThreads (S2 <= 32)
-    bool resid = ps.mode == kP2Residual;
-    unsigned long long v[4] = {0ull, 0ull, 0ull, 0ull};
-    if (tid < G) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            v[j] = __ldcg(sums + (size_t)tid * 4 + j);  // written by other CTAs: read past L1
-    }
-    // totals: exact, so the order of the additions does not matter
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const unsigned long long t = warp_sum_u64(v[j]);
-        if (lane == 0)
-            sh.sl[wid][j] = t;
-    }
-    __syncthreads();
-    unsigned long long tot[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        for (int w = 0; w < kWarps; ++w)
-            tot[j] += sh.sl[w][j];
-    unsigned long long A = tot[2], B = resid ? tot[3] : 1ull;
-    i128 R = p2_value(tot[0], resid ? tot[1] : 0ull, A, B);
-    const bool fallback = R <= 0;
-    int owner = S2 - 1, wr = kWarps - 1;
-    i128 rel = 0;
-    if (!fallback) {
-        // each group's value, then the slice and warp range holding theta, in order
-        const i128 gv = tid < G ? p2_value(v[0], resid ? v[1] : 0ull, A, B) : (i128)0;
-        __syncthreads();  // sh.sl is read above
-        const i128 theta = scaled_floor128(sh.rec.u, R);
-        i128 total;
-        const i128 incl = block_scan_i128(gv, total, sh.scan);
-        const int first = block_first(tid < G && incl > theta, sh.wmin);
-        if (tid == first) {
-            sh.rel = theta - (incl - gv);
-            sh.owner = tid / kWarps;
-            sh.wr = tid % kWarps;
-        }
-        __syncthreads();
-        if (first < kThreads) {
-            rel = sh.rel;
-            owner = sh.owner;
-            wr = sh.wr;
-        }
-        __syncthreads();
-    } else {
-        // no mass (unreachable in exact arithmetic for a residual): sample p,
-        // sweeping every slice again here with J = all ids
-        ps.mode = kP2Full;
-        ps.nz = 0;
-        ps.zero_at = -1;
-        ps.zero_chunk = -1;
-        resid = false;
-        B = 1;
-        unsigned long long total = 0;
-        for (int k = 0; k < S2; ++k) {
-            const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
-            if (lane == 0)
-                sh.w[wid][0] = r.jt;
-            __syncthreads();
-            for (int w = 0; w < kWarps; ++w)
-                total += sh.w[w][0];
-            __syncthreads();
-        }
-        A = total;
-        R = (i128)A;
-        const i128 theta = scaled_floor128(sh.rec.u, R);
-        i128 before = 0;
-        for (int k = 0; k < S2; ++k) {  // the owner slice, then its warp range
-            const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
-            if (lane == 0)
-                sh.w[wid][0] = r.jt;
-            __syncthreads();
-            i128 sv = 0;
-            for (int w = 0; w < kWarps; ++w)
-                sv += (i128)sh.w[w][0];
-            if (theta < before + sv || k == S2 - 1) {
-                owner = k;
-                rel = theta - before;
-                for (int w = 0; w < kWarps; ++w) {
-                    wr = w;
-                    if (rel < (i128)sh.w[w][0])
-                        break;
-                    if (w < kWarps - 1)
-                        rel -= (i128)sh.w[w][0];
-                }
-                break;
-            }
-            before += sv;
-            __syncthreads();
-        }
-        __syncthreads();
-    }
-    if (sh.rec.mass && tid == 0)
-        *sh.rec.mass = (float)(resid ? i128_to_double(R) / ((double)A * (double)B) : i128_to_double(R) / (double)A);
-    if (R <= 0) {
-        if (tid == 0)
-            *sh.rec.out = -1;  // an all-zero row: nothing to draw from (not reachable for a valid row)
-        return;
-    }
-    const Seq s = p2_slice(q, owner);
-    int r0, r1;
-    warp_range(s, wr, r0, r1);
-    const T *trow = reinterpret_cast<const T *>(sh.rec.trow);
-    const T *drow = reinterpret_cast<const T *>(sh.rec.drow);
-    if (resid)
-        p2_owner<T, ALIGNED, true, false>(sh.scan, sh.wmin, s, trow, drow, nullptr, nullptr, ps, r0, r1, rel, A, B,
-                                          sh.rec.out);
-    else
-        p2_owner<T, ALIGNED, false, false>(sh.scan, sh.wmin, s, trow, drow, nullptr, nullptr, ps, r0, r1, rel, A, B,
-                                           sh.rec.out);
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// One slice task: record t / S2, slice t % S2.  The record's writer may still
-// be filling it: its ready flag is awaited first (bounded).  False when that
-// wait ran out.  All threads of the CTA call it.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ bool p2_run_task(const P2Launch &q, P2Shared &sh, P2Smem &sm, int t)
-{
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int e = t / q.S2, k = t % q.S2;
-    const WsLayout L = ws_layout(q.B, q.S2, q.tree != 0);
-    if (tid == 0) {
-        const volatile unsigned *ready = reinterpret_cast<const volatile unsigned *>(q.ws + L.ready) + e;
-        const unsigned long long t0 = globaltimer_ns();
-        int ok = 1;
-        while (!*ready) {
-            if (globaltimer_ns() - t0 > kWorkerWaitNs) {
-                ok = 0;
-                break;
-            }
-            __nanosleep(32);
-        }
-        __threadfence();  // the record's fields, written before its flag
-        if (ok)
-            sh.rec = reinterpret_cast<const P2Record *>(q.ws + L.records)[e];
-        sh.last = ok;
-    }
-    __syncthreads();
-    if (!sh.last)
-        return false;
-    const int nz = q.tree ? sh.rec.nz : 0;
-    for (int i = tid; i < nz; i += kThreads)
-        sh.zset[i] = reinterpret_cast<const int *>(q.ws + L.zsets)[(size_t)e * kMaxTree + i];
-    __syncthreads();
-    P2Seq ps;
-    ps.rt = sh.rec.rt;
-    ps.rd = sh.rec.rd;
-    ps.mode = sh.rec.mode;
-    ps.zero_at = sh.rec.zero_at;
-    ps.zero_chunk = ps.zero_at >= 0 ? ps.zero_at / Elem<T>::W : -1;
-    ps.zset = sh.zset;
-    ps.nz = nz;
-    const RangeSums r = p2_task_sweep<T, ALIGNED>(q, sh, ps, k, sm);
-    unsigned long long *sums = reinterpret_cast<unsigned long long *>(q.ws + L.sums);
-    unsigned long long *mine = sums + ((size_t)e * q.S2 + k) * kWarps * 4;
-    if (lane == 0) {
-        mine[wid * 4 + 0] = r.jt;
-        mine[wid * 4 + 1] = r.jd;
-        mine[wid * 4 + 2] = r.at;
-        mine[wid * 4 + 3] = r.ad;
-    }
-    __threadfence();  // the sums are visible before the count says so
-    __syncthreads();
-    if (tid == 0)
-        sh.last = atomicAdd(reinterpret_cast<unsigned *>(q.ws + L.counters) + e, 1u) == (unsigned)(q.S2 - 1);
-    __syncthreads();
-    if (sh.last) {
-        __threadfence();  // every other task's sums, counted before ours
-        p2_finish<T, ALIGNED>(q, sh, ps, sums + (size_t)e * q.S2 * kWarps * 4, sm);
-    }
-    __syncthreads();  // sh is reused by the next task
-    return true;
-}
-
-// A CTA whose own sequence is decided runs pass-2 tasks until every sequence
-// is decided and every task handed out (see the notes above).  While clusters
-// are still to start, it takes only a task whose record is already appended
-// (one compare-and-swap on the number handed out) and otherwise leaves, so
-// that it holds no SM slot an unscheduled cluster needs.  Once every cluster
-// has started it claims the next task number with one fetch-and-add (a claim
-// may run ahead of the records: the CTA then waits, bounded, for that record
-// to be published, or leaves once every sequence is decided and the number is
-// past the last task).  All threads of the CTA call it.
-template <typename T, bool ALIGNED>
-__device__ __noinline__ void p2_worker(const Params &p)
-{
-    extern __shared__ __align__(16) unsigned char dyn_smem[];
-    P2Smem &sm = *reinterpret_cast<P2Smem *>(dyn_smem);
-    P2Shared &sh = *reinterpret_cast<P2Shared *>(dyn_smem + ((sizeof(P2Smem) + 15) & ~(size_t)15));
-    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
-    volatile WsHeader *vh = hdr;
-    P2Launch q;
-    q.ws = p.ws;
-    q.B = p.B;
-    q.S2 = p.ws_s2;
-    q.num_chunks = p.num_chunks;
-    q.V = p.V;
-    q.tree = p.parent != nullptr;
-    const WsLayout L = ws_layout(q.B, q.S2, q.tree != 0);
-    const volatile unsigned *ready = reinterpret_cast<const volatile unsigned *>(p.ws + L.ready);
-    const unsigned S2 = (unsigned)q.S2;
-    long long held = -1;  // thread 0: a claimed task number not yet run
-    unsigned long long idle_since = 0;
-    unsigned nap = 32;
-    for (;;) {
-        if (threadIdx.x == 0) {
-            int task = -1, state = 0;  // 0: wait, 1: run task, 2: leave
-            if (vh->started < (unsigned)p.B) {
-                const unsigned taken = vh->taken;
-                if (taken < vh->count * S2 && atomicCAS(&hdr->taken, taken, taken + 1u) == taken) {
-                    task = (int)taken;
-                    state = 1;
-                } else {
-                    state = 2;  // clusters still to start need this slot; they will run their own tasks
-                }
-            } else {
-                if (held < 0)
-                    held = (long long)atomicAdd(&hdr->taken, 1u);
-                const unsigned e = (unsigned)(held / S2);
-                if (e < vh->count && ready[e]) {
-                    task = (int)held;
-                    held = -1;
-                    state = 1;
-                } else if (vh->decided >= (unsigned)p.B && e >= vh->count) {
-                    state = 2;  // every sequence is decided and this number is past the last task
-                } else {
-                    const unsigned long long now = globaltimer_ns();
-                    if (!idle_since)
-                        idle_since = now;
-                    if (now - idle_since > kWorkerWaitNs) {
-                        state = 2;
-                        if (p.status)
-                            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
-                    }
-                }
-            }
-            sh.task = task;
-            sh.state = state;
-        }
-        __syncthreads();
-        const int state = sh.state, task = sh.task;
-        __syncthreads();
-        if (state == 2)
-            return;
-        if (state == 0) {
-            __nanosleep(nap);
-            nap = nap < 512 ? 2 * nap : nap;
-            continue;
-        }
-        nap = 32;
-        idle_since = 0;
-        if (!p2_run_task<T, ALIGNED>(q, sh, sm, task) && threadIdx.x == 0 && p.status)
-            atomicOr(p.status, SPEC_STATUS_TIMEOUT);
-    }
-}
-
-// Cluster start and sequence end for the task scheme (no-ops without a workspace).
-__device__ __forceinline__ void p2_start(const Params &p, int rank)
-{
-    if (p.ws && rank == 0 && threadIdx.x == 0)
-        atomicAdd(&reinterpret_cast<WsHeader *>(p.ws)->started, 1u);
-}
-// After the sequence's decision (and its record, if any): counts it decided,
-// then runs pass-2 tasks.  All threads of the CTA call it, then return.
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ void p2_leave(const Params &p, int rank)
-{
-    if (!p.ws)
-        return;
-    if (rank == 0 && threadIdx.x == 0)
-        p2_decided(p);
-    p2_worker<T, ALIGNED>(p);
 }
 
 // ===========================================================================
@@ -2152,10 +1699,8 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
 
     const uint32_t bad = check_inputs(p, b, g, temp);
     init_diagnostics(p, b, rank);
-    p2_start(p, rank);
     if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
         write_invalid(p, b, rank, bad);
-        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
     cluster_arrive_relaxed();  // paired with the wait before the first DSMEM store
@@ -2180,10 +1725,9 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     if (wid == 0)
         gather_logits<T>(p, s, lane, gt);
     exchange_rows(sh, s, nrows);
-    const bool go = decide_and_write<T>(p, sh, s, gt);  // uniform over the cluster; no DSMEM access follows
-    if (go)
-        chain_pass2<T, ALIGNED>(p, sh, s, sh.n);  // with a workspace: the record only
-    p2_leave<T, ALIGNED>(p, rank);
+    if (!decide_and_write<T>(p, sh, s, gt))
+        return;  // uniform over the cluster; no DSMEM access follows
+    chain_pass2<T, ALIGNED>(p, sh, s, sh.n);
 }
 
 // ===========================================================================
@@ -2215,10 +1759,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
 
     const uint32_t bad = check_inputs(p, b, g, temp);
     init_diagnostics(p, b, rank);
-    p2_start(p, rank);
     if (bad) {  // uniform over the cluster: every CTA leaves before any barrier
         write_invalid(p, b, rank, bad);
-        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
     if (tid == 0)
@@ -2350,9 +1892,9 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
                 count_round(p.counters, p.hist, g, n);
         }
     }
-    if (s.sampled && !bits)  // uniform over the cluster
-        chain_pass2<T, ALIGNED, STAGED>(p, sh, s, n, stage, STAGED ? stage + cap : nullptr);
-    p2_leave<T, ALIGNED>(p, rank);
+    if (!s.sampled || bits)
+        return;  // uniform over the cluster; no DSMEM access follows
+    chain_pass2<T, ALIGNED, STAGED>(p, sh, s, n, stage, STAGED ? stage + cap : nullptr);
 }
 
 // ===========================================================================
@@ -2404,12 +1946,10 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
         bad |= SPEC_STATUS_BAD_TREE;
     if (__syncthreads_or(bad_token))
         bad |= SPEC_STATUS_BAD_TOKEN;
-    p2_start(p, rank);
     if (bad) {
         write_invalid(p, b, rank, bad);
         if (rank == 0 && p.out_path && tid < N)
             p.out_path[base + tid] = -1;
-        p2_leave<T, ALIGNED>(p, rank);
         return;
     }
     if (tid < kMaxTree) {
@@ -2546,7 +2086,6 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
         write_invalid(p, b, rank, bits);
         if (rank == 0 && p.out_path && tid < N)
             p.out_path[base + tid] = -1;
-        p2_leave<T, ALIGNED>(p, rank);
         return;  // uniform over the cluster; no DSMEM access follows
     }
     if (rank == 0) {
@@ -2562,10 +2101,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
                 count_round(p.counters, p.hist, nn - 1, n);
         }
     }
-    if (!s.sampled) {
-        p2_leave<T, ALIGNED>(p, rank);
+    if (!s.sampled)
         return;
-    }
     P2Seq ps;
     ps.rt = exact_row(sh.row[0], temp);
     ps.rd = ps.rt;
@@ -2580,23 +2117,6 @@ __global__ void __launch_bounds__(kThreads, 4) spec_tree_kernel(const Params p)
     if (u >= 1.0f)
         u = __uint_as_float(0x3F7FFFFFu);
     const T *row = row_ptr<T>(p, s, node);
-    if (p.ws) {  // pass 2 as a record (with its zero set) for any CTA's tasks
-        if (rank == 0) {
-            if (tid == 0)
-                sh.n = p2_append(p, ps, row, row, p.out_tokens + base + n, nullptr, u);
-            __syncthreads();
-            const WsLayout L = ws_layout(p.B, p.ws_s2, true);
-            int *z = reinterpret_cast<int *>(p.ws + L.zsets) + (size_t)sh.n * kMaxTree;
-            for (int i = tid; i < tr.nrej; i += kThreads)
-                z[i] = tr.rej[i];
-            __threadfence();
-            __syncthreads();
-            if (tid == 0)
-                p2_publish(p, sh.n);
-        }
-        p2_leave<T, ALIGNED>(p, rank);
-        return;
-    }
     pass2_sample<T, ALIGNED, false>(sh, s, row, row, nullptr, nullptr, ps, u, p.out_tokens + base + n, nullptr);
 }
 

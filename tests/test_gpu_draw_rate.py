@@ -112,7 +112,7 @@ def test_sampler_full_rows(sv, oracle_mod, temp):
         assert tally.far == 0 and tally.mism < RATE * max(tally.picks, 100_000), (tally.mism, tally.picks)
 
 
-def _verify_draws(sv, t, d, tokens, u0, us, kernel, point=False, workspace=True):
+def _verify_draws(sv, t, d, tokens, u0, us, kernel, point=False):
     import torch
 
     B = t.shape[0]
@@ -130,30 +130,29 @@ def _verify_draws(sv, t, d, tokens, u0, us, kernel, point=False, workspace=True)
     out_t = torch.empty((k, B, 2), dtype=torch.int32, device=dev)
     out_n = torch.empty((k, B), dtype=torch.int32, device=dev)
     for i in range(k):
-        sv.verify(tl, dl, tok, nd, u_dev[i], temps, out_tokens=out_t[i], out_num_accepted=out_n[i], kernel=kernel,
-                  workspace=workspace)
+        sv.verify(tl, dl, tok, nd, u_dev[i], temps, out_tokens=out_t[i], out_num_accepted=out_n[i], kernel=kernel)
     torch.cuda.synchronize()
     return out_t.cpu().numpy(), out_n.cpu().numpy()
 
 
 @gpu
-@pytest.mark.parametrize("kernel,workspace", [(0, True), (3, True), (0, False)])
-def test_verify_bonus_rows(sv, oracle_mod, kernel, workspace):
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_verify_bonus_rows(sv, oracle_mod, kernel):
     t, d = _rows(256, 2, 9002)
     B = t.shape[0]
     us = _uniforms(B, 400, 41)
     tokens = np.zeros(B, np.int32)  # accepted whatever it is: u = 0 and p(x) > 0
-    out_t, out_n = _verify_draws(sv, t, d, tokens, 0.0, us, kernel, workspace=workspace)
+    out_t, out_n = _verify_draws(sv, t, d, tokens, 0.0, us, kernel)
     assert (out_n == 1).all()
     ref, margins = _oracle(oracle_mod, t[:, 1], us, 1.0)
     tally = Tally()
     tally.add(out_t[:, :, 1], ref, margins)
-    tally.check(f"bonus rows, kernel {kernel}, workspace {workspace}")
+    tally.check(f"bonus rows, kernel {kernel}")
 
 
 @gpu
-@pytest.mark.parametrize("kernel,workspace", [(0, True), (3, True), (0, False)])
-def test_verify_residual_rows(sv, oracle_mod, kernel, workspace):
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_verify_residual_rows(sv, oracle_mod, kernel):
     t, d = _rows(256, 2, 9003)
     B = t.shape[0]
     tf = workloads.bf16_bits_to_f64(t[:, 0])
@@ -164,12 +163,12 @@ def test_verify_residual_rows(sv, oracle_mod, kernel, workspace):
     q /= q.sum(axis=1, keepdims=True)
     tokens = np.argmax(q - p, axis=1).astype(np.int32)  # q(x) > p(x): rejected when u is just below 1
     us = _uniforms(B, 400, 51)
-    out_t, out_n = _verify_draws(sv, t, d, tokens, BELOW_ONE, us, kernel, workspace=workspace)
+    out_t, out_n = _verify_draws(sv, t, d, tokens, BELOW_ONE, us, kernel)
     assert (out_n == 0).all()
     ref, margins = _oracle(oracle_mod, t[:, 0], us, 1.0, mode=oracle_mod.PICK_RESIDUAL, d_rows=d[:, 0])
     tally = Tally()
     tally.add(out_t[:, :, 0], ref, margins)
-    tally.check(f"residual rows, kernel {kernel}, workspace {workspace}")
+    tally.check(f"residual rows, kernel {kernel}")
 
 
 @gpu

@@ -3,7 +3,7 @@ launches a fixed-shape step): the replay gives the bits of the eager call.
 Each call runs eagerly first, so the one-time per-device set-up (kernel
 attributes, cluster occupancy queries) happens outside the capture; what the
 host code does on every call (argument checks, the launch shape, the
-residency check of the early-exit and ring kernels) runs inside it."""
+residency check of the early-exit kernel) runs inside it."""
 import numpy as np
 import pytest
 

@@ -22,17 +22,17 @@ def sv():
     return m
 
 
-def run_debug(sv, batch, kernel=0, workspace=True):
+def run_debug(sv, batch, kernel=0):
     import torch
 
     dev = sv.to_device(batch)
-    d = sv.verify_debug(**dev, kernel=kernel, workspace=workspace)
+    d = sv.verify_debug(**dev, kernel=kernel)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in d.items()}
 
 
-def check_batch(sv, oracle_mod, batch, diagnostics=True, kernel=0, workspace=True):
-    d = run_debug(sv, batch, kernel, workspace)
+def check_batch(sv, oracle_mod, batch, diagnostics=True, kernel=0):
+    d = run_debug(sv, batch, kernel)
     ref = oracle_mod.verify_batch(batch)
     rep = parity.compare(batch, d["out_tokens"], d["out_num_accepted"], ref, gpu_status=d["seq_status"])
     assert rep.mismatches_far == 0, (str(rep), rep.far_detail[:5])
@@ -48,31 +48,11 @@ def check_batch(sv, oracle_mod, batch, diagnostics=True, kernel=0, workspace=Tru
 
 
 @gpu
-@pytest.mark.parametrize("workspace", [True, False])
 @pytest.mark.parametrize("cfg,greedy", [(1, False), (2, False), (2, True), (3, False), (4, False), (5, False)])
-def test_config_parity(sv, oracle_mod, cfg, greedy, workspace):
-    """workspace=True: pass 2 as the second launch; False: inside the verification kernel."""
+def test_config_parity(sv, oracle_mod, cfg, greedy):
     batch = workloads.make_config(cfg, greedy=greedy)
-    rep, d, ref = check_batch(sv, oracle_mod, batch, workspace=workspace)
-    print(f"cfg{cfg}{'-greedy' if greedy else ''} workspace={workspace}: {rep}")
-
-
-@gpu
-@pytest.mark.parametrize("kernel", [0, 3])
-@pytest.mark.parametrize("cfg", [3, 4, 5])
-def test_workspace_and_one_kernel_agree(sv, cfg, kernel):
-    """The two pass-2 paths sum the same integer weights: identical tokens."""
-    import torch
-
-    batch = workloads.make_config(cfg, B=96 if cfg == 5 else None)
-    dev = sv.to_device(batch)
-    a = [t.clone() for t in sv.verify(**dev, kernel=kernel, workspace=True)]
-    b = sv.verify(**dev, kernel=kernel, workspace=False)
-    ws = torch.zeros(sv.workspace_size(batch.B, batch.V, sv.SPEC_BF16) + 256, dtype=torch.uint8, device="cuda")
-    c = sv.verify(**dev, kernel=kernel, workspace=ws)
-    torch.cuda.synchronize()
-    for x, y, z in zip(a, b, c):
-        assert torch.equal(x, y) and torch.equal(x, z)
+    rep, d, ref = check_batch(sv, oracle_mod, batch)
+    print(f"cfg{cfg}{'-greedy' if greedy else ''}: {rep}")
 
 
 @gpu
