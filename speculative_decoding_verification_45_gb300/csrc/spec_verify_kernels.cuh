@@ -81,6 +81,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kUnroll = 8;         // pass 1: 16-byte loads in flight per thread
 constexpr int kMaxOrdered = 1024;  // longest-first scheduling for B up to this
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLog2eLo = (float)(1.4426950408889634073599 - (double)kLog2e);  // log2(e) - kLog2e
 constexpr float kLn2 = 0.69314718055994531f;
 
 struct Params {
@@ -389,16 +390,17 @@ struct RowAcc {
     }
 };
 
-// floor(w * 2^60) for a finite w in [0, 16), by integer operations only (a
-// float-to-64-bit-integer conversion instruction would run on the FP64 pipe).
-__device__ __forceinline__ unsigned long long to_fixed60(float w)
+// floor(w * 2^(60 - sc)) for a finite w >= 0 with w * 2^(60 - sc) < 2^64, by
+// integer operations only (a float-to-64-bit-integer conversion instruction
+// would run on the FP64 pipe).  sc = 0: w on the 2^-60 grid itself.
+__device__ __forceinline__ unsigned long long to_fixed60(float w, int sc = 0)
 {
     const uint32_t bits = __float_as_uint(w);
     const int ex = (int)(bits >> 23);  // w >= 0: no sign bit
     if (ex == 0)
         return 0ull;  // zero or below 2^-126, far under the 2^-60 unit
     const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
-    const int sh = ex - 90;  // w = mant * 2^(ex - 150), so w * 2^60 = mant * 2^(ex - 90)
+    const int sh = ex - 90 - sc;  // w = mant * 2^(ex - 150), so w * 2^(60 - sc) = mant * 2^(ex - 90 - sc)
     if (sh >= 0)
         return mant << sh;
     if (sh <= -24)
@@ -417,16 +419,24 @@ __device__ __forceinline__ unsigned long long to_fixed60(float w)
 // change about one full-row draw in a thousand against the float64
 // definition; a residual max(0, p - q) of small total amplifies that by
 // 1/total.  Pass 2 therefore puts every weight on a 2^-60 integer grid:
-//   * a "heavy" id, whose float32 weight is within a factor 2^kHeavySpan of the
-//     row's largest, gets 2^(l*K - mref) to about 2^-36 relative (exact_weight:
+//   * a "heavy" id, with l*K above m - kHeavySpan - 1 for the row's integer
+//     maximum m, gets 2^(l*K - mref) to about 2^-36 relative (exact_weight:
 //     K = log2(e)/T as a float-float pair, a float-float table of 2^(i/32) and
 //     a degree-4 polynomial for the rest -- the table-driven exponential of
 //     P. T. P. Tang, ACM TOMS 15(2), 1989 -- with Dekker's exact product and
 //     Knuth's exact sum splits);
-//   * every other id keeps ex2.approx(l*K - mref) in float32, summed in float32
-//     per chunk in id order and rounded to the grid once per chunk.  These ids
-//     hold at most ~V * 2^-kHeavySpan of the top weight, and their errors are
-//     unbiased.
+//   * every other id keeps a float32 weight ex2.approx(l*K - mf), summed in
+//     float32 per chunk in id order and rounded to the grid once per chunk
+//     (an exact power-of-two rescale by 2^-sf on the way).  The fast
+//     reference mf = m - kFastRef puts the heavy threshold at argument 0, so
+//     the ids just below it, whose weights carry the largest absolute errors,
+//     get arguments with rounding errors under 2^-24: what is left is
+//     ex2.approx's own relative error (~2^-22).  The same reference at the
+//     grid's mref would leave arguments near -kHeavySpan - ez, rounded to
+//     2^-20.  A draw's chance to land between two versions of a boundary
+//     grows with V * err * sqrt(threshold weight), so the 4x smaller error
+//     lets the threshold rise 16x (span 18 -> 14) at the same bound; on the
+//     V = 128256, T = 1 Zipf rows that cuts the heavy ids from 17 % to 4 %.
 // Sums of grid integers are exact and order-free, so every CTA and every pass
 // sees the same boundaries.  A residual max(0, p - q) = max(0, a/A - b/B) (a, b
 // the target and draft weights, A, B their row totals) is sampled as the
@@ -434,7 +444,8 @@ __device__ __forceinline__ unsigned long long to_fixed60(float w)
 // p > q; a sum over J is then A_J*B - B_J*A, so a single sweep that keeps A_J
 // and B_J per warp range and A, B per row is enough.  (An id that float32
 // misplaces in J has |p - q| ~ 1e-7 p, so its contribution is negligible.)
-constexpr float kHeavySpan = 18.0f;  // log2 of the heavy window below the top weight
+constexpr float kHeavySpan = 14.0f;  // log2 of the heavy window below the top weight
+constexpr float kFastRef = kHeavySpan + 1.0f;  // fast path: reference this far below the row's max
 constexpr int kP2Unroll = 4;         // pass-2 sweep: chunks in flight per thread (one row; half each for two)
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic rounds x to an integer for |x| < 2^22
 constexpr float kLn2Lo = -1.9046542121259336e-09f;  // ln 2 - (float)ln 2
@@ -469,14 +480,17 @@ constexpr Exp2Table make_exp2_table()
 }
 __device__ const Exp2Table kExp2Table = make_exp2_table();
 
-// One row's weight scale: weight_j = 2^(l_j * K - mref), K = khi + klo.
+// One row's weight scale: weight_j = 2^(l_j * K - mref), K = khi + klo.  The
+// fast path works in units 2^sf times larger, fast weight 2^(l_j * K - mf)
+// with mf = mref - sf, so that the heavy threshold sits at fast argument 0.
 struct ExactRow {
     float khi, klo;  // log2(e)/T as a float-float pair
-    float nmref;     // -mref (integer-valued)
+    float nmf;       // -mf (integer-valued)
+    int sf;          // mref - mf: grid weight = fast weight * 2^-sf
     int e60;         // 60 - mref: weight * 2^60 = 2^(n + e60) * 2^f
-    float heavy;     // fast argument above this: exact weight (+inf: none)
+    float heavy;     // fast argument above this: exact weight (0, or +inf: none)
     bool wide;       // |l * K| may pass 2^12: fold the product's low part in first
-    float c;         // 2^ez / Z: float32 probability = fast weight * c (the set J)
+    float c;         // 2^-kFastRef / Z: float32 probability = fast weight * c (the set J)
 };
 
 // floor((s + lo) * 2^E) for a normalised float-float pair (s in [1/2, 2),
@@ -497,15 +511,16 @@ __device__ __forceinline__ unsigned long long fixed_pair(float s, float lo, int 
     return (unsigned long long)M >> (-sh);
 }
 
-// round(v * 2^60) for a float v with |v| < 8, signed, by integer operations.
-__device__ __forceinline__ long long fixed60_signed(float v)
+// v * 2^(60 - sc), truncated towards zero, for a float v with |v| * 2^(60 - sc)
+// < 2^63, signed, by integer operations.
+__device__ __forceinline__ long long fixed60_signed(float v, int sc = 0)
 {
     const uint32_t b = __float_as_uint(v);
     const int ex = (int)((b >> 23) & 0xFFu);
     if (ex == 0)
         return 0;  // zero or below 2^-126
     const unsigned long long mant = (b & 0x7FFFFFu) | 0x800000u;
-    const int sh = ex - 90;  // |v| * 2^60 = mant * 2^(ex - 90)
+    const int sh = ex - 90 - sc;  // |v| * 2^(60 - sc) = mant * 2^(ex - 90 - sc)
     const unsigned long long mag = sh >= 0 ? mant << sh : (sh <= -24 ? 0ull : mant >> (-sh));
     return (b >> 31) ? -(long long)mag : (long long)mag;
 }
@@ -585,19 +600,28 @@ struct P2Seq {
 __device__ __forceinline__ ExactRow exact_row(const RowStat &st, float temp)
 {
     ExactRow er;
-    const double K = 1.4426950408889634 / (double)temp;
-    er.khi = __double2float_rd(K);  // so that klo > 0: l = -inf gives -inf, not NaN
-    er.klo = (float)(K - (double)er.khi);
+    // K = (kLog2e + kLog2eLo) / temp as a float-float pair, by float32
+    // operations only (FP64 is a slow pipe on this GPU): q = RN(kLog2e / temp)
+    // leaves the exact remainder kLog2e - q * temp (one FMA).  khi is then
+    // stepped one ulp down when needed so that klo > 0: l = -inf must give
+    // -inf, not -inf + inf.
+    const float q = __fdiv_rn(kLog2e, temp);
+    const float rem = __fmaf_rn(-q, temp, kLog2e);
+    const float lo = __fdiv_rn(__fadd_rn(rem, kLog2eLo), temp);  // |lo| <= ulp(q) / 2
+    er.khi = lo > 0.0f ? q : __uint_as_float(__float_as_uint(q) - 1u);
+    er.klo = lo > 0.0f ? lo : __fadd_rn(lo, __fsub_rn(q, er.khi));
     const float z = st.hi + st.lo;  // >= 1/2
     const int ez = (int)((__float_as_uint(z) >> 23) & 0xFFu) - 126;  // z < 2^ez
     const float mref = st.m + (float)ez;
-    er.nmref = -mref;
+    er.nmf = kFastRef - st.m;  // mf = m - kFastRef
+    er.sf = ez + (int)kFastRef;
     er.e60 = 60 - (int)mref;
     const float am = fabsf(st.m) + 48.0f;  // bound on |l * K| over heavy ids
     er.wide = am >= 4096.0f;
-    // heavy: fast weight above 2^-kHeavySpan of the largest (which is >= 2^(-ez-1))
-    er.heavy = am < 2097152.0f ? -(kHeavySpan + 1.0f + (float)ez) : INFINITY;
-    er.c = (float)(ldexp(1.0, ez) / (double)z);
+    // heavy: weight above 2^-(kHeavySpan + 1) of the row's largest l * K, i.e.
+    // fast argument l * K - m + kFastRef above 0
+    er.heavy = am < 2097152.0f ? 0.0f : INFINITY;
+    er.c = __fdiv_rn(1.0f / (float)(1 << (int)kFastRef), z);
     return er;
 }
 
@@ -616,7 +640,7 @@ __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, in
 {
     constexpr int W = Elem<T>::W, P = W / 2;
     const float2 kh = make_float2(ps.rt.khi, ps.rt.khi), kl = make_float2(ps.rt.klo, ps.rt.klo);
-    const float2 nmt = make_float2(ps.rt.nmref, ps.rt.nmref), nmd = make_float2(ps.rd.nmref, ps.rd.nmref);
+    const float2 nmt = make_float2(ps.rt.nmf, ps.rt.nmf), nmd = make_float2(ps.rd.nmf, ps.rd.nmf);
     uint32_t inj = (1u << W) - 1u;
     if (!RESID && ps.mode == kP2Zero) {
         if (c == ps.zero_chunk)
@@ -1384,10 +1408,10 @@ __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const
                 const int c = base + u * 32 + lane;
                 float runt[Elem<T>::W], rund[Elem<T>::W];
                 const ChunkP2 o = p2_chunk<T, RESID>(tv[u], dv[u], c, ps, runt, rund);
-                jt += to_fixed60(o.jt);
+                jt += to_fixed60(o.jt, ps.rt.sf);
                 compensated_add(ath, atl, o.at);
                 if (RESID) {
-                    jd += to_fixed60(o.jd);
+                    jd += to_fixed60(o.jd, ps.rd.sf);
                     compensated_add(adh, adl, o.ad);
                 }
                 if (!__any_sync(0xffffffffu, o.heavy != 0))
@@ -1436,8 +1460,10 @@ __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const
     RangeSums r;
     r.jt = warp_sum_u64(jt);
     r.jd = warp_sum_u64(jd);
-    r.at = warp_sum_u64(hat + (unsigned long long)((long long)to_fixed60(ath) + fixed60_signed(atl)));
-    r.ad = warp_sum_u64(had + (unsigned long long)((long long)to_fixed60(adh) + fixed60_signed(adl)));
+    r.at = warp_sum_u64(hat + (unsigned long long)((long long)to_fixed60(ath, ps.rt.sf) +
+                                                    fixed60_signed(atl, ps.rt.sf)));
+    r.ad = warp_sum_u64(had + (unsigned long long)((long long)to_fixed60(adh, ps.rd.sf) +
+                                                    fixed60_signed(adl, ps.rd.sf)));
     return r;
 }
 
@@ -1474,7 +1500,7 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, c
             if (RESID)
                 dv = slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s);
             o = p2_chunk<T, RESID>(tv, dv, c, ps, runt, rund);
-            unsigned long long jt = to_fixed60(o.jt), jd = RESID ? to_fixed60(o.jd) : 0ull;
+            unsigned long long jt = to_fixed60(o.jt, ps.rt.sf), jd = RESID ? to_fixed60(o.jd, ps.rd.sf) : 0ull;
             for (uint32_t hm = o.heavy; hm; hm &= hm - 1u) {
                 const int bit = __ffs(hm) - 1, e = bit & 7;
                 if (!((o.inj >> e) & 1u))
@@ -1530,8 +1556,8 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, c
                         wv += y;
                 }
                 const unsigned long long pd = __shfl_sync(0xffffffffu, wv, W + e);
-                const unsigned long long at = to_fixed60(rt_e) + wv;
-                const i128 cum = RESID ? p2_value(at, to_fixed60(rd_e) + pd, A, B) : (i128)at;
+                const unsigned long long at = to_fixed60(rt_e, ps.rt.sf) + wv;
+                const i128 cum = RESID ? p2_value(at, to_fixed60(rd_e, ps.rd.sf) + pd, A, B) : (i128)at;
                 const unsigned hit = __ballot_sync(0xffffffffu, lane < W && off_s < cum);
                 if (lane == 0)
                     *outn = (base + first) * W + (hit ? __ffs(hit) - 1 : W - 1);  // chunk base + first
