@@ -28,11 +28,11 @@
  *           smallest id j with u * S < C_j, C_j the running sum of the weights
  *           in id order and S their total.  The weights are integers on a
  *           2^-60 grid, each within about 2^-36 of its exact value where it
- *           matters (ids whose weight is within a factor 2^20 of the row's
- *           largest; float32 for the rest), so every sum is exact and y
- *           differs from the float64 definition only when u lies within
- *           ~1e-10 of a boundary C_j / S (rows whose |logit| * log2(e) / T
- *           passes 2^21 keep float32 weights throughout).
+ *           matters (ids whose weight is within a factor 2^15 of the row's
+ *           largest; float32, to about 2^-22, for the rest), so every sum is
+ *           exact and y differs from the float64 definition only when u lies
+ *           within ~1e-9 of a boundary C_j / S (rows whose
+ *           |logit| * log2(e) / T passes 2^21 keep float32 weights throughout).
  *   T == 0: greedy; a_i = argmax of the raw target logits of row i (lowest id
  *           on ties); position i accepts iff x_i == a_i; y = a_n.  No draft row
  *           and no uniform is read.
@@ -139,7 +139,7 @@ spec_status spec_verify(const void *target_logits, const void *draft_logits, con
  * normalisers are merged from per-CTA partials, so the split of a row (the
  * cluster size) and the kernel variant move p-hat and q-hat by about 1e-7
  * relative, and an accept test that close to its threshold (or a final draw
- * within ~1e-10 of a CDF boundary) may come out differently.  Greedy (T == 0)
+ * within ~1e-9 of a CDF boundary) may come out differently.  Greedy (T == 0)
  * results never change. */
 typedef struct spec_verify_options {
     int cluster_size; /* CTAs sharing one sequence's rows: 0 = automatic, else 1 to 16 */

@@ -37,13 +37,13 @@
 //     draft when a draft was rejected) and puts every sampling weight on an
 //     exact 2^-60 integer grid: ids near the top of the row get an extended-
 //     precision exp2 (about 2^-36 relative), the rest their float32 value, so
-//     that the draw agrees with the float64 definition except within ~1e-10
+//     that the draw agrees with the float64 definition except within ~1e-9
 //     of a boundary (see "pass 2" below).  Per-warp and per-CTA sums cross the
 //     cluster over DSMEM; the CTA whose slice holds floor(u*S) recomputes one
 //     warp range of it and writes the id.
 //
 // Kernels sharing that protocol:
-//   spec_verify_stream_kernel (default) 128-bit loads straight into registers,
+//   spec_verify_stream_kernel (full sweep) 128-bit loads straight into registers,
 //                             32 reducing warps per SM; element loads when rows
 //                             are not 16-byte aligned; variants that read
 //                             several rows per round trip for narrow slices.
@@ -634,11 +634,31 @@ struct ChunkP2 {
     uint32_t inj;          // bit e: id e in J
 };
 
-template <typename T, bool RESID>
+template <typename T, bool RESID, bool FULL = false>
 __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, int c, const P2Seq &ps,
                                             float (&runt)[Elem<T>::W], float (&rund)[Elem<T>::W])
 {
     constexpr int W = Elem<T>::W, P = W / 2;
+    if constexpr (FULL) {  // p itself (J = every id): one sum, no J flags
+        const float2 kh = make_float2(ps.rt.khi, ps.rt.khi), kl = make_float2(ps.rt.klo, ps.rt.klo);
+        const float2 nmt = make_float2(ps.rt.nmf, ps.rt.nmf);
+        ChunkP2 o{0.0f, 0.0f, 0.0f, 0.0f, 0u, (1u << W) - 1u};
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+            const float2 l = pair<T>(tv, q);
+            float2 y = __ffma2_rn(l, kh, nmt);
+            y = __ffma2_rn(l, kl, y);
+            const float2 w = ex2_pair(y);
+            const bool h0 = y.x > ps.rt.heavy, h1 = y.y > ps.rt.heavy;
+            o.heavy |= ((uint32_t)h0 << (2 * q)) | ((uint32_t)h1 << (2 * q + 1));
+            o.jt = __fadd_rn(o.jt, h0 ? 0.0f : w.x);
+            runt[2 * q] = o.jt;
+            o.jt = __fadd_rn(o.jt, h1 ? 0.0f : w.y);
+            runt[2 * q + 1] = o.jt;
+        }
+        o.at = o.jt;
+        return o;
+    }
     const float2 kh = make_float2(ps.rt.khi, ps.rt.khi), kl = make_float2(ps.rt.klo, ps.rt.klo);
     const float2 nmt = make_float2(ps.rt.nmf, ps.rt.nmf), nmd = make_float2(ps.rd.nmf, ps.rd.nmf);
     uint32_t inj = (1u << W) - 1u;
@@ -1381,7 +1401,7 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 // its heavy ids are queued (slot, lane, id, J) and spread over the lanes, 32
 // exact weights at a time, while the batch's chunks wait in shared memory.
 // All threads of the warp call it.
-template <typename T, bool ALIGNED, bool RESID, bool STAGED>
+template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
 __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const T *drow, const uint4 *tst,
                                               const uint4 *dst, const P2Seq &ps, P2Smem &sm)
 {
@@ -1407,7 +1427,7 @@ __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const
                     break;  // uniform over the warp
                 const int c = base + u * 32 + lane;
                 float runt[Elem<T>::W], rund[Elem<T>::W];
-                const ChunkP2 o = p2_chunk<T, RESID>(tv[u], dv[u], c, ps, runt, rund);
+                const ChunkP2 o = p2_chunk<T, RESID, FULL>(tv[u], dv[u], c, ps, runt, rund);
                 jt += to_fixed60(o.jt, ps.rt.sf);
                 compensated_add(ath, atl, o.at);
                 if (RESID) {
@@ -1481,7 +1501,7 @@ __device__ __forceinline__ double i128_to_double(i128 v)
 // recomputed chunk by chunk with the sweep's arithmetic (identical bits), one
 // chunk per thread and pass; a block scan finds the chunk, its thread the id
 // from the running sums in id order.  All threads of the CTA call it.
-template <typename T, bool ALIGNED, bool RESID, bool STAGED>
+template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
 __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, const T *trow, const T *drow,
                                       const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0, int r1, i128 rel,
                                       unsigned long long A, unsigned long long B, int32_t *outn)
@@ -1499,7 +1519,7 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, c
             tv = slice_chunk<T, ALIGNED, STAGED>(trow, tst, c, s);
             if (RESID)
                 dv = slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s);
-            o = p2_chunk<T, RESID>(tv, dv, c, ps, runt, rund);
+            o = p2_chunk<T, RESID, FULL>(tv, dv, c, ps, runt, rund);
             unsigned long long jt = to_fixed60(o.jt, ps.rt.sf), jd = RESID ? to_fixed60(o.jd, ps.rd.sf) : 0ull;
             for (uint32_t hm = o.heavy; hm; hm &= hm - 1u) {
                 const int bit = __ffs(hm) - 1, e = bit & 7;
@@ -1578,7 +1598,7 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, c
 // that hold all of it) samples p instead.  mass_out (rank 0; may be NULL):
 // the normalised total (residual mass, or 1 - p(removed ids)).  All threads
 // of every CTA of the cluster call it.
-template <typename T, bool ALIGNED, bool STAGED>
+template <typename T, bool ALIGNED, bool STAGED, bool ONE_ROW = false>
 __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T *trow, const T *drow,
                                           const uint4 *tst, const uint4 *dst, P2Seq ps, float u, int32_t *outn,
                                           float *mass_out)
@@ -1593,8 +1613,9 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     bool resid = false;
     for (;; ++att) {
         resid = ps.mode == kP2Residual;
-        const RangeSums r = resid ? p2_sweep<T, ALIGNED, true, STAGED>(s, trow, drow, tst, dst, ps, sm)
-                                  : p2_sweep<T, ALIGNED, false, STAGED>(s, trow, drow, tst, dst, ps, sm);
+        const RangeSums r = ONE_ROW ? p2_sweep<T, ALIGNED, false, STAGED, true>(s, trow, drow, tst, dst, ps, sm)
+                            : resid   ? p2_sweep<T, ALIGNED, true, STAGED>(s, trow, drow, tst, dst, ps, sm)
+                                      : p2_sweep<T, ALIGNED, false, STAGED>(s, trow, drow, tst, dst, ps, sm);
         if (lane == 0) {
             sh.p2w[wid][0] = r.jt;
             sh.p2w[wid][1] = r.jd;
@@ -1659,7 +1680,10 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     }
     int r0, r1;
     warp_range(s, w, r0, r1);
-    if (resid)
+    if (ONE_ROW)
+        p2_owner<T, ALIGNED, false, STAGED, true>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
+                                                  outn);
+    else if (resid)
         p2_owner<T, ALIGNED, true, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
     else
         p2_owner<T, ALIGNED, false, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
@@ -1690,7 +1714,7 @@ __device__ __forceinline__ P2Seq chain_p2seq(const SharedState &sh, const Seq &s
 // across its cluster.  STAGED: tst and dst hold this CTA's slices of rows t_n
 // and d_n (early exit with rows in host memory), so pass 2 reads neither row
 // again.
-template <typename T, bool ALIGNED, bool STAGED = false>
+template <typename T, bool ALIGNED, bool POINT, bool STAGED = false>
 __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, const Seq &s, int n,
                                             const uint4 *tst = nullptr, const uint4 *dst = nullptr)
 {
@@ -1701,7 +1725,17 @@ __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, co
     const T *drow = rows ? row_ptr<T>(p, s, g + 1 + n) : trow;
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
     float *mass = p.resid_mass ? p.resid_mass + b : nullptr;
-    pass2_sample<T, ALIGNED, STAGED>(sh, s, trow, drow, tst, rows ? dst : tst, ps, final_uniform(p, s), outn, mass);
+    // Rows of one-row calls (gamma_max = 0 and no draft rows: the sampler) are
+    // always p and take a pass 2 specialised for it, a separate function in the
+    // point-mass instantiations only, so that the verify kernels' code is
+    // unchanged (B = 256, V = 128256 sampler: 53.4 against 56.9 us; folding
+    // the specialisation into the shared function cost the verify kernels
+    // 1-2 us).
+    if (POINT && s.gmax == 0)
+        pass2_sample<T, ALIGNED, STAGED, true>(sh, s, trow, drow, tst, tst, ps, final_uniform(p, s), outn, mass);
+    else
+        pass2_sample<T, ALIGNED, STAGED>(sh, s, trow, drow, tst, rows ? dst : tst, ps, final_uniform(p, s), outn,
+                                         mass);
 }
 
 // ===========================================================================
@@ -1753,7 +1787,7 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     exchange_rows(sh, s, nrows);
     if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; no DSMEM access follows
-    chain_pass2<T, ALIGNED>(p, sh, s, sh.n);
+    chain_pass2<T, ALIGNED, POINT>(p, sh, s, sh.n);
 }
 
 // ===========================================================================
@@ -1920,7 +1954,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     }
     if (!s.sampled || bits)
         return;  // uniform over the cluster; no DSMEM access follows
-    chain_pass2<T, ALIGNED, STAGED>(p, sh, s, n, stage, STAGED ? stage + cap : nullptr);
+    chain_pass2<T, ALIGNED, POINT, STAGED>(p, sh, s, n, stage, STAGED ? stage + cap : nullptr);
 }
 
 // ===========================================================================
