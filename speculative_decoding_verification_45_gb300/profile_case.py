@@ -2,12 +2,13 @@
 profilers (ncu) and quick timing:
 
     python -m speculative_decoding_verification_45_gb300.profile_case \
-        {verify,early,tree,sample,ngram} [--reps N] [--host]
+        {verify,full,early,tree,sample,ngram} [--reps N] [--host] [--config C]
 
-verify / early : spec_verify (full sweep / row-ordered early exit) on the
-                 B=256, gamma=4, V=128256 bf16 workload; with --host the
-                 inputs stay in page-locked host memory and the kernels read
-                 them over the host link (zero copy)
+verify         : spec_verify with the automatic kernel choice on workload
+                 --config (default 5: B=256, gamma=4, V=128256 bf16)
+full / early   : the same with the full sweep / the row-ordered early exit;
+                 with --host the inputs stay in page-locked host memory and
+                 the kernels read them over the host link (zero copy)
 tree           : spec_tree_verify, 32 sequences of 64-node Medusa-style trees
                  over V=128256 (half greedy, half T=1)
 sample         : spec_sample, 256 rows of V=128256 (target-only round)
@@ -27,20 +28,25 @@ def main(argv=None):
     from speculative_decoding_verification_45_gb300 import workloads
 
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("case", choices=["verify", "early", "tree", "sample", "ngram"])
+    ap.add_argument("case", choices=["verify", "full", "early", "tree", "sample", "ngram"])
     ap.add_argument("--reps", type=int, default=10)
-    ap.add_argument("--host", action="store_true", help="verify/early: inputs in page-locked host memory")
+    ap.add_argument("--host", action="store_true", help="verify/full/early: inputs in page-locked host memory")
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5],
+                    help="verify/full/early: the workload (sample, tree, ngram use config 5's sizes)")
     args = ap.parse_args(argv)
     sv.build()
     torch.cuda.set_device(0)
-    batch = workloads.make_config(5)
-    if args.case in ("verify", "early", "sample"):
+    batch = workloads.make_config(args.config if args.case in ("verify", "full", "early") else 5)
+    if args.case in ("verify", "full", "early", "sample"):
         dev = sv.to_device(batch)
         if args.host and args.case != "sample":
             dev = {k: v.cpu().pin_memory() for k, v in dev.items()}
     if args.case == "verify":
         def call():
             sv.verify(**dev)
+    elif args.case == "full":
+        def call():
+            sv.verify(**dev, kernel=sv.KERNEL_REGISTER)
     elif args.case == "early":
         def call():
             sv.verify(**dev, kernel=sv.KERNEL_EARLY)

@@ -199,7 +199,10 @@ def test_host_inputs_sample_tree_ngram(sv):
     logits = dev["target_logits"][:, 0].contiguous()
     u = dev["uniforms"][:, 0].contiguous()
     a = sv.sample(logits, u, dev["temperature"])
-    b = sv.sample(logits.cpu().pin_memory(), u.cpu().pin_memory(), dev["temperature"].cpu().pin_memory())
+    # named page-locked inputs, alive until the synchronisation below (the rule
+    # the header states; the binding also holds them until the stream passes)
+    logits_h, u_h, temp_h = logits.cpu().pin_memory(), u.cpu().pin_memory(), dev["temperature"].cpu().pin_memory()
+    b = sv.sample(logits_h, u_h, temp_h)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
 
@@ -213,7 +216,8 @@ def test_host_inputs_sample_tree_ngram(sv):
 
     ctx, lens = workloads.ngram_contexts(16, 1024, 500, seed=5)
     ca = sv.ngram_propose(torch.from_numpy(ctx).cuda(), torch.from_numpy(lens).cuda(), 1, 4, 6)
-    cb = sv.ngram_propose(torch.from_numpy(ctx).pin_memory(), torch.from_numpy(lens).pin_memory(), 1, 4, 6)
+    ctx_h, lens_h = torch.from_numpy(ctx).pin_memory(), torch.from_numpy(lens).pin_memory()
+    cb = sv.ngram_propose(ctx_h, lens_h, 1, 4, 6)
     torch.cuda.synchronize()
     for x, y in zip(ca, cb):
         np.testing.assert_array_equal(x.cpu().numpy(), y.cpu().numpy())
@@ -270,3 +274,29 @@ def test_host_inputs_random_batches(sv, oracle_mod, seed):
     assert int(st_h.item()) == int(st_d.item())
     rep = parity.compare(batch, got[0].cpu().numpy(), got[1].cpu().numpy(), oracle_mod.verify_batch(batch))
     assert rep.mismatches_far == 0, rep.far_detail[:3]
+
+
+@gpu
+def test_page_locked_inputs_held_until_the_stream_passes(sv):
+    """The binding keeps page-locked inputs referenced until an event recorded
+    after the launch has completed, so torch's pinned-memory cache cannot hand
+    a block to someone else while the kernel still reads it over the link."""
+    import weakref
+
+    import torch
+
+    batch = workloads.make_config(5, B=32)
+    dev = sv.to_device(batch)
+    ref_t, ref_n = sv.verify(**dev, kernel=sv.KERNEL_EARLY)
+    torch.cuda.synchronize()
+    host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+    refs = [weakref.ref(t) for t in host.values()]
+    toks, num = sv.verify(**host, kernel=sv.KERNEL_EARLY)
+    del host
+    assert all(r() is not None for r in refs)  # only the binding holds them now
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(toks.cpu().numpy(), ref_t.cpu().numpy())
+    np.testing.assert_array_equal(num.cpu().numpy(), ref_n.cpu().numpy())
+    sv.verify(**dev, kernel=sv.KERNEL_EARLY)  # a later call drops the references whose event has completed
+    torch.cuda.synchronize()
+    assert all(r() is None for r in refs)
