@@ -401,7 +401,9 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
         if ((uintptr_t)q & 3u)
             return SPEC_ERR_INVALID_ARG;
     const bool aligned = aligned16(target) && (!draft || aligned16(draft)) && ((size_t)V * (size_t)es) % 16 == 0;
-    const bool point = gmax > 0 && !draft;
+    // point-mass kernels also for gamma_max = 0 (the sampler: no draft rows at
+    // all), whose pass 2 is specialised for rows that are always p
+    const bool point = gmax == 0 || !draft;
     // automatic: full sweep or early exit (the debug call's row diagnostics
     // need the full sweep, which reads every row)
     if (want_kind < 0 && gmax > 0 && !p_hat && !q_hat && !logz_t && !logz_d) {
@@ -674,7 +676,7 @@ spec_status spec_verify_launch_shape(int B, int gamma_max, int V, spec_dtype dty
             want = aligned ? kKindEarlyAligned : kKindEarly;
     }
     Shape shp;
-    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, want, 0, &shp, false, gamma_max == 0);
+    spec_status st = resolve_shape(B > 0 ? B : 1, V, dtype, aligned, want, 0, &shp, gamma_max == 0, gamma_max == 0);
     if (st != SPEC_OK)
         return st;
     if (kernel)

@@ -491,6 +491,7 @@ struct ExactRow {
     float heavy;     // fast argument above this: exact weight (0, or +inf: none)
     bool wide;       // |l * K| may pass 2^12: fold the product's low part in first
     float c;         // 2^-kFastRef / Z: float32 probability = fast weight * c (the set J)
+    float koff;      // keep_flag offset: 1 (heavy above fast argument 0), +inf (no heavy ids)
 };
 
 // floor((s + lo) * 2^E) for a normalised float-float pair (s in [1/2, 2),
@@ -621,6 +622,7 @@ __device__ __forceinline__ ExactRow exact_row(const RowStat &st, float temp)
     // heavy: weight above 2^-(kHeavySpan + 1) of the row's largest l * K, i.e.
     // fast argument l * K - m + kFastRef above 0
     er.heavy = am < 2097152.0f ? 0.0f : INFINITY;
+    er.koff = am < 2097152.0f ? 1.0f : INFINITY;
     er.c = __fdiv_rn(1.0f / (float)(1 << (int)kFastRef), z);
     return er;
 }
@@ -634,6 +636,29 @@ struct ChunkP2 {
     uint32_t inj;          // bit e: id e in J
 };
 
+// sat(a * b + c) with subnormal inputs and results flushed to zero: with
+// |b| = 2^127 it maps every finite a to exactly 0 or 1 (NaN gives 0).
+__device__ __forceinline__ float fma_ftz_sat(float a, float b, float c)
+{
+    float d;
+    asm("fma.rn.ftz.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 1 for a tail id (fast argument at most 0, a subnormal counting as 0, or any
+// id of a row without exact weights, whose koff is +inf), 0 for a heavy one;
+// -inf gives 1.
+__device__ __forceinline__ float keep_flag(float y, const ExactRow &er)
+{
+    return fma_ftz_sat(y, -0x1p127f, er.koff);
+}
+
+// The low 8 bits of a float holding an integer in [0, 255].
+__device__ __forceinline__ uint32_t float_bits8(float m)
+{
+    return __float_as_uint(__fadd_rn(m, 8388608.0f)) & 0xFFu;
+}
+
 template <typename T, bool RESID, bool FULL = false>
 __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, int c, const P2Seq &ps,
                                             float (&runt)[Elem<T>::W], float (&rund)[Elem<T>::W])
@@ -643,19 +668,22 @@ __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, in
         const float2 kh = make_float2(ps.rt.khi, ps.rt.khi), kl = make_float2(ps.rt.klo, ps.rt.klo);
         const float2 nmt = make_float2(ps.rt.nmf, ps.rt.nmf);
         ChunkP2 o{0.0f, 0.0f, 0.0f, 0.0f, 0u, (1u << W) - 1u};
+        float tm = 0.0f;  // tail ids as a bit mask held in a float (exact below 2^24)
 #pragma unroll
         for (int q = 0; q < P; ++q) {
             const float2 l = pair<T>(tv, q);
             float2 y = __ffma2_rn(l, kh, nmt);
             y = __ffma2_rn(l, kl, y);
             const float2 w = ex2_pair(y);
-            const bool h0 = y.x > ps.rt.heavy, h1 = y.y > ps.rt.heavy;
-            o.heavy |= ((uint32_t)h0 << (2 * q)) | ((uint32_t)h1 << (2 * q + 1));
-            o.jt = __fadd_rn(o.jt, h0 ? 0.0f : w.x);
+            const float k0 = keep_flag(y.x, ps.rt), k1 = keep_flag(y.y, ps.rt);
+            tm = __fmaf_rn(k0, (float)(1 << (2 * q)), tm);
+            tm = __fmaf_rn(k1, (float)(2 << (2 * q)), tm);
+            o.jt = __fmaf_rn(w.x, k0, o.jt);
             runt[2 * q] = o.jt;
-            o.jt = __fadd_rn(o.jt, h1 ? 0.0f : w.y);
+            o.jt = __fmaf_rn(w.y, k1, o.jt);
             runt[2 * q + 1] = o.jt;
         }
+        o.heavy = ~float_bits8(tm) & ((1u << W) - 1u);
         o.at = o.jt;
         return o;
     }
@@ -672,23 +700,27 @@ __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, in
         }
     }
     ChunkP2 o{0.0f, 0.0f, 0.0f, 0.0f, 0u, 0u};
+    float tm = 0.0f, dm = 0.0f, jm = 0.0f;  // tail ids (target, draft) and J, as float bit masks
     // one id at a time, in id order (the running sums are sequential)
     auto step = [&](int e, float yt, float wt, float yd, float wd) {
-        const bool ht = yt > ps.rt.heavy;
-        const float a = ht ? 0.0f : wt;
-        bool j = (inj >> e) & 1u;
+        const float kt = keep_flag(yt, ps.rt);
+        const float a = __fmul_rn(wt, kt);
+        tm = __fmaf_rn(kt, (float)(1 << e), tm);
+        float jf;
         if (RESID) {
-            const bool hd = yd > ps.rd.heavy;
-            const float b = hd ? 0.0f : wd;
-            j = __fmul_rn(wt, ps.rt.c) > __fmul_rn(wd, ps.rd.c);
-            o.heavy |= (uint32_t)hd << (8 + e);
+            const float kd = keep_flag(yd, ps.rd);
+            const float b = __fmul_rn(wd, kd);
+            dm = __fmaf_rn(kd, (float)(1 << e), dm);
+            // J: p > q by the float32 probabilities, as an exact 0 or 1
+            jf = fma_ftz_sat(__fmaf_rn(wt, ps.rt.c, -__fmul_rn(wd, ps.rd.c)), 0x1p127f, 0.0f);
             o.ad = __fadd_rn(o.ad, b);
-            o.jd = __fadd_rn(o.jd, j ? b : 0.0f);
+            o.jd = __fmaf_rn(b, jf, o.jd);
+        } else {
+            jf = ((inj >> e) & 1u) ? 1.0f : 0.0f;
         }
-        o.heavy |= (uint32_t)ht << e;
-        o.inj |= (uint32_t)j << e;
+        jm = __fmaf_rn(jf, (float)(1 << e), jm);
         o.at = __fadd_rn(o.at, a);
-        o.jt = __fadd_rn(o.jt, j ? a : 0.0f);
+        o.jt = __fmaf_rn(a, jf, o.jt);
         runt[e] = o.jt;
         rund[e] = o.jd;
     };
@@ -708,6 +740,8 @@ __device__ __forceinline__ ChunkP2 p2_chunk(const uint4 &tv, const uint4 &dv, in
         step(2 * q, y.x, w.x, x.x, v.x);
         step(2 * q + 1, y.y, w.y, x.y, v.y);
     }
+    o.heavy = (~float_bits8(tm) & ((1u << W) - 1u)) | (RESID ? (~float_bits8(dm) & ((1u << W) - 1u)) << 8 : 0u);
+    o.inj = float_bits8(jm);
     return o;
 }
 
@@ -1725,12 +1759,12 @@ __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, co
     const T *drow = rows ? row_ptr<T>(p, s, g + 1 + n) : trow;
     int32_t *outn = p.out_tokens + (size_t)b * (s.gmax + 1) + n;
     float *mass = p.resid_mass ? p.resid_mass + b : nullptr;
-    // Rows of one-row calls (gamma_max = 0 and no draft rows: the sampler) are
-    // always p and take a pass 2 specialised for it, a separate function in the
-    // point-mass instantiations only, so that the verify kernels' code is
-    // unchanged (B = 256, V = 128256 sampler: 53.4 against 56.9 us; folding
-    // the specialisation into the shared function cost the verify kernels
-    // 1-2 us).
+    // Rows of one-row calls (gamma_max = 0: the sampler, which the host runs on
+    // the point-mass instantiations) are always p and take a pass 2
+    // specialised for it, a separate function in those instantiations only, so
+    // that the verify kernels' code is unchanged (B = 256, V = 128256 sampler:
+    // 53.4 against 56.9 us; folding the specialisation into the shared function
+    // cost the verify kernels 1-2 us).
     if (POINT && s.gmax == 0)
         pass2_sample<T, ALIGNED, STAGED, true>(sh, s, trow, drow, tst, tst, ps, final_uniform(p, s), outn, mass);
     else
