@@ -248,22 +248,24 @@ def _zipf_cfg(rng: np.random.Generator, B: int, gamma: int, V: int, ragged: bool
     return Batch(target, draft, tokens, num_draft, uniforms, temp, BF16, name)
 
 
-def zipf_sequences(B: int, rows: int, V: int, seed: int, sigma=(0.2, 2.0)):
+def zipf_sequences(B: int, rows: int, V: int, seed: int, sigma=(0.2, 2.0), dtype: str = BF16):
     """Rows of the large workloads' generator for the draw-rate tests: per
     sequence b one Zipf shift (a random permutation of ranks), target rows
     t_i ~ N(0, 3^2) + shift for i < rows, draft rows d_i = t_i + N(0, s_b^2)
-    for i < rows - 1 with s_b ~ U[sigma], all rounded to bfloat16.
-    Returns (target [B, rows, V], draft [B, rows - 1, V]) as bfloat16 bits."""
+    for i < rows - 1 with s_b ~ U[sigma], all rounded to dtype.
+    Returns (target [B, rows, V], draft [B, rows - 1, V]) as bfloat16 bits
+    (uint16) or float32."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    target = np.empty((B, rows, V), dtype=np.uint16)
-    draft = np.empty((B, max(rows - 1, 0), V), dtype=np.uint16)
+    store = np.uint16 if dtype == BF16 else np.float32
+    target = np.empty((B, rows, V), dtype=store)
+    draft = np.empty((B, max(rows - 1, 0), V), dtype=store)
     for b in range(B):
         shift = _zipf_shift(rng, V)
         t = rng.normal(0.0, 3.0, size=(rows, V)) + shift
         s_b = rng.uniform(sigma[0], sigma[1])
-        target[b] = _round(t, BF16)
+        target[b] = _round(t, dtype)
         if rows > 1:
-            draft[b] = _round(t[: rows - 1] + rng.normal(0.0, s_b, size=(rows - 1, V)), BF16)
+            draft[b] = _round(t[: rows - 1] + rng.normal(0.0, s_b, size=(rows - 1, V)), dtype)
     return target, draft
 
 

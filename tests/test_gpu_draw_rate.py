@@ -10,7 +10,8 @@ of them 1e-7 to 1e-9 apart, so this is a test of the weights' precision: each
 pick is compared with oracle.pick_many on the same row and uniform.
 
 Draws come from:
-  * spec_sample (target-only / draft-side sampling): 512 rows x 200 uniforms;
+  * spec_sample (target-only / draft-side sampling): 512 rows x 200 uniforms
+    (and 512 float32 rows of V = 32000 x 200);
   * spec_verify bonus rows: every draft accepted (accept uniform 0), 256
     sequences x 400 final uniforms, both kernels;
   * spec_verify residual rows: a rejection forced at position 0 (x = argmax of
@@ -84,6 +85,34 @@ def _bf16(a, dev):
     import torch
 
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+@gpu
+def test_sampler_full_rows_float32(sv, oracle_mod):
+    """float32 rows (4 ids per 16-byte chunk) of the same recipe at V = 32000:
+    the other chunk layout of the exact draw, 512 rows x 200 uniforms."""
+    import torch
+
+    V32 = 32000
+    t, _ = workloads.zipf_sequences(512, 1, V32, 9005, dtype="f32")
+    rows = t[:, 0]
+    us = _uniforms(rows.shape[0], 200, 33)
+    logits = torch.from_numpy(np.ascontiguousarray(rows)).to("cuda")
+    temps = torch.ones(rows.shape[0], dtype=torch.float32, device="cuda")
+    out = torch.empty((200, rows.shape[0]), dtype=torch.int32, device="cuda")
+    u_dev = torch.from_numpy(us).to("cuda")
+    for i in range(200):
+        sv.sample(logits, u_dev[i], temps, out_tokens=out[i])
+    torch.cuda.synchronize()
+    picks = np.empty((200, rows.shape[0]), np.int32)
+    margins = np.empty((200, rows.shape[0]), np.float64)
+    for b in range(rows.shape[0]):
+        p, m, _ = oracle_mod.pick_many(rows[b], "f32", 1.0, us[:, b])
+        picks[:, b] = p
+        margins[:, b] = m
+    tally = Tally()
+    tally.add(out.cpu().numpy(), picks, margins)
+    tally.check("sampler float32 T=1")
 
 
 @gpu
