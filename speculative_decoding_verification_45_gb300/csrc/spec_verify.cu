@@ -206,7 +206,8 @@ bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
 }
 
 // Automatic cluster size.  First the smallest power of two giving about six
-// CTAs per SM in the grid, at most 8 (16 for one or two sequences) and at least
+// CTAs per SM in the grid, at most 8 (16 for one or two sequences with long
+// rows, lone_cap) and at least
 // kThreads/2 chunks per CTA and row.  A thread reads its chunks of a row in
 // batches of kUnroll loads, and on GB300 the sweep time follows the number of
 // batches, not the bytes in the last one: when the slice leaves a second batch
@@ -217,10 +218,18 @@ bool cluster_launchable(int dev, spec_dtype dt, int kind, int C, bool point)
 // against 57 us at 8).
 int per_thread_chunks(int num_chunks, int C) { return ((num_chunks + C - 1) / C + kThreads - 1) / kThreads; }
 
+// One or two sequences with long rows (at least 512 chunks per CTA at 16) take
+// clusters of up to 16: B = 1, V = 128256 (config 3's rows): 22.5 us at 16
+// against 23.6 at 8; V = 151936: 12.7 against 17.6.  Shorter rows stop at 8,
+// where the cluster's barriers and exchanges cost more than the smaller
+// slices save: B = 1, V = 32000 (config 2): 25.6 us at 8 against 27.9 at 16
+// (graph replay, 10-call graphs).
+int lone_cap(int B, int num_chunks) { return (B <= 2 && num_chunks >= 16 * 512) ? 16 : 8; }
+
 int auto_cluster(int B, int num_chunks, int sms)
 {
     const long long target = 6LL * sms;
-    const int cap = B <= 2 ? 16 : 8;  // a lone sequence needs every CTA it can get
+    const int cap = lone_cap(B, num_chunks);
     int C = 1;
     while (C < cap && (long long)B * C < target && num_chunks / (C * 2) >= kThreads / 2)
         C *= 2;
@@ -240,7 +249,7 @@ int auto_cluster(int B, int num_chunks, int sms)
 // sampler).  Every cluster then does the same work, and a few long CTAs that
 // are all resident at once beat a grid of several waves for the streaming:
 // the largest power of two with B*C <= 2 * SMs (at most 8; 16 for one or two
-// rows).  But the final draw's exact weights (pass 2) cost several times the
+// long rows, lone_cap).  But the final draw's exact weights (pass 2) cost several times the
 // streaming's ALU work per byte and run on the row's own CTAs, so a long row
 // (at least 4096 chunks) is split over at least 4 CTAs.  Measured on GB300,
 // 10-call graphs, V = 128256 bf16, half the rows at T = 1: B = 256 takes
@@ -248,7 +257,7 @@ int auto_cluster(int B, int num_chunks, int sms)
 // at the first rule's 4 and 8.
 int sampler_cluster(int B, int num_chunks, int sms)
 {
-    const int cap = B <= 2 ? 16 : 8;
+    const int cap = lone_cap(B, num_chunks);
     int C = 1;
     while (C < cap && (long long)B * C * 2 <= 2LL * sms)
         C *= 2;

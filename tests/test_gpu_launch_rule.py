@@ -10,7 +10,7 @@ from tests.test_gpu_parity import sv  # noqa: F401
 gpu = pytest.mark.gpu
 
 # config -> (kernel, cluster size) on a 152-SM GB300
-EXPECTED = {1: (3, 2), 2: (2, 16), 3: (2, 8), 4: (3, 10), 5: (3, 4)}
+EXPECTED = {1: (3, 2), 2: (2, 8), 3: (2, 8), 4: (3, 10), 5: (3, 4)}
 
 
 @gpu
@@ -35,4 +35,6 @@ def test_sampler_cluster_for_long_rows(sv):
     C, ctas, _, kernel = sv.launch_shape(256, 0, 128256, "bf16")
     assert (C, ctas, kernel) == (4, 1024, 2)  # rows of >= 4096 chunks: at least 4 CTAs each
     C, _, _, _ = sv.launch_shape(64, 0, 32000, "bf16")
-    assert C == 4  # 2000 chunks: the one-wave rule alone (largest power of two with B*C <= 2*SMs)
+    assert C == 4  # 4000 chunks: the one-wave rule alone (largest power of two with B*C <= 2*SMs)
+    assert sv.launch_shape(1, 4, 128256, "bf16")[0] == 16  # one sequence, long rows: up to 16 CTAs
+    assert sv.launch_shape(1, 5, 32000, "bf16")[0] == 8  # shorter rows stop at 8
