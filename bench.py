@@ -227,6 +227,9 @@ def run_reference(args):
     per_seq = (time.perf_counter() - t0) / cal
     total_steps = args.steps + args.warmup
     per_step = max(1, min(batch.B, int(60.0 / max(total_steps, 1) / max(per_seq, 1e-6))))
+    # whole multiples of the thread count (the oracle runs one sequence per
+    # thread), so that no host core idles in a step
+    per_step = min(batch.B, max(cores, per_step // cores * cores))
     samples = [_slice(batch, (i * per_step) % batch.B, per_step) for i in range(4)]
     for i in range(args.warmup):
         oracle.verify_batch(samples[i % 4], diagnostics=False, nthreads=cores)
