@@ -1521,6 +1521,27 @@ __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const
     return r;
 }
 
+__device__ __forceinline__ i128 shfl_i128(i128 v, int src)
+{
+    const unsigned long long lo = __shfl_sync(0xffffffffu, (unsigned long long)v, src);
+    const long long hi = __shfl_sync(0xffffffffu, (long long)(v >> 64), src);
+    return (i128)(((u128)(unsigned long long)hi << 64) | lo);
+}
+
+// Inclusive scan of a signed 128-bit value over the warp's lanes.
+__device__ __forceinline__ i128 warp_scan_i128(i128 v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long lo = __shfl_up_sync(0xffffffffu, (unsigned long long)v, d);
+        const long long hi = __shfl_up_sync(0xffffffffu, (long long)(v >> 64), d);
+        if (lane >= d)
+            v += (i128)(((u128)(unsigned long long)hi << 64) | lo);
+    }
+    return v;
+}
+
 // Signed 128-bit value as a double (diagnostics only).
 __device__ __forceinline__ double i128_to_double(i128 v)
 {
@@ -1536,12 +1557,15 @@ __device__ __forceinline__ double i128_to_double(i128 v)
 // chunk per thread and pass; a block scan finds the chunk, its thread the id
 // from the running sums in id order.  All threads of the CTA call it.
 template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
-__device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, const T *trow, const T *drow,
-                                      const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0, int r1, i128 rel,
-                                      unsigned long long A, unsigned long long B, int32_t *outn)
+__device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2Smem &sm, const Seq &s, const T *trow,
+                                      const T *drow, const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0,
+                                      int r1, i128 rel, unsigned long long A, unsigned long long B, int32_t *outn)
 {
     constexpr int W = Elem<T>::W;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // per warp: slots 0 (target) and 1 (draft) stage the lanes' chunks, slot 2
+    // holds each lane's sums of exact weights (target, draft)
+    unsigned long long *hs = reinterpret_cast<unsigned long long *>(&sm.stage[wid][2][0]);
     i128 carry = 0;
     for (int base = r0; base < r1; base += kThreads) {
         const int c = base + tid;
@@ -1554,18 +1578,45 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, const Seq &s, c
             if (RESID)
                 dv = slice_chunk<T, ALIGNED, STAGED>(drow, dst, c, s);
             o = p2_chunk<T, RESID, FULL>(tv, dv, c, ps, runt, rund);
-            unsigned long long jt = to_fixed60(o.jt, ps.rt.sf), jd = RESID ? to_fixed60(o.jd, ps.rd.sf) : 0ull;
-            for (uint32_t hm = o.heavy; hm; hm &= hm - 1u) {
-                const int bit = __ffs(hm) - 1, e = bit & 7;
-                if (!((o.inj >> e) & 1u))
-                    continue;
-                if (bit >> 3)
-                    jd += exact_weight(elem<T>(dv, e), ps.rd);
-                else
-                    jt += exact_weight(elem<T>(tv, e), ps.rt);
+        }
+        // heavy ids in J: queued (slot, lane, element) and computed one per lane
+        uint32_t hj = o.heavy & (o.inj | (o.inj << 8));
+        hs[2 * lane] = 0ull;
+        hs[2 * lane + 1] = 0ull;
+        __syncwarp();
+        int queued = 0;
+        if (__any_sync(0xffffffffu, hj != 0)) {
+            sm.stage[wid][0][lane] = tv;
+            sm.stage[wid][1][lane] = dv;
+            const int cnt = __popc(hj);
+            int incl = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d)
+                    incl += y;
             }
+            int off = incl - cnt;
+            queued = __shfl_sync(0xffffffffu, incl, 31);
+            for (; hj; hj &= hj - 1u) {
+                const int bit = __ffs(hj) - 1;
+                sm.queue[wid][off++] = (unsigned short)((bit >> 3) | (lane << 3) | ((bit & 7) << 8));
+            }
+            __syncwarp();
+            for (int k = lane; k < queued; k += 32) {
+                const unsigned ent = sm.queue[wid][k];
+                const int row = ent & 1, src = (ent >> 3) & 31;
+                const float l = staged_elem<T>(&sm.stage[wid][row][src], (ent >> 8) & 7);
+                atomicAdd(&hs[2 * src + row], exact_weight(l, row ? ps.rd : ps.rt));
+            }
+        }
+        __syncwarp();
+        if (c < r1) {
+            const unsigned long long jt = to_fixed60(o.jt, ps.rt.sf) + hs[2 * lane];
+            const unsigned long long jd = RESID ? to_fixed60(o.jd, ps.rd.sf) + hs[2 * lane + 1] : 0ull;
             v = RESID ? p2_value(jt, jd, A, B) : (i128)jt;
         }
+        __syncwarp();
         i128 total;
         const i128 incl = block_scan_i128(v, total, scan_tmp);
         const int first = block_first(c < r1 && carry + incl > rel, wmin);
@@ -1642,7 +1693,7 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     unsigned long long A = 0, B = 1;
-    i128 R = 0;
+    i128 R = 0, vsrc = 0, isrc = 0;
     int att = 0;
     bool resid = false;
     for (;; ++att) {
@@ -1665,17 +1716,14 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
                 *cluster.map_shared_rank(&sh.p2recv[att][s.rank][tid], d) = v;
         }
         cluster_sync_all();
-        A = 0;
-        B = 0;
-        for (int src = 0; src < s.C; ++src) {
-            A += sh.p2recv[att][src][2];
-            B += sh.p2recv[att][src][3];
-        }
-        if (!resid)
-            B = 1;
-        R = 0;
-        for (int src = 0; src < s.C; ++src)
-            R += p2_value(sh.p2recv[att][src][0], resid ? sh.p2recv[att][src][1] : 0ull, A, B);
+        // lane k < C of every warp takes source rank k: row totals A, B, the
+        // ranks' values and their running sums (identical in every warp)
+        const bool src_lane = lane < s.C;
+        A = warp_sum_u64(src_lane ? sh.p2recv[att][lane][2] : 0ull);
+        B = resid ? warp_sum_u64(src_lane ? sh.p2recv[att][lane][3] : 0ull) : 1ull;
+        vsrc = src_lane ? p2_value(sh.p2recv[att][lane][0], resid ? sh.p2recv[att][lane][1] : 0ull, A, B) : (i128)0;
+        isrc = warp_scan_i128(vsrc);
+        R = shfl_i128(isrc, 31);
         if (R > 0 || att == 1)
             break;
         ps.mode = kP2Full;  // no mass: sample p of the target row
@@ -1688,39 +1736,29 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     if (R <= 0)
         return;  // nothing to draw from
     const i128 theta = scaled_floor128(u, R);  // the draw: first weight whose running sum passes theta
-    // the rank whose slice holds it
-    i128 before = 0;
-    int owner = s.C - 1;
-    for (int src = 0; src < s.C; ++src) {
-        const i128 v = p2_value(sh.p2recv[att][src][0], resid ? sh.p2recv[att][src][1] : 0ull, A, B);
-        if (theta < before + v) {
-            owner = src;
-            break;
-        }
-        before += v;
-    }
+    // the rank whose slice holds it: the first whose running sum passes theta
+    const unsigned hit_src = __ballot_sync(0xffffffffu, lane < s.C && isrc > theta);
+    const int owner = hit_src ? __ffs(hit_src) - 1 : s.C - 1;
     if (owner != s.rank)
         return;
-    // the warp range inside the slice
-    i128 rel = theta - before;
-    int w = kWarps - 1;
-    for (int k = 0; k < kWarps; ++k) {
-        const i128 v = p2_value(sh.p2w[k][0], resid ? sh.p2w[k][1] : 0ull, A, B);
-        if (rel < v) {
-            w = k;
-            break;
-        }
-        rel -= v;
-    }
+    // the warp range inside the slice, the same way over the warps' values
+    const i128 rel0 = theta - shfl_i128(isrc - vsrc, owner);
+    const i128 vw = lane < kWarps ? p2_value(sh.p2w[lane][0], resid ? sh.p2w[lane][1] : 0ull, A, B) : (i128)0;
+    const i128 iw = warp_scan_i128(vw);
+    const unsigned hit_w = __ballot_sync(0xffffffffu, lane < kWarps && iw > rel0);
+    const int w = hit_w ? __ffs(hit_w) - 1 : kWarps - 1;
+    const i128 rel = rel0 - shfl_i128(iw - vw, w);
     int r0, r1;
     warp_range(s, w, r0, r1);
     if (ONE_ROW)
-        p2_owner<T, ALIGNED, false, STAGED, true>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
+        p2_owner<T, ALIGNED, false, STAGED, true>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
                                                   outn);
     else if (resid)
-        p2_owner<T, ALIGNED, true, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
+        p2_owner<T, ALIGNED, true, STAGED>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
+                                           outn);
     else
-        p2_owner<T, ALIGNED, false, STAGED>(sh.p2scan, sh.cnt, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B, outn);
+        p2_owner<T, ALIGNED, false, STAGED>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
+                                            outn);
 }
 
 // Pass-2 weights of a chain sequence whose cut is n (sh.row holds the merged
