@@ -1554,8 +1554,11 @@ __device__ __forceinline__ double i128_to_double(i128 v)
 // The owner CTA's search inside warp range [r0, r1) of its slice, which holds
 // the draw (rel = theta - start of the range, on the exact grid).  The range is
 // recomputed chunk by chunk with the sweep's arithmetic (identical bits), one
-// chunk per thread and pass; a block scan finds the chunk, its thread the id
-// from the running sums in id order.  All threads of the CTA call it.
+// chunk per thread and pass; the exact weights of a warp's heavy ids in J are
+// queued and computed one per lane, then added to their chunks' sums with
+// shared-memory atomics (integer sums: any order gives the same bits).  A
+// block scan finds the chunk, and the warp holding it the id from the running
+// sums in id order.  All threads of the CTA call it.
 template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
 __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2Smem &sm, const Seq &s, const T *trow,
                                       const T *drow, const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0,
@@ -1678,7 +1681,9 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2Smem &sm, con
 // Pass 2 of one sequence across its cluster: the inverse-CDF draw with uniform
 // u from the weights ps describes, into *outn.  Every CTA sweeps its slice
 // (p2_sweep), the CTA totals cross the cluster over DSMEM, and the CTA whose
-// slice holds floor(u * R) searches one warp range of it.  A total R of 0 (a
+// slice holds floor(u * R) searches one warp range of it; the rank and the
+// warp range are found lane-parallel (one source per lane, a warp scan and a
+// ballot) in every warp alike.  A total R of 0 (a
 // residual with no mass, unreachable in exact arithmetic, or p without ids
 // that hold all of it) samples p instead.  mass_out (rank 0; may be NULL):
 // the normalised total (residual mass, or 1 - p(removed ids)).  All threads
