@@ -105,7 +105,10 @@ const void *kernel_for(spec_dtype dt, int kind, bool point)
 constexpr int kStagedDynMax = 200 * 1024;
 // Largest dynamic shared memory a kernel kind is launched with: the staged
 // early exit, or pass 2's staging area and queue.
-int kernel_dyn_smem(int kind) { return kind == kKindEarlyStaged ? kStagedDynMax : kP2SmemBytes; }
+int kernel_dyn_smem(int kind)
+{
+    return kind == kKindEarlyStaged ? kStagedDynMax : kind == kKindWide8 ? kP2SmemBytesWide : kP2SmemBytes;
+}
 int variant_slot(spec_dtype dt, int kind, bool point)
 {
     return ((dt == SPEC_BF16 ? 2 : 0) + (point ? 1 : 0)) * kKinds + kind;
@@ -485,7 +488,7 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;
     prm.out_path = nullptr;
-    size_t dyn = (size_t)kP2SmemBytes;
+    size_t dyn = (size_t)(shp.kind == kKindWide8 ? kP2SmemBytesWide : kP2SmemBytes);
     if (shp.kind == kKindEarlyStaged)
         dyn += (size_t)nslot * (size_t)slice * 16;
 

@@ -756,13 +756,19 @@ template <typename T> __device__ __forceinline__ float staged_elem(const uint4 *
 // Dynamic shared memory of pass 2: the chunks of one warp batch (kP2Slots
 // slots: kP2Unroll chunks of one row, or half as many of two) and the queue of
 // their heavy ids.
+// The small-grid full sweep (2 CTAs per SM, registers and shared memory to
+// spare) takes twice as many chunks per batch: fewer, longer trips where the
+// few resident warps leave latency exposed.
 constexpr int kP2Slots = kP2Unroll;
-static_assert(kP2Slots <= 8, "queue entries keep the slot in 3 bits");
-struct P2Smem {
-    uint4 stage[kWarps][kP2Slots][32];
-    unsigned short queue[kWarps][kP2Slots * 32 * 8];
+constexpr int kP2SlotsWide = 2 * kP2Unroll;
+template <int S> struct P2SmemT {
+    static_assert(S <= 8, "queue entries keep the slot in 3 bits");
+    uint4 stage[kWarps][S][32];
+    unsigned short queue[kWarps][S * 32 * 8];
 };
+using P2Smem = P2SmemT<kP2Slots>;
 constexpr int kP2SmemBytes = (int)sizeof(P2Smem);
+constexpr int kP2SmemBytesWide = (int)sizeof(P2SmemT<kP2SlotsWide>);
 
 typedef __int128 i128;
 typedef unsigned __int128 u128;
@@ -1435,11 +1441,11 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 // its heavy ids are queued (slot, lane, id, J) and spread over the lanes, 32
 // exact weights at a time, while the batch's chunks wait in shared memory.
 // All threads of the warp call it.
-template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
+template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false, int SLOTS = kP2Slots>
 __device__ __forceinline__ RangeSums p2_sweep(const Seq &s, const T *trow, const T *drow, const uint4 *tst,
-                                              const uint4 *dst, const P2Seq &ps, P2Smem &sm)
+                                              const uint4 *dst, const P2Seq &ps, P2SmemT<SLOTS> &sm)
 {
-    constexpr int U = RESID ? kP2Slots / 2 : kP2Slots;  // chunks per row in a batch
+    constexpr int U = RESID ? SLOTS / 2 : SLOTS;  // chunks per row in a batch
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int r0, r1;
     warp_range(s, wid, r0, r1);
@@ -1559,8 +1565,8 @@ __device__ __forceinline__ double i128_to_double(i128 v)
 // shared-memory atomics (integer sums: any order gives the same bits).  A
 // block scan finds the chunk, and the warp holding it the id from the running
 // sums in id order.  All threads of the CTA call it.
-template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false>
-__device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2Smem &sm, const Seq &s, const T *trow,
+template <typename T, bool ALIGNED, bool RESID, bool STAGED, bool FULL = false, int SLOTS = kP2Slots>
+__device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2SmemT<SLOTS> &sm, const Seq &s, const T *trow,
                                       const T *drow, const uint4 *tst, const uint4 *dst, const P2Seq &ps, int r0,
                                       int r1, i128 rel, unsigned long long A, unsigned long long B, int32_t *outn)
 {
@@ -1688,13 +1694,13 @@ __device__ __noinline__ void p2_owner(i128 *scan_tmp, int *wmin, P2Smem &sm, con
 // that hold all of it) samples p instead.  mass_out (rank 0; may be NULL):
 // the normalised total (residual mass, or 1 - p(removed ids)).  All threads
 // of every CTA of the cluster call it.
-template <typename T, bool ALIGNED, bool STAGED, bool ONE_ROW = false>
+template <typename T, bool ALIGNED, bool STAGED, bool ONE_ROW = false, int SLOTS = kP2Slots>
 __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T *trow, const T *drow,
                                           const uint4 *tst, const uint4 *dst, P2Seq ps, float u, int32_t *outn,
                                           float *mass_out)
 {
     extern __shared__ __align__(16) unsigned char dyn_smem[];
-    P2Smem &sm = *reinterpret_cast<P2Smem *>(dyn_smem);
+    P2SmemT<SLOTS> &sm = *reinterpret_cast<P2SmemT<SLOTS> *>(dyn_smem);
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     unsigned long long A = 0, B = 1;
@@ -1703,9 +1709,9 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     bool resid = false;
     for (;; ++att) {
         resid = ps.mode == kP2Residual;
-        const RangeSums r = ONE_ROW ? p2_sweep<T, ALIGNED, false, STAGED, true>(s, trow, drow, tst, dst, ps, sm)
-                            : resid   ? p2_sweep<T, ALIGNED, true, STAGED>(s, trow, drow, tst, dst, ps, sm)
-                                      : p2_sweep<T, ALIGNED, false, STAGED>(s, trow, drow, tst, dst, ps, sm);
+        const RangeSums r = ONE_ROW ? p2_sweep<T, ALIGNED, false, STAGED, true, SLOTS>(s, trow, drow, tst, dst, ps, sm)
+                            : resid ? p2_sweep<T, ALIGNED, true, STAGED, false, SLOTS>(s, trow, drow, tst, dst, ps, sm)
+                                    : p2_sweep<T, ALIGNED, false, STAGED, false, SLOTS>(s, trow, drow, tst, dst, ps, sm);
         if (lane == 0) {
             sh.p2w[wid][0] = r.jt;
             sh.p2w[wid][1] = r.jd;
@@ -1756,14 +1762,14 @@ __device__ __noinline__ void pass2_sample(SharedState &sh, const Seq &s, const T
     int r0, r1;
     warp_range(s, w, r0, r1);
     if (ONE_ROW)
-        p2_owner<T, ALIGNED, false, STAGED, true>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
-                                                  outn);
+        p2_owner<T, ALIGNED, false, STAGED, true, SLOTS>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel,
+                                                         A, B, outn);
     else if (resid)
-        p2_owner<T, ALIGNED, true, STAGED>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
-                                           outn);
+        p2_owner<T, ALIGNED, true, STAGED, false, SLOTS>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel,
+                                                         A, B, outn);
     else
-        p2_owner<T, ALIGNED, false, STAGED>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1, rel, A, B,
-                                            outn);
+        p2_owner<T, ALIGNED, false, STAGED, false, SLOTS>(sh.p2scan, sh.cnt, sm, s, trow, drow, tst, dst, ps, r0, r1,
+                                                          rel, A, B, outn);
 }
 
 // Pass-2 weights of a chain sequence whose cut is n (sh.row holds the merged
@@ -1791,7 +1797,7 @@ __device__ __forceinline__ P2Seq chain_p2seq(const SharedState &sh, const Seq &s
 // across its cluster.  STAGED: tst and dst hold this CTA's slices of rows t_n
 // and d_n (early exit with rows in host memory), so pass 2 reads neither row
 // again.
-template <typename T, bool ALIGNED, bool POINT, bool STAGED = false>
+template <typename T, bool ALIGNED, bool POINT, bool STAGED = false, int SLOTS = kP2Slots>
 __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, const Seq &s, int n,
                                             const uint4 *tst = nullptr, const uint4 *dst = nullptr)
 {
@@ -1809,10 +1815,11 @@ __device__ __forceinline__ void chain_pass2(const Params &p, SharedState &sh, co
     // 53.4 against 56.9 us; folding the specialisation into the shared function
     // cost the verify kernels 1-2 us).
     if (POINT && s.gmax == 0)
-        pass2_sample<T, ALIGNED, STAGED, true>(sh, s, trow, drow, tst, tst, ps, final_uniform(p, s), outn, mass);
+        pass2_sample<T, ALIGNED, STAGED, true, SLOTS>(sh, s, trow, drow, tst, tst, ps, final_uniform(p, s), outn,
+                                                      mass);
     else
-        pass2_sample<T, ALIGNED, STAGED>(sh, s, trow, drow, tst, rows ? dst : tst, ps, final_uniform(p, s), outn,
-                                         mass);
+        pass2_sample<T, ALIGNED, STAGED, false, SLOTS>(sh, s, trow, drow, tst, rows ? dst : tst, ps,
+                                                       final_uniform(p, s), outn, mass);
 }
 
 // ===========================================================================
@@ -1864,7 +1871,7 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     exchange_rows(sh, s, nrows);
     if (!decide_and_write<T>(p, sh, s, gt))
         return;  // uniform over the cluster; no DSMEM access follows
-    chain_pass2<T, ALIGNED, POINT>(p, sh, s, sh.n);
+    chain_pass2<T, ALIGNED, POINT, false, KB == 8 ? kP2SlotsWide : kP2Slots>(p, sh, s, sh.n);
 }
 
 // ===========================================================================
