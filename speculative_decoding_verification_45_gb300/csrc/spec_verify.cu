@@ -482,8 +482,8 @@ spec_status run(const void *target, const void *draft, const int32_t *tokens, co
     // two-rows-per-trip variant, 1 for the staged early exit) skips it and its
     // prologue.
     const long long slots = (long long)shp.sms * (shp.kind == kKindEarlyStaged ? 1 : shp.kind == kKindWide8 ? 2 : 4);
-    // (one row per sequence: every cost is equal, so the order is the identity)
-    prm.ordered = (gmax > 0 && B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
+    // (in a one-row call the sampled rows, which draw exactly, go first)
+    prm.ordered = (B <= kMaxOrdered && (long long)B * shp.C > slots) ? 1 : 0;
     prm.counters = opt ? reinterpret_cast<unsigned long long *>(opt->counters) : nullptr;
     prm.hist = opt ? reinterpret_cast<unsigned long long *>(opt->accept_hist) : nullptr;
     prm.parent = nullptr;

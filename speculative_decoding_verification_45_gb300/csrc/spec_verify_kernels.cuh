@@ -1179,13 +1179,17 @@ __device__ __forceinline__ float final_uniform(const Params &p, const Seq &s)
 }
 
 
-// Number of rows sequence i reads: g + 1 target rows, plus g draft rows when
-// sampled; 0 for an invalid draft count.
+// Cost of sequence i for the longest-first order: the rows it reads, g + 1
+// target rows plus, when sampled, g draft rows; 0 for an invalid draft count.
+// With point-mass proposals no draft row exists and a sampled sequence counts
+// one row more for its final draw, which sweeps a row again: in a one-row call
+// (gamma_max = 0) that puts the sampled rows before the greedy ones.
+template <bool POINT>
 __device__ __forceinline__ int seq_cost(const Params &p, int g, float temp)
 {
     if (g < 0 || g > p.gmax)
         return 0;
-    return g + 1 + (temp > 0.0f ? g : 0);
+    return g + 1 + (temp > 0.0f ? (POINT ? 1 : g) : 0);
 }
 
 struct SeqPick {
@@ -1198,7 +1202,10 @@ struct SeqPick {
 // order of decreasing row count (ties by index), so the longest start first and
 // the grid's tail is made of short ones; the block scheduler dispatches
 // clusters in index order.  Every CTA of the cluster computes the same value.
-// All threads of the CTA call it (blockDim.x >= kThreads).
+// All threads of the CTA call it (blockDim.x >= kThreads).  The point-mass
+// kernels, where batches of equal cost are common (one-row calls at one
+// temperature), stop once the histogram shows a single bin.
+template <bool POINT>
 __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
 {
     if (!p.ordered)
@@ -1214,7 +1221,12 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
         const bool in = active && i < p.B;
         gv[e] = (in && p.num_draft) ? p.num_draft[i] : 0;
         tv[e] = in ? p.temperature[i] : 0.0f;
-        cost[e] = in ? seq_cost(p, gv[e], tv[e]) : -1;
+        cost[e] = in ? seq_cost<POINT>(p, gv[e], tv[e]) : -1;
+        if (POINT && in && i == k) {  // the answer when every sequence costs the same
+            sh.seq = k;
+            sh.seq_g = gv[e];
+            sh.seq_temp = tv[e];
+        }
     }
     if (tid <= kMaxRows)
         sh.hist[tid] = 0;
@@ -1245,12 +1257,14 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
         const int inc = __shfl_sync(0xffffffffu, j < 32 ? inc0 : inc1, src);
         const int h = __shfl_sync(0xffffffffu, j < 32 ? h0 : h1, src);
         if (tid == 0) {
-            sh.bin = kMaxRows - j;
+            sh.bin = POINT && h == p.B ? -1 : kMaxRows - j;  // one bin: cluster k takes sequence k
             sh.rank_in_bin = k - (inc - h);
         }
     }
     __syncthreads();
     const int bin = sh.bin, want = sh.rank_in_bin;
+    if (POINT && bin < 0)
+        return SeqPick{sh.seq, sh.seq_g, sh.seq_temp};
     int mine = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
@@ -1836,7 +1850,7 @@ __global__ void __launch_bounds__(kThreads, KB == 8 ? 2 : 4) spec_verify_stream_
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const SeqPick pick = seq_for_cluster<POINT>(p, sh, (int)(blockIdx.x / (unsigned)C));
     const int b = pick.b, g = pick.g;
     const float temp = pick.temp;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -1896,7 +1910,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_verify_early_kernel(const Pa
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const SeqPick pick = seq_for_cluster(p, sh, (int)(blockIdx.x / (unsigned)C));
+    const SeqPick pick = seq_for_cluster<POINT>(p, sh, (int)(blockIdx.x / (unsigned)C));
     const int b = pick.b, g = pick.g;
     const float temp = pick.temp;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;

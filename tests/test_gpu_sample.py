@@ -121,3 +121,34 @@ def test_sample_random_rows(sv, oracle_mod, seed):
     rep = parity.compare(batch, out, np.zeros(batch.B, np.int32), ref)
     assert rep.mismatches_far == 0, rep.far_detail[:3]
     assert int(status.item()) == int(np.bitwise_or.reduce(ref.seq_status))
+
+
+@gpu
+@pytest.mark.parametrize("mix", ["greedy", "sampled", "scattered", "invalid"])
+def test_sample_row_order_matches_oracle(sv, oracle_mod, mix):
+    """768 rows of 128256 ids fill more than one wave of clusters, so rows are
+    handed out by cost, sampled rows first (they also draw from the row): one
+    bin (every row greedy or every row sampled), the two kinds scattered over
+    the batch at random, and some rows with an invalid temperature.  Each row's
+    token must not depend on the order in which clusters took the rows."""
+    import torch
+
+    big = workloads.make_config(5)
+    rows = np.concatenate([big.target[:, 0]] * 3)
+    B = rows.shape[0]
+    rng = np.random.default_rng(102)
+    temps = {"greedy": np.zeros(B), "sampled": np.ones(B),
+             "scattered": (rng.random(B) < 0.3).astype(np.float64),
+             "invalid": np.where(rng.random(B) < 0.1, -1.0, (rng.random(B) < 0.5).astype(np.float64))}[mix]
+    batch = _as_round(rows, rng.random(B).astype(np.float32), temps.astype(np.float32), big.dtype)
+    ref = oracle_mod.verify_batch(batch)
+    dev = sv.to_device(batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = sv.sample(dev["target_logits"][:, 0].contiguous(), dev["uniforms"][:, 0].contiguous(),
+                    dev["temperature"], status=status)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    out = np.stack([got, np.zeros_like(got)], 1)[:, :1]
+    rep = parity.compare(batch, out, np.zeros(batch.B, np.int32), ref)
+    assert rep.mismatches_far == 0, rep.far_detail[:3]
+    assert int(status.item()) == int(np.bitwise_or.reduce(ref.seq_status))
