@@ -1204,7 +1204,7 @@ struct SeqPick {
 // clusters in index order.  Every CTA of the cluster computes the same value.
 // All threads of the CTA call it (blockDim.x >= kThreads).  The point-mass
 // kernels, where batches of equal cost are common (one-row calls at one
-// temperature), stop once the histogram shows a single bin.
+// temperature), first test with one barrier whether every cost is the same.
 template <bool POINT>
 __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
 {
@@ -1222,15 +1222,24 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
         gv[e] = (in && p.num_draft) ? p.num_draft[i] : 0;
         tv[e] = in ? p.temperature[i] : 0.0f;
         cost[e] = in ? seq_cost<POINT>(p, gv[e], tv[e]) : -1;
-        if (POINT && in && i == k) {  // the answer when every sequence costs the same
-            sh.seq = k;
-            sh.seq_g = gv[e];
-            sh.seq_temp = tv[e];
-        }
     }
     if (tid <= kMaxRows)
         sh.hist[tid] = 0;
-    __syncthreads();
+    if constexpr (POINT) {
+        // one cost for every sequence: cluster k takes sequence k (loads issued
+        // before the barrier, used only then)
+        const int gk = p.num_draft ? p.num_draft[k] : 0;
+        const float tk = p.temperature[k];
+        const int c0 = seq_cost<POINT>(p, p.num_draft ? p.num_draft[0] : 0, p.temperature[0]);
+        bool same = true;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            same = same && (cost[e] < 0 || cost[e] == c0);
+        if (__syncthreads_and(same))
+            return SeqPick{k, gk, tk};
+    } else {
+        __syncthreads();
+    }
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
         if (cost[e] >= 0)
@@ -1257,14 +1266,12 @@ __device__ SeqPick seq_for_cluster(const Params &p, SharedState &sh, int k)
         const int inc = __shfl_sync(0xffffffffu, j < 32 ? inc0 : inc1, src);
         const int h = __shfl_sync(0xffffffffu, j < 32 ? h0 : h1, src);
         if (tid == 0) {
-            sh.bin = POINT && h == p.B ? -1 : kMaxRows - j;  // one bin: cluster k takes sequence k
+            sh.bin = kMaxRows - j;
             sh.rank_in_bin = k - (inc - h);
         }
     }
     __syncthreads();
     const int bin = sh.bin, want = sh.rank_in_bin;
-    if (POINT && bin < 0)
-        return SeqPick{sh.seq, sh.seq_g, sh.seq_temp};
     int mine = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
